@@ -1,0 +1,187 @@
+"""CPU oracle for the half-precision GEMM C = A.B -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The CUDA
+library never loads it and shares no code with it.
+
+The arithmetic lives in ``hgemm_oracle.c`` (plain C, fp64, k ascending), built
+into ``liboracle.so`` by :func:`build`.  This module only marshals numpy
+arrays of raw 16-bit patterns into it, and states the acceptance measure:
+
+* ``Cref = sum_k dec(A[i,k]) * dec(B[k,j])`` and
+  ``Den = sum_k |dec(A[i,k])| * |dec(B[k,j])|`` -- the matrix product with both
+  operands row-major ("hgemm_mma_m16n8k16_mma2x4_warp4x4_kernel", section 1.1)
+  accumulated wider than the inputs ("tensor-cores-cutlass-and-cute",
+  section 四.1, and the "post_1787550000" experiment, section 3: wide
+  accumulation is the floor);
+* the normalised error ``max |C - Cref| / Den`` (entries with ``Den == 0``
+  must be exactly zero).
+
+Parity is pinned in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hgemm_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F16, BF16 = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compiles ``hgemm_oracle.c`` with the host C compiler; returns the path."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+             "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, p = ctypes.c_int64, ctypes.c_void_p
+            lib.oracle_gemm.argtypes = [p, p, ctypes.c_int, i64, i64, i64, i64, i64,
+                                        i64, i64, i64, p, p, ctypes.c_int]
+            lib.oracle_gemm.restype = ctypes.c_int
+            lib.oracle_gemm_entries.argtypes = [p, p, ctypes.c_int, i64, i64, i64, i64, i64,
+                                                i64, p, p, p, p, p]
+            lib.oracle_gemm_entries.restype = ctypes.c_int
+            lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
+            lib.oracle_decode_f16.restype = ctypes.c_double
+            lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
+            lib.oracle_decode_bf16.restype = ctypes.c_double
+            lib.oracle_decode_array.argtypes = [p, ctypes.c_int, i64, p]
+            lib.oracle_decode_array.restype = None
+            _lib = lib
+    return _lib
+
+
+def _u16(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint16:
+        raise TypeError("oracle inputs are raw 16-bit patterns (numpy uint16)")
+    return x
+
+
+def _ptr(x: np.ndarray) -> int:
+    return x.ctypes.data
+
+
+def gemm(A: np.ndarray, B: np.ndarray, dtype_in: int, M: int, N: int, K: int,
+         lda: int, ldb: int, batch: int = 1, strideA: int = 0, strideB: int = 0,
+         threads: int | None = None):
+    """Full product.  ``A``/``B`` are flat uint16 buffers read with the given
+    leading dimensions and batch strides (in elements).  Returns ``(Cref, Den)``
+    as fp64 arrays of shape ``(batch, M, N)``."""
+    lib = _load()
+    A, B = _u16(A), _u16(B)
+    _check_extent(A, M, K, lda, batch, strideA)
+    _check_extent(B, K, N, ldb, batch, strideB)
+    Cref = np.empty((batch, M, N), dtype=np.float64)
+    Den = np.empty((batch, M, N), dtype=np.float64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = lib.oracle_gemm(_ptr(A), _ptr(B), dtype_in, M, N, K, lda, ldb, batch,
+                         strideA, strideB, _ptr(Cref), _ptr(Den), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_gemm rejected its arguments")
+    return Cref, Den
+
+
+def gemm_entries(A: np.ndarray, B: np.ndarray, dtype_in: int, K: int, lda: int, ldb: int,
+                 eb, ei, ej, strideA: int = 0, strideB: int = 0):
+    """The same definition for the entries ``(eb[e], ei[e], ej[e])`` only."""
+    lib = _load()
+    A, B = _u16(A), _u16(B)
+    eb = np.ascontiguousarray(eb, dtype=np.int64)
+    ei = np.ascontiguousarray(ei, dtype=np.int64)
+    ej = np.ascontiguousarray(ej, dtype=np.int64)
+    n = eb.size
+    if not (ei.size == n and ej.size == n):
+        raise ValueError("entry index arrays differ in length")
+    if n:
+        # every element the sums touch must lie inside the buffers
+        amax = int(eb.max()) * strideA + int(ei.max()) * lda + max(K - 1, 0)
+        bmax = int(eb.max()) * strideB + max(K - 1, 0) * ldb + int(ej.max())
+        if K > 0 and (amax >= A.size or bmax >= B.size):
+            raise ValueError("entry indices reach outside the operand buffers")
+    Cref = np.empty(n, dtype=np.float64)
+    Den = np.empty(n, dtype=np.float64)
+    rc = lib.oracle_gemm_entries(_ptr(A), _ptr(B), dtype_in, K, lda, ldb, strideA, strideB,
+                                 n, _ptr(eb), _ptr(ei), _ptr(ej), _ptr(Cref), _ptr(Den))
+    if rc != 0:
+        raise ValueError("oracle_gemm_entries rejected its arguments")
+    return Cref, Den
+
+
+def decode(bits: np.ndarray, dtype: int) -> np.ndarray:
+    """Reads raw fp16 (dtype 0) or bf16 (dtype 1) patterns with the oracle's
+    own decoder; returns fp64 of the same shape."""
+    lib = _load()
+    bits = _u16(bits)
+    out = np.empty(bits.shape, dtype=np.float64)
+    lib.oracle_decode_array(_ptr(bits), int(dtype), bits.size, _ptr(out))
+    return out
+
+
+def decode_one(h: int, dtype: int) -> float:
+    lib = _load()
+    return lib.oracle_decode_f16(h) if dtype == F16 else lib.oracle_decode_bf16(h)
+
+
+def normalized_error(C: np.ndarray, Cref: np.ndarray, Den: np.ndarray) -> float:
+    """``max |C - Cref| / Den`` over entries with ``Den > 0``; an entry with
+    ``Den == 0`` (an empty sum or a zero row/column) that is not exactly zero
+    counts as an infinite error, and a NaN anywhere in C where Cref is finite
+    does too."""
+    C = np.asarray(C, dtype=np.float64)
+    if C.shape != Cref.shape:
+        raise ValueError(f"shape mismatch {C.shape} vs {Cref.shape}")
+    if C.size == 0:
+        return 0.0
+    bad_nan = np.isnan(C) & ~np.isnan(Cref)
+    if bad_nan.any():
+        return float("inf")
+    zero = Den == 0
+    if (C[zero] != 0).any():
+        return float("inf")
+    nz = ~zero
+    if not nz.any():
+        return 0.0
+    return float(np.max(np.abs(C[nz] - Cref[nz]) / Den[nz]))
+
+
+def flops(M: int, N: int, K: int, batch: int = 1) -> int:
+    """2*M*N*K per product: one multiply and one add per term
+    ("tensor-cores-cutlass-and-cute", section 四.1)."""
+    return 2 * M * N * K * batch
+
+
+def min_bytes(M: int, N: int, K: int, in_bytes: int, out_bytes: int, batch: int = 1) -> int:
+    """Each of A, B read once and C written once
+    ("tensor-cores-cutlass-and-cute", section 四.1)."""
+    return batch * (M * K * in_bytes + K * N * in_bytes + M * N * out_bytes)
+
+
+def _check_extent(X: np.ndarray, rows: int, cols: int, ld: int, batch: int, stride: int):
+    if rows == 0 or cols == 0:
+        return
+    if ld < cols:
+        raise ValueError("leading dimension shorter than a row")
+    last = (batch - 1) * stride + (rows - 1) * ld + cols - 1
+    if last >= X.size:
+        raise ValueError("operand buffer too small for its shape")
