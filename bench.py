@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of libhgemm on the GEMM workloads; prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload square4096|square8192|batched_qk|ragged4095|
+                                ragged4095_h|skinny|int512]
+
+A step is one product C = A.B of the workload (every step of the hot path:
+operand copies when an operand is misaligned, the tensor-core kernel and its
+epilogue), with inputs already resident in HBM.  The default workload is the
+4096^3 bf16 GEMM (N(0,1) inputs, seed 1, bf16 out), the configuration the
+metric is quoted on.
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and ``torch.cuda.synchronize()``; CUDA events on the launching stream time the
+whole region and every launch.  L2 is defeated by rotating enough copies of
+the inputs and outputs that the working set exceeds twice the L2 size.
+Clocks and throttle reasons are sampled with nvidia-smi while the GPU is under
+load (the timed region, extended by an untimed probe loop when the region is
+shorter than the sampling period).
+
+Multi-GPU: the product does not shard in this library (every box runs one
+GPU), so ``--gpus N`` under torchrun runs N independent replicas; ``value`` is
+the FLOPs of all ranks divided by the slowest rank's time.
+
+``--impl reference`` times the CPU oracle (the only other implementation of
+the method) on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense fp16/bf16 tensor peak (or % HBM BW)"
+NOMINAL_TC_TFLOPS = 2250.0   # dense fp16/bf16 per GPU, nominal
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 2**20
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="square4096")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16": d["bf16_tflops"], "bf16_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "hbm": d["hbm_gbs"], "source": "measured"}
+    except Exception:
+        return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float, device) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        sm, smax, reasons = [], [], set()
+        for ts, line in self.lines:
+            if ts < t0 or ts > t1:
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "tensor_core_dense_swizzled_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch of the main kernel from a committed ncu capture,
+    or None when absent or taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_hash") == kernel_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def workload_numbers(w):
+    import oracle  # only for the FLOP / byte formulas used in the report
+    flops = oracle.flops(w.M, w.N, w.K, w.batch)
+    ob = 4 if w.dtype_out == "f32" else 2
+    nbytes = oracle.min_bytes(w.M, w.N, w.K, 2, ob, w.batch)
+    return flops, nbytes, ob
+
+
+def flops_of(w):
+    return 2 * w.M * w.N * w.K * w.batch
+
+
+def min_bytes_of(w):
+    ob = 4 if w.dtype_out == "f32" else 2
+    return w.batch * (w.M * w.K * 2 + w.K * w.N * 2 + w.M * w.N * ob), ob
+
+
+def roofline_bound(w) -> str:
+    fl = flops_of(w)
+    by, _ = min_bytes_of(w)
+    ridge = NOMINAL_TC_TFLOPS * 1e12 / (NOMINAL_HBM_GBS * 1e9)
+    return "tensor" if fl / by > ridge else "hbm"
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_rows_time(w, A_bits, B_bits, rows: int, threads: int) -> float:
+    import oracle
+    din = 0 if w.dtype_in == "f16" else 1
+    t0 = time.perf_counter()
+    oracle.gemm(A_bits[: max(1, rows * w.lda)], B_bits[: (w.K - 1) * w.ldb + w.N] if w.batch == 1 else B_bits,
+                din, rows, w.N, w.K, w.lda, w.ldb, 1, 0, 0, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_inputs(w):
+    import numpy as np
+    import torch
+
+    from tensor_core_dense_swizzled_gb300 import inputs
+    A, B = inputs.make_inputs(w)
+    ab = A.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    bb = B.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    return ab, bb
+
+
+def cpu_baseline(w, target_s: float = 12.0):
+    """Times the oracle, as it stands, on the host cores on whole rows of C of
+    batch 0 (a bounded sample of the workload); returns the cpu_baseline dict."""
+    ab, bb = cpu_inputs(w)
+    threads = os.cpu_count() or 1
+    rows = min(w.M, threads)
+    t = oracle_rows_time(w, ab, bb, rows, threads)
+    per_row = t / rows
+    rows = int(max(threads, min(w.M, math.floor(target_s / max(per_row, 1e-9) / threads) * threads)))
+    rows = min(rows, w.M)
+    t = oracle_rows_time(w, ab, bb, rows, threads)
+    fl = 2 * rows * w.N * w.K
+    return {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": min(threads, rows), "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of C (batch 0) of {w.name}: {rows}x{w.N}x{w.K}, "
+                      f"fp64 triple loop, {t:.1f} s"}
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return 0
+    ab, bb = cpu_inputs(w)
+    threads = os.cpu_count() or 1
+    # size each step so that warm-up + timed steps take about 90 s in total
+    t1 = oracle_rows_time(w, ab, bb, min(w.M, threads), threads) / min(w.M, threads) * threads
+    per_step_budget = 90.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(w.M, math.floor(per_step_budget / max(t1 / threads, 1e-9)))))
+    for _ in range(args.warmup):
+        oracle_rows_time(w, ab, bb, rows, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_rows_time(w, ab, bb, rows, threads)
+    dt = time.perf_counter() - t0
+    fl = 2 * rows * w.N * w.K * args.steps
+    value = fl / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": min(threads, rows), "kind": "oracle",
+                         "sample": f"each step: rows 0..{rows - 1} of C of {w.name} ({rows}x{w.N}x{w.K})"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, world, extra=None):
+    c = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "dtype_in": w.dtype_in,
+         "dtype_out": w.dtype_out, "seed": w.seed, "parallelism": "replicas" if world > 1 else "single",
+         "layout": "A MxK, B KxN, C MxN row-major"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args, w, world, rank, local, pg):
+    import torch
+
+    import __graft_entry__
+    from tensor_core_dense_swizzled_gb300 import hgemm as H
+    from tensor_core_dense_swizzled_gb300 import inputs
+
+    __graft_entry__.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    DT = {"f16": H.HGEMM_F16, "bf16": H.HGEMM_BF16, "f32": H.HGEMM_F32}
+    TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    A, B = inputs.make_inputs(w)
+    flops = flops_of(w)
+    min_bytes, ob = min_bytes_of(w)
+    set_bytes = A.numel() * 2 + B.numel() * 2 + w.batch * w.M * w.N * ob
+    nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes))
+    shape_c = (w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N)
+    sets, plans = [], []
+    for _ in range(nsets):
+        sets.append((A.to(dev), B.to(dev), torch.empty(shape_c, dtype=TD[w.dtype_out], device=dev)))
+        plans.append(H.hgemm_plan_create(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, w.batch, w.strideA,
+                                         w.strideB, w.strideC, DT[w.dtype_in], DT[w.dtype_out]))
+    info = H.hgemm_plan_get_info(plans[0])
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        a, b, c = sets[i % nsets]
+        H.hgemm_run(plans[i % nsets], a, b, c, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    st = H.hgemm_check(plans[0], stream)
+    if st != 0:
+        raise RuntimeError(f"warm-up failed: {H.STATUS.get(st)} {H.hgemm_last_error_detail()}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)  # let nvidia-smi come up
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    t_wall1 = time.time()
+    region_ms = starts[0].elapsed_time(ends[-1])
+    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    # keep the GPU busy (untimed) long enough for the clock sampler to see it
+    probe_until = t_wall0 + 1.0
+    j = 0
+    while time.time() < probe_until:
+        for _ in range(50):
+            step(j)
+            j += 1
+        torch.cuda.synchronize(dev)
+    t_wall2 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0 - 0.05, max(t_wall1, t_wall2) + 0.05)
+    clocks["window"] = "timed" if t_wall1 - t_wall0 >= 1.0 else "timed+probe"
+    st = H.hgemm_check(plans[0], stream)
+    if st != 0:
+        raise RuntimeError(f"timed run failed: {H.STATUS.get(st)} {H.hgemm_last_error_detail()}")
+
+    region_ms = max_over_ranks(pg, region_ms, dev)
+    value = flops * args.steps * world / (region_ms * 1e-3) / 1e12
+    avg_launch_ms = statistics.mean(per_launch)
+    bound = roofline_bound(w)
+    peaks = load_peaks()
+    sustained = region_ms > 1000.0
+    if bound == "tensor":
+        achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+        peak = peaks["bf16_sustained"] if sustained else peaks["bf16"]
+        unit = "TFLOP/s"
+        peak_kind = ("sustained" if sustained else "burst") + f" bf16, {peaks['source']}"
+    else:
+        achieved = min_bytes / (avg_launch_ms * 1e-3) / 1e9
+        peak = peaks["hbm"]
+        unit = "GB/s"
+        peak_kind = f"copy bandwidth, {peaks['source']}"
+    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": committed_traffic(w.name), "peak_kind": peak_kind,
+            "algorithmic_per_launch": flops if bound == "tensor" else min_bytes,
+            "launch_ms": avg_launch_ms, "kernels_per_launch": info["kernels_per_run"]}
+
+    # end to end through the C ABI with host buffers (copies inside the timed region)
+    e2e = None
+    if args.e2e_steps > 0:
+        Ah = A.pin_memory()
+        Bh = B.pin_memory()
+        Ch = torch.empty(shape_c, dtype=TD[w.dtype_out]).pin_memory()
+        H.hgemm_run_host(plans[0], Ah, Bh, Ch, stream)  # allocates the staging buffers
+        barrier(pg)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            H.hgemm_run_host(plans[0], Ah, Bh, Ch, stream)
+        dt = time.perf_counter() - t0
+        dt = max_over_ranks(pg, dt, dev)
+        e2e = {"value": flops * args.e2e_steps * world / dt / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": A.numel() * 2 + B.numel() * 2,
+               "d2h_bytes_per_step": w.batch * w.M * w.N * ob, "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    for p in plans:
+        H.hgemm_plan_destroy(p)
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype_in, "data": "synthetic",
+        "config": config_of(w, world, {
+            "l2": f"{nsets} rotating input/output sets ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)",
+            "path": {2: "tiled", 3: "skinny", 1: "zero_fill", 0: "empty"}[info["path"]],
+            "tile": [info["tile_m"], info["tile_n"], info["tile_k"]], "stages": info["stages"],
+            "split_k": info["split_k"], "grid": info["grid"]}),
+        "pct_nominal_tensor_peak": 100.0 * value / world / NOMINAL_TC_TFLOPS,
+        "pct_nominal_hbm": 100.0 * (min_bytes * args.steps / (region_ms * 1e-3) / 1e9) / NOMINAL_HBM_GBS,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * info["kernels_per_run"],
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    from tensor_core_dense_swizzled_gb300 import inputs
+    if args.workload not in inputs.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(inputs.WORKLOADS)}")
+    w = inputs.WORKLOADS[args.workload]
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    world, rank, local, pg = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, rank, world)
+        return run_ours(args, w, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,178 @@
+/*
+ * hgemm.h -- C ABI of libhgemm: half-precision tensor-core GEMM on GB300
+ * (sm_103a).
+ *
+ * The operation (defined in "hgemm_mma_m16n8k16_mma2x4_warp4x4_kernel",
+ * section 1.1: C = A x B with A[M x K] and B[K x N] both row-major, C row-major;
+ * fp32 accumulation as in "tensor-cores-cutlass-and-cute", section 四.1):
+ *
+ *     C_b[i][j] = sum_{k<K} A_b[i][k] * B_b[k][j]      for b < batch
+ *
+ * with fp16 or bf16 inputs, fp32 accumulation, and fp32, fp16 or bf16
+ * output (fp32 -> fp16/bf16 rounds to nearest even).  Element (i,k) of A_b is at
+ * A + b*strideA + i*lda + k, element (k,j) of B_b at B + b*strideB + k*ldb + j,
+ * and element (i,j) of C_b at C + b*strideC + i*ldc + j.  All leading
+ * dimensions and strides count elements, not bytes.  C is overwritten (no
+ * alpha/beta).  The argument checks follow the host wrapper of the
+ * "tensor-cores-cutlass-and-cute" Ampere kernel (section 四.4): a bad dtype or
+ * shape is refused, never reinterpreted.
+ *
+ * Ownership.  The caller owns A, B, C and the stream.  A plan owns its device
+ * workspace (error word, split-K partials, aligned copies of misaligned
+ * operands) and its cached TMA descriptors; hgemm_plan_destroy frees them.
+ * A plan is bound to the CUDA device that is current when it is created, and
+ * one plan must not run on two streams at once (its workspace is shared).
+ *
+ * Errors.  Every entry point returns a status and never aborts, exits or
+ * prints.  hgemm_last_error_detail() gives a message for the calling thread's
+ * last failure.  Kernel launches are asynchronous: a device-side watchdog
+ * timeout surfaces at hgemm_check().
+ *
+ * Alignment.  Pointers must be element-aligned.  When a base pointer is
+ * 16-byte aligned and its leading dimension and batch stride are multiples of
+ * 16 bytes, the operand is read by TMA in place; otherwise it is first copied
+ * into an aligned workspace buffer.  A misaligned C is written with
+ * predicated stores instead of TMA stores.  Nothing is refused for alignment.
+ */
+#ifndef HGEMM_H
+#define HGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HGEMM_F16 = 0,  /* IEEE binary16 */
+    HGEMM_BF16 = 1, /* bfloat16 */
+    HGEMM_F32 = 2   /* IEEE binary32 (output only) */
+} hgemm_dtype_t;
+
+typedef enum {
+    HGEMM_OK = 0,
+    HGEMM_ERR_INVALID_ARG = 1, /* null pointer with work to do, negative size, ld too short, bad dtype */
+    HGEMM_ERR_UNSUPPORTED = 2, /* well-formed request this build does not implement */
+    HGEMM_ERR_NO_DEVICE = 3,   /* no CUDA device, or not an sm_103 device */
+    HGEMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (see detail) */
+    HGEMM_ERR_OOM = 5,         /* device or host allocation failed */
+    HGEMM_ERR_TIMEOUT = 6      /* a device-side wait ran out of time (kernel aborted cleanly) */
+} hgemm_status_t;
+
+/* Execution paths a plan can take (hgemm_plan_info_t.path). */
+enum {
+    HGEMM_PATH_EMPTY = 0,     /* M == 0 or N == 0: nothing to do */
+    HGEMM_PATH_ZERO_FILL = 1, /* K == 0: C is set to zero (the empty sum) */
+    HGEMM_PATH_TILED = 2,     /* persistent TMA + tcgen05 kernel, 128 x BN tiles */
+    HGEMM_PATH_SKINNY = 3     /* small M: swap-AB, split-K, weights streamed from HBM */
+};
+
+typedef struct hgemm_plan_s *hgemm_plan_t;
+
+/* Optional knobs for hgemm_plan_create_ex; zero-initialise and set what you
+ * need.  They exist for testing and tuning: the defaults are what
+ * hgemm_plan_create picks. */
+typedef struct {
+    int force_path;           /* 0: automatic; HGEMM_PATH_TILED or HGEMM_PATH_SKINNY to force */
+    int force_generic_store;  /* 1: predicated st.global epilogue even when C suits TMA */
+    int force_repack;         /* 1: copy A and B to aligned workspace even when aligned */
+    int tile_n;               /* 0: automatic; 128 or 256 (tiled path) */
+    int split_k;              /* 0: automatic; >= 1 (skinny path) */
+    uint64_t timeout_ns;      /* 0: default (2 s); device watchdog for each pipeline wait */
+} hgemm_options_t;
+
+/* Read-only description of what a plan will launch. */
+typedef struct {
+    int path;             /* HGEMM_PATH_* */
+    int tile_m, tile_n, tile_k;
+    int stages;           /* shared-memory pipeline depth */
+    int split_k;          /* K splits (skinny path), else 1 */
+    int grid;             /* CTAs of the main kernel (persistent: <= SM count) */
+    int repack_a;         /* 1: A is copied to an aligned workspace first */
+    int repack_b;         /* 1: B likewise */
+    int tma_store;        /* 1: TMA-store epilogue; 0: predicated st.global */
+    int kernels_per_run;  /* kernel launches one hgemm_run makes */
+    int64_t workspace_bytes;
+} hgemm_plan_info_t;
+
+/* Creates a plan for C_b = A_b . B_b, b < batch.
+ *   M, N, K          >= 0.  M == 0 or N == 0 makes an empty plan; K == 0 a
+ *                    plan that writes zeros.
+ *   lda >= K, ldb >= N, ldc >= N (elements; checked only when that operand
+ *                    has rows to read or write).
+ *   batch >= 1; strideA/B/C (elements) are used only when batch > 1 and must
+ *                    then be >= 0.
+ *   dtype_in  in {HGEMM_F16, HGEMM_BF16} (applies to both A and B).
+ *   dtype_out in {HGEMM_F32, HGEMM_F16, HGEMM_BF16}.
+ * Validation needs no GPU; on valid arguments the current device must be an
+ * sm_103 GPU (else HGEMM_ERR_NO_DEVICE).  Device workspace is allocated here.
+ * On success *plan receives a handle the caller must destroy. */
+hgemm_status_t hgemm_plan_create(hgemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
+                                 int64_t lda, int64_t ldb, int64_t ldc, int64_t batch,
+                                 int64_t strideA, int64_t strideB, int64_t strideC,
+                                 hgemm_dtype_t dtype_in, hgemm_dtype_t dtype_out);
+
+/* As hgemm_plan_create, with options (NULL = defaults). */
+hgemm_status_t hgemm_plan_create_ex(hgemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
+                                    int64_t lda, int64_t ldb, int64_t ldc, int64_t batch,
+                                    int64_t strideA, int64_t strideB, int64_t strideC,
+                                    hgemm_dtype_t dtype_in, hgemm_dtype_t dtype_out,
+                                    const hgemm_options_t *options);
+
+/* Enqueues the product on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  A, B, C are device pointers laid out as the plan says.  Returns
+ * once the kernels are enqueued; the result is ready when the stream is.
+ * INVALID_ARG for a null pointer when the plan has work to do. */
+hgemm_status_t hgemm_run(hgemm_plan_t plan, const void *A, const void *B, void *C, void *stream);
+
+/* End-to-end variant for operands in HOST memory (pinned memory is fastest):
+ * copies A and B to plan-owned device buffers on `stream`, runs the product,
+ * copies the M x N block(s) of C back into the host buffer (elements outside
+ * the block are left untouched), and synchronises `stream` before returning.
+ * The device buffers are allocated on the first call and kept by the plan. */
+hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void *B_host,
+                              void *C_host, void *stream);
+
+/* Synchronises `stream` and reads the plan's device error word.  Returns
+ * HGEMM_ERR_TIMEOUT if a pipeline wait of an earlier hgemm_run ran out of
+ * time (the kernel then left C incomplete but released all its resources),
+ * HGEMM_ERR_CUDA if the stream reports a CUDA error, else HGEMM_OK.  The
+ * error word is cleared on read. */
+hgemm_status_t hgemm_check(hgemm_plan_t plan, void *stream);
+
+/* Frees the plan's workspace; the caller must make sure no hgemm_run of it
+ * is still executing.  NULL is accepted. */
+hgemm_status_t hgemm_plan_destroy(hgemm_plan_t plan);
+
+/* Fills *info with what the plan launches. */
+hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info);
+
+/* One-shot product: looks up (or creates and keeps) a plan for these
+ * arguments in a process-wide cache, then runs it on `stream`.  Cached plans
+ * live until hgemm_cache_clear() or process exit. */
+hgemm_status_t hgemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t strideA,
+                     int64_t strideB, int64_t strideC, hgemm_dtype_t dtype_in,
+                     hgemm_dtype_t dtype_out, void *stream);
+
+/* Destroys every cached one-shot plan (the caller makes sure none is running). */
+hgemm_status_t hgemm_cache_clear(void);
+
+/* Watchdog self-test: launches a one-warp kernel that waits, with the same
+ * bounded wait the GEMM pipeline uses, on an mbarrier that nothing signals.
+ * The wait must give up after `timeout_ns` and report it.  On return
+ * *device_code holds the error word the kernel wrote (non-zero when the
+ * watchdog fired) and the status is HGEMM_ERR_TIMEOUT in that case. */
+hgemm_status_t hgemm_watchdog_selftest(uint64_t timeout_ns, void *stream, int32_t *device_code);
+
+const char *hgemm_status_string(hgemm_status_t status);
+const char *hgemm_last_error_detail(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t hgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HGEMM_H */

@@ -1,0 +1,682 @@
+// api.cpp -- the C ABI of libhgemm (declared in include/hgemm.h).
+//
+// Host side only: argument validation, the choice of execution path, the
+// device workspace, TMA tensor-map encoding and kernel launches.  The checks
+// mirror the host wrapper of the Ampere kernel in
+// "tensor-cores-cutlass-and-cute" section 四.4 (device, dtype, shape and
+// layout are checked before any pointer is reinterpreted), widened to the
+// strided, batched and ragged cases the library accepts.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "hgemm.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr int64_t kMaxDim = (1ll << 31) - 1;
+
+thread_local std::string g_detail;
+
+hgemm_status_t fail(hgemm_status_t s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_detail = buf;
+    return s;
+}
+
+hgemm_status_t cuda_fail(cudaError_t e, const char *what) {
+    return fail(e == cudaErrorMemoryAllocation ? HGEMM_ERR_OOM : HGEMM_ERR_CUDA, "%s: %s (%s)", what,
+                cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+inline int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int out_bytes(hgemm_dtype_t d) { return d == HGEMM_F32 ? 4 : 2; }
+inline int out_type(hgemm_dtype_t d) {
+    return d == HGEMM_F32 ? hg::OUT_F32 : (d == HGEMM_BF16 ? hg::OUT_BF16 : hg::OUT_F16);
+}
+
+// Encodes a 3-D tiled map over a row-major [batch][rows][cols] array with the
+// given element size, leading dimension and batch stride (elements).
+hgemm_status_t encode_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dt, int esize,
+                         int64_t cols, int64_t rows, int64_t batch, int64_t ld, int64_t stride,
+                         uint32_t box_cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return fail(HGEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    int64_t bstride = stride * esize;
+    if (batch == 1) bstride = round_up(rows * ld * esize, 16);
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * esize), static_cast<cuuint64_t>(bstride)};
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(HGEMM_ERR_CUDA,
+                    "cuTensorMapEncodeTiled failed (%d): dims %lld x %lld x %lld, ld %lld, "
+                    "stride %lld, box %u x %u",
+                    static_cast<int>(r), static_cast<long long>(cols), static_cast<long long>(rows),
+                    static_cast<long long>(batch), static_cast<long long>(ld),
+                    static_cast<long long>(stride), box_cols, box_rows);
+    return HGEMM_OK;
+}
+
+}  // namespace
+
+struct hgemm_plan_s {
+    int64_t M, N, K, lda, ldb, ldc, batch, sA, sB, sC;
+    hgemm_dtype_t din, dout;
+    hgemm_options_t opt;
+    int device, num_sms;
+    int path;
+    // tiled path
+    int bn;
+    // skinny path
+    int nu, split, kb_per;
+    int grid;
+    bool ld_repack_a, ld_repack_b;  // forced by leading dimension / stride
+    bool ldc_tma;                   // C's ld / stride allow TMA stores
+    uint64_t timeout_ns;
+    // workspace: [err 256 B][counters][partials][A copy][B copy]
+    char *ws = nullptr;
+    size_t ws_bytes = 0, off_counters = 0, off_partials = 0, off_apack = 0, off_bpack = 0;
+    size_t apack_bytes = 0, bpack_bytes = 0;
+    bool have_apack = false, have_bpack = false;  // workspace holds room for the copy
+    int64_t lda_p = 0, ldb_p = 0, sA_p = 0, sB_p = 0;
+    // host-buffer (end-to-end) staging
+    char *dA = nullptr, *dB = nullptr, *dC = nullptr;
+    size_t dA_bytes = 0, dB_bytes = 0, dC_bytes = 0;
+    // tensor-map cache
+    const void *mA = nullptr, *mB = nullptr;
+    void *mC = nullptr;
+    bool maps_ok = false;
+    CUtensorMap tmA, tmB, tmC;
+};
+
+namespace {
+
+int64_t span_elems(int64_t rows, int64_t cols, int64_t ld, int64_t batch, int64_t stride) {
+    if (rows == 0 || cols == 0) return 0;
+    return (batch - 1) * stride + (rows - 1) * ld + cols;
+}
+
+hgemm_status_t validate(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        int64_t batch, int64_t sA, int64_t sB, int64_t sC, hgemm_dtype_t din,
+                        hgemm_dtype_t dout) {
+    if (din != HGEMM_F16 && din != HGEMM_BF16)
+        return fail(HGEMM_ERR_INVALID_ARG, "dtype_in must be HGEMM_F16 or HGEMM_BF16 (got %d)",
+                    static_cast<int>(din));
+    if (dout != HGEMM_F16 && dout != HGEMM_BF16 && dout != HGEMM_F32)
+        return fail(HGEMM_ERR_INVALID_ARG, "dtype_out must be HGEMM_F32, HGEMM_F16 or HGEMM_BF16 (got %d)",
+                    static_cast<int>(dout));
+    if (M < 0 || N < 0 || K < 0)
+        return fail(HGEMM_ERR_INVALID_ARG, "negative size M=%lld N=%lld K=%lld",
+                    static_cast<long long>(M), static_cast<long long>(N), static_cast<long long>(K));
+    if (batch < 1) return fail(HGEMM_ERR_INVALID_ARG, "batch must be >= 1 (got %lld)", static_cast<long long>(batch));
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim || batch > kMaxDim)
+        return fail(HGEMM_ERR_UNSUPPORTED, "sizes above 2^31-1 are not supported");
+    if (M > 0 && K > 0 && lda < K)
+        return fail(HGEMM_ERR_INVALID_ARG, "lda (%lld) < K (%lld)", static_cast<long long>(lda), static_cast<long long>(K));
+    if (K > 0 && N > 0 && ldb < N)
+        return fail(HGEMM_ERR_INVALID_ARG, "ldb (%lld) < N (%lld)", static_cast<long long>(ldb), static_cast<long long>(N));
+    if (M > 0 && N > 0 && ldc < N)
+        return fail(HGEMM_ERR_INVALID_ARG, "ldc (%lld) < N (%lld)", static_cast<long long>(ldc), static_cast<long long>(N));
+    if (batch > 1 && (sA < 0 || sB < 0 || sC < 0))
+        return fail(HGEMM_ERR_INVALID_ARG, "negative batch stride");
+    if (batch > 1 && M > 0 && N > 0 && sC < (M - 1) * ldc + N)
+        return fail(HGEMM_ERR_INVALID_ARG, "strideC (%lld) makes the batches of C overlap",
+                    static_cast<long long>(sC));
+    const int64_t tiles = batch * ceil_div(M, 128) * ceil_div(N, 128);
+    if (tiles > kMaxDim) return fail(HGEMM_ERR_UNSUPPORTED, "too many output tiles");
+    return HGEMM_OK;
+}
+
+// Picks the split count for the skinny path: the smallest split whose units
+// fill the persistent grid to >= 90% (units per wave), else the best found.
+int choose_split(int64_t work_tiles, int num_kb, int num_sms) {
+    int best = 1;
+    double best_eff = 0;
+    for (int s = 1; s <= 16 && s <= num_kb; ++s) {
+        const int kb_per = static_cast<int>(ceil_div(num_kb, s));
+        const int s_eff = static_cast<int>(ceil_div(num_kb, kb_per));
+        if (s_eff != s) continue;
+        if (s > 1 && kb_per < 4) break;
+        const int64_t units = work_tiles * s;
+        const int64_t waves = ceil_div(units, num_sms);
+        const double eff = static_cast<double>(units) / static_cast<double>(waves * num_sms);
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = s;
+        }
+        if (eff >= 0.9) return s;
+    }
+    return best;
+}
+
+hgemm_status_t alloc_workspace(hgemm_plan_s *p) {
+    size_t off = 256;  // error word (+ padding)
+    p->off_counters = off;
+    size_t counters = 0, partials = 0;
+    if (p->path == HGEMM_PATH_SKINNY) {
+        const int64_t num_n = ceil_div(p->N, 128);
+        counters = static_cast<size_t>(p->batch * num_n) * 4 * sizeof(int32_t);
+        if (p->split > 1)
+            partials = static_cast<size_t>(p->batch) * p->split * num_n * p->nu * 128 * sizeof(float);
+    }
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off + counters), 256));
+    p->off_partials = off;
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off + partials), 256));
+    if (p->path == HGEMM_PATH_TILED || p->path == HGEMM_PATH_SKINNY) {
+        // aligned copies of A and B; allocated whenever a copy can be needed
+        // (by the leading dimension now, or by a misaligned pointer later)
+        p->lda_p = round_up(p->K, 8);
+        p->sA_p = p->M * p->lda_p;
+        p->ldb_p = round_up(p->N, 8);
+        p->sB_p = p->K * p->ldb_p;
+        p->apack_bytes = static_cast<size_t>(p->batch * p->sA_p * 2);
+        p->bpack_bytes = static_cast<size_t>(p->batch * p->sB_p * 2);
+    }
+    p->ws_bytes = off;
+    p->off_apack = p->off_bpack = 0;
+    if (p->ld_repack_a || p->opt.force_repack) {
+        p->off_apack = p->ws_bytes;
+        p->ws_bytes = static_cast<size_t>(round_up(static_cast<int64_t>(p->ws_bytes + p->apack_bytes), 256));
+        p->have_apack = true;
+    }
+    if (p->ld_repack_b || p->opt.force_repack) {
+        p->off_bpack = p->ws_bytes;
+        p->ws_bytes = static_cast<size_t>(round_up(static_cast<int64_t>(p->ws_bytes + p->bpack_bytes), 256));
+        p->have_bpack = true;
+    }
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&p->ws), p->ws_bytes);
+    if (e != cudaSuccess) {
+        p->ws = nullptr;
+        return cuda_fail(e, "cudaMalloc(workspace)");
+    }
+    e = cudaMemset(p->ws, 0, p->off_partials);  // error word + counters start at zero
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
+    return HGEMM_OK;
+}
+
+// Grows the workspace when a run needs an operand copy the plan did not
+// foresee (a misaligned base pointer).  Synchronous; happens at most once per
+// operand and plan.
+hgemm_status_t ensure_pack(hgemm_plan_s *p, bool need_a, bool need_b) {
+    const bool add_a = need_a && !p->have_apack;
+    const bool add_b = need_b && !p->have_bpack;
+    if (!add_a && !add_b) return HGEMM_OK;
+    size_t need = p->ws_bytes;
+    size_t off_a = p->off_apack, off_b = p->off_bpack;
+    if (add_a) {
+        off_a = need;
+        need = static_cast<size_t>(round_up(static_cast<int64_t>(need + p->apack_bytes), 256));
+    }
+    if (add_b) {
+        off_b = need;
+        need = static_cast<size_t>(round_up(static_cast<int64_t>(need + p->bpack_bytes), 256));
+    }
+    char *nws = nullptr;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    e = cudaMalloc(reinterpret_cast<void **>(&nws), need);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+    e = cudaMemcpy(nws, p->ws, p->off_partials, cudaMemcpyDeviceToDevice);
+    if (e != cudaSuccess) {
+        cudaFree(nws);
+        return cuda_fail(e, "cudaMemcpy(workspace)");
+    }
+    cudaFree(p->ws);
+    p->ws = nws;
+    p->ws_bytes = need;
+    p->off_apack = off_a;
+    p->off_bpack = off_b;
+    p->have_apack = p->have_apack || add_a;
+    p->have_bpack = p->have_bpack || add_b;
+    p->maps_ok = false;
+    return HGEMM_OK;
+}
+
+hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, int64_t lda,
+                           int64_t ldb, int64_t ldc, int64_t batch, int64_t sA, int64_t sB,
+                           int64_t sC, hgemm_dtype_t din, hgemm_dtype_t dout,
+                           const hgemm_options_t *options) {
+    if (!out) return fail(HGEMM_ERR_INVALID_ARG, "plan pointer is NULL");
+    *out = nullptr;
+    hgemm_status_t st = validate(M, N, K, lda, ldb, ldc, batch, sA, sB, sC, din, dout);
+    if (st != HGEMM_OK) return st;
+    hgemm_options_t opt{};
+    if (options) opt = *options;
+    if (opt.force_path != 0 && opt.force_path != HGEMM_PATH_TILED && opt.force_path != HGEMM_PATH_SKINNY)
+        return fail(HGEMM_ERR_INVALID_ARG, "force_path must be 0, HGEMM_PATH_TILED or HGEMM_PATH_SKINNY");
+    if (opt.tile_n != 0 && opt.tile_n != 128 && opt.tile_n != 256)
+        return fail(HGEMM_ERR_INVALID_ARG, "tile_n must be 0, 128 or 256");
+    if (opt.split_k < 0) return fail(HGEMM_ERR_INVALID_ARG, "split_k must be >= 0");
+    if (opt.force_path == HGEMM_PATH_SKINNY && M > 32)
+        return fail(HGEMM_ERR_UNSUPPORTED, "the skinny path handles M <= 32 (got %lld)", static_cast<long long>(M));
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(HGEMM_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3)
+        return fail(HGEMM_ERR_NO_DEVICE, "libhgemm is built for sm_103a; device %d is sm_%d%d", dev,
+                    major, minor);
+
+    hgemm_plan_s *p = new (std::nothrow) hgemm_plan_s();
+    if (!p) return fail(HGEMM_ERR_OOM, "host allocation failed");
+    p->M = M; p->N = N; p->K = K;
+    p->lda = lda; p->ldb = ldb; p->ldc = ldc; p->batch = batch;
+    p->sA = batch > 1 ? sA : 0;
+    p->sB = batch > 1 ? sB : 0;
+    p->sC = batch > 1 ? sC : 0;
+    p->din = din; p->dout = dout; p->opt = opt;
+    p->device = dev; p->num_sms = sms;
+    p->timeout_ns = opt.timeout_ns ? opt.timeout_ns : kDefaultTimeoutNs;
+    p->bn = 0; p->nu = 0; p->split = 1; p->kb_per = 0; p->grid = 0;
+
+    if (M == 0 || N == 0) {
+        p->path = HGEMM_PATH_EMPTY;
+    } else if (K == 0) {
+        p->path = HGEMM_PATH_ZERO_FILL;
+    } else if (opt.force_path == HGEMM_PATH_SKINNY || (opt.force_path == 0 && M <= 32)) {
+        p->path = HGEMM_PATH_SKINNY;
+    } else {
+        p->path = HGEMM_PATH_TILED;
+    }
+
+    const int ob = out_bytes(dout);
+    p->ld_repack_a = (lda * 2) % 16 != 0 || (batch > 1 && (p->sA * 2) % 16 != 0);
+    p->ld_repack_b = (ldb * 2) % 16 != 0 || (batch > 1 && (p->sB * 2) % 16 != 0);
+    p->ldc_tma = (ldc * ob) % 16 == 0 && (batch == 1 || (p->sC * ob) % 16 == 0) && !opt.force_generic_store;
+
+    const int num_kb = static_cast<int>(ceil_div(K, 64));
+    if (p->path == HGEMM_PATH_TILED) {
+        p->bn = opt.tile_n ? opt.tile_n : (N <= 128 ? 128 : 256);
+        const int64_t tiles = batch * ceil_div(M, 128) * ceil_div(N, p->bn);
+        p->grid = static_cast<int>(tiles < sms ? tiles : sms);
+    } else if (p->path == HGEMM_PATH_SKINNY) {
+        p->nu = M <= 16 ? 16 : 32;
+        const int64_t work = batch * ceil_div(N, 128);
+        int split = opt.split_k ? opt.split_k : choose_split(work, num_kb, sms);
+        if (split > num_kb) split = num_kb;
+        if (split < 1) split = 1;
+        p->kb_per = static_cast<int>(ceil_div(num_kb, split));
+        p->split = static_cast<int>(ceil_div(num_kb, p->kb_per));  // no empty split
+        const int64_t units = work * p->split;
+        p->grid = static_cast<int>(units < sms ? units : sms);
+    }
+    st = alloc_workspace(p);
+    if (st != HGEMM_OK) {
+        if (p->ws) cudaFree(p->ws);
+        delete p;
+        return st;
+    }
+    *out = p;
+    return HGEMM_OK;
+}
+
+hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *C, bool tma_store) {
+    if (p->maps_ok && A == p->mA && B == p->mB && C == p->mC) return HGEMM_OK;
+    const CUtensorMapDataType dt =
+        p->din == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const bool packed_a = p->have_apack && A == p->ws + p->off_apack;
+    const bool packed_b = p->have_bpack && B == p->ws + p->off_bpack;
+    const int64_t lda = packed_a ? p->lda_p : p->lda;
+    const int64_t sA = packed_a ? p->sA_p : p->sA;
+    const int64_t ldb = packed_b ? p->ldb_p : p->ldb;
+    const int64_t sB = packed_b ? p->sB_p : p->sB;
+    hgemm_status_t st;
+    if (p->path == HGEMM_PATH_TILED) {
+        st = encode_3d(&p->tmA, A, dt, 2, p->K, p->M, p->batch, lda, sA, 64, 128);
+        if (st != HGEMM_OK) return st;
+        st = encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64);
+        if (st != HGEMM_OK) return st;
+        if (tma_store) {
+            const CUtensorMapDataType ct = p->dout == HGEMM_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                           : p->dout == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+            const int ob = out_bytes(p->dout);
+            st = encode_3d(&p->tmC, C, ct, ob, p->N, p->M, p->batch, p->ldc, p->sC,
+                           static_cast<uint32_t>(128 / ob), 32);
+            if (st != HGEMM_OK) return st;
+        } else {
+            std::memset(&p->tmC, 0, sizeof(p->tmC));
+        }
+    } else {
+        st = encode_3d(&p->tmA, A, dt, 2, p->K, p->M, p->batch, lda, sA, 64,
+                       static_cast<uint32_t>(p->nu));
+        if (st != HGEMM_OK) return st;
+        st = encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64);
+        if (st != HGEMM_OK) return st;
+        std::memset(&p->tmC, 0, sizeof(p->tmC));
+    }
+    p->mA = A; p->mB = B; p->mC = C;
+    p->maps_ok = true;
+    return HGEMM_OK;
+}
+
+hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, cudaStream_t s) {
+    if (p->path == HGEMM_PATH_EMPTY) return HGEMM_OK;
+    if (!C) return fail(HGEMM_ERR_INVALID_ARG, "C is NULL");
+    const int ob = out_bytes(p->dout);
+    if ((reinterpret_cast<uintptr_t>(C) % ob) != 0) return fail(HGEMM_ERR_INVALID_ARG, "C is not element-aligned");
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device)
+        return fail(HGEMM_ERR_INVALID_ARG, "plan was created on device %d but device %d is current", p->device, cur);
+    cudaError_t e;
+    if (p->path == HGEMM_PATH_ZERO_FILL) {
+        e = hg::launch_zero_fill(C, p->ldc, p->sC, p->M, p->N, p->batch, ob, p->num_sms, s);
+        return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "zero-fill launch");
+    }
+    if (!A || !B) return fail(HGEMM_ERR_INVALID_ARG, "A or B is NULL");
+    if ((reinterpret_cast<uintptr_t>(A) & 1) || (reinterpret_cast<uintptr_t>(B) & 1))
+        return fail(HGEMM_ERR_INVALID_ARG, "A or B is not element-aligned");
+
+    const bool pack_a = p->ld_repack_a || p->opt.force_repack || !aligned16(A);
+    const bool pack_b = p->ld_repack_b || p->opt.force_repack || !aligned16(B);
+    hgemm_status_t st = ensure_pack(p, pack_a, pack_b);
+    if (st != HGEMM_OK) return st;
+    const void *Ae = A;
+    const void *Be = B;
+    if (pack_a) {
+        e = hg::launch_repack16(A, p->lda, p->sA, p->ws + p->off_apack, p->lda_p, p->sA_p, p->M,
+                                p->K, p->batch, p->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, "repack(A) launch");
+        Ae = p->ws + p->off_apack;
+    }
+    if (pack_b) {
+        e = hg::launch_repack16(B, p->ldb, p->sB, p->ws + p->off_bpack, p->ldb_p, p->sB_p, p->K,
+                                p->N, p->batch, p->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, "repack(B) launch");
+        Be = p->ws + p->off_bpack;
+    }
+    int32_t *err = reinterpret_cast<int32_t *>(p->ws);
+    const uint32_t bf = p->din == HGEMM_BF16 ? 1u : 0u;
+    if (p->path == HGEMM_PATH_TILED) {
+        const bool ts = p->ldc_tma && aligned16(C);
+        st = encode_maps(p, Ae, Be, C, ts);
+        if (st != HGEMM_OK) return st;
+        hg::TiledParams tp{};
+        tp.M = static_cast<int32_t>(p->M);
+        tp.N = static_cast<int32_t>(p->N);
+        tp.K = static_cast<int32_t>(p->K);
+        tp.batch = static_cast<int32_t>(p->batch);
+        tp.num_m = static_cast<int32_t>(ceil_div(p->M, 128));
+        tp.num_n = static_cast<int32_t>(ceil_div(p->N, p->bn));
+        tp.num_kb = static_cast<int32_t>(ceil_div(p->K, 64));
+        tp.tiles = tp.batch * tp.num_m * tp.num_n;
+        tp.group_m = 16;
+        tp.idesc = hg::idesc_f16(bf, 0, 1, 128, static_cast<uint32_t>(p->bn));
+        tp.C = C;
+        tp.ldc = p->ldc;
+        tp.strideC = p->sC;
+        tp.err = err;
+        tp.timeout_ns = p->timeout_ns;
+        e = hg::launch_tiled(p->bn, out_type(p->dout), ts, p->tmA, p->tmB, p->tmC, tp, p->grid, s);
+        return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "tiled kernel launch");
+    }
+    // skinny
+    st = encode_maps(p, Ae, Be, C, false);
+    if (st != HGEMM_OK) return st;
+    hg::SkinnyParams sp{};
+    sp.M = static_cast<int32_t>(p->M);
+    sp.N = static_cast<int32_t>(p->N);
+    sp.K = static_cast<int32_t>(p->K);
+    sp.batch = static_cast<int32_t>(p->batch);
+    sp.num_n = static_cast<int32_t>(ceil_div(p->N, 128));
+    sp.num_kb = static_cast<int32_t>(ceil_div(p->K, 64));
+    sp.split = p->split;
+    sp.kb_per_split = p->kb_per;
+    sp.units = sp.batch * sp.split * sp.num_n;
+    sp.idesc = hg::idesc_f16(bf, 1, 0, 128, static_cast<uint32_t>(p->nu));
+    sp.C = C;
+    sp.ldc = p->ldc;
+    sp.strideC = p->sC;
+    sp.partials = reinterpret_cast<float *>(p->ws + p->off_partials);
+    sp.counters = reinterpret_cast<int32_t *>(p->ws + p->off_counters);
+    sp.err = err;
+    sp.timeout_ns = p->timeout_ns;
+    e = hg::launch_skinny(p->nu, out_type(p->dout), p->tmA, p->tmB, sp, p->grid, s);
+    return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "skinny kernel launch");
+}
+
+// ---------------------------------------------------------------- one-shot cache
+
+using CacheKey = std::tuple<int, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t,
+                            int64_t, int64_t, int64_t, int, int>;
+std::mutex g_cache_mu;
+std::map<CacheKey, hgemm_plan_s *> g_cache;
+
+}  // namespace
+
+extern "C" {
+
+hgemm_status_t hgemm_plan_create(hgemm_plan_t *plan, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                 int64_t ldb, int64_t ldc, int64_t batch, int64_t strideA,
+                                 int64_t strideB, int64_t strideC, hgemm_dtype_t dtype_in,
+                                 hgemm_dtype_t dtype_out) {
+    return plan_create(plan, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, dtype_in,
+                       dtype_out, nullptr);
+}
+
+hgemm_status_t hgemm_plan_create_ex(hgemm_plan_t *plan, int64_t M, int64_t N, int64_t K,
+                                    int64_t lda, int64_t ldb, int64_t ldc, int64_t batch,
+                                    int64_t strideA, int64_t strideB, int64_t strideC,
+                                    hgemm_dtype_t dtype_in, hgemm_dtype_t dtype_out,
+                                    const hgemm_options_t *options) {
+    return plan_create(plan, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, dtype_in,
+                       dtype_out, options);
+}
+
+hgemm_status_t hgemm_run(hgemm_plan_t plan, const void *A, const void *B, void *C, void *stream) {
+    if (!plan) return fail(HGEMM_ERR_INVALID_ARG, "plan is NULL");
+    return plan_run(plan, A, B, C, static_cast<cudaStream_t>(stream));
+}
+
+hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void *B_host, void *C_host,
+                              void *stream) {
+    if (!plan) return fail(HGEMM_ERR_INVALID_ARG, "plan is NULL");
+    hgemm_plan_s *p = plan;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->path == HGEMM_PATH_EMPTY) return HGEMM_OK;
+    if (!C_host || (p->path != HGEMM_PATH_ZERO_FILL && (!A_host || !B_host)))
+        return fail(HGEMM_ERR_INVALID_ARG, "host pointer is NULL");
+    const int ob = out_bytes(p->dout);
+    const size_t a_bytes = static_cast<size_t>(span_elems(p->M, p->K, p->lda, p->batch, p->sA)) * 2;
+    const size_t b_bytes = static_cast<size_t>(span_elems(p->K, p->N, p->ldb, p->batch, p->sB)) * 2;
+    const size_t c_bytes = static_cast<size_t>(span_elems(p->M, p->N, p->ldc, p->batch, p->sC)) * ob;
+    cudaError_t e;
+    auto grow = [&](char **buf, size_t *have, size_t want) -> cudaError_t {
+        if (*have >= want) return cudaSuccess;
+        if (*buf) cudaFree(*buf);
+        *buf = nullptr;
+        *have = 0;
+        cudaError_t r = cudaMalloc(reinterpret_cast<void **>(buf), want < 16 ? 16 : want);
+        if (r == cudaSuccess) *have = want;
+        return r;
+    };
+    if ((e = grow(&p->dA, &p->dA_bytes, a_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(A staging)");
+    if ((e = grow(&p->dB, &p->dB_bytes, b_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(B staging)");
+    if ((e = grow(&p->dC, &p->dC_bytes, c_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(C staging)");
+    if (p->path != HGEMM_PATH_ZERO_FILL) {
+        if ((e = cudaMemcpyAsync(p->dA, A_host, a_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+            return cuda_fail(e, "copy A to device");
+        if ((e = cudaMemcpyAsync(p->dB, B_host, b_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+            return cuda_fail(e, "copy B to device");
+    }
+    hgemm_status_t st = plan_run(p, p->dA, p->dB, p->dC, s);
+    if (st != HGEMM_OK) return st;
+    // copy back only the M x N block of each batch: host elements between rows stay intact
+    for (int64_t b = 0; b < p->batch; ++b) {
+        const size_t off = static_cast<size_t>(b * p->sC) * ob;
+        e = cudaMemcpy2DAsync(static_cast<char *>(C_host) + off, static_cast<size_t>(p->ldc) * ob,
+                              p->dC + off, static_cast<size_t>(p->ldc) * ob,
+                              static_cast<size_t>(p->N) * ob, static_cast<size_t>(p->M),
+                              cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e, "copy C to host");
+    }
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return HGEMM_OK;
+}
+
+hgemm_status_t hgemm_check(hgemm_plan_t plan, void *stream) {
+    if (!plan) return fail(HGEMM_ERR_INVALID_ARG, "plan is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream reports an error");
+    int32_t word = 0;
+    e = cudaMemcpy(&word, plan->ws, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word != 0) {
+        // clear the word and any split-K counters an aborted run left behind
+        cudaMemset(plan->ws, 0, plan->off_partials);
+        const unsigned role = (static_cast<uint32_t>(word) >> 16) & 0xFFu;
+        const unsigned idx = static_cast<uint32_t>(word) & 0xFFFFu;
+        static const char *names[] = {"?", "TMA producer", "MMA issuer", "epilogue", "drain", "self-test"};
+        return fail(HGEMM_ERR_TIMEOUT, "device wait timed out: role %s, barrier %u (code 0x%08x)",
+                    role < 6 ? names[role] : "?", idx, static_cast<uint32_t>(word));
+    }
+    return HGEMM_OK;
+}
+
+hgemm_status_t hgemm_plan_destroy(hgemm_plan_t plan) {
+    if (!plan) return HGEMM_OK;
+    if (plan->ws) cudaFree(plan->ws);
+    if (plan->dA) cudaFree(plan->dA);
+    if (plan->dB) cudaFree(plan->dB);
+    if (plan->dC) cudaFree(plan->dC);
+    delete plan;
+    return HGEMM_OK;
+}
+
+hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
+    if (!plan || !info) return fail(HGEMM_ERR_INVALID_ARG, "plan or info is NULL");
+    hgemm_plan_info_t r{};
+    r.path = plan->path;
+    r.tile_k = 64;
+    r.split_k = 1;
+    if (plan->path == HGEMM_PATH_TILED) {
+        r.tile_m = 128;
+        r.tile_n = plan->bn;
+        r.stages = hg::tiled_stages(plan->bn);
+        r.tma_store = plan->ldc_tma ? 1 : 0;
+    } else if (plan->path == HGEMM_PATH_SKINNY) {
+        r.tile_m = plan->nu;
+        r.tile_n = 128;
+        r.stages = hg::skinny_stages(plan->nu);
+        r.split_k = plan->split;
+    }
+    r.grid = plan->grid;
+    const bool busy = plan->path == HGEMM_PATH_TILED || plan->path == HGEMM_PATH_SKINNY;
+    r.repack_a = (busy && (plan->ld_repack_a || plan->opt.force_repack)) ? 1 : 0;
+    r.repack_b = (busy && (plan->ld_repack_b || plan->opt.force_repack)) ? 1 : 0;
+    r.kernels_per_run = plan->path == HGEMM_PATH_EMPTY ? 0 : 1 + r.repack_a + r.repack_b;
+    if (plan->path == HGEMM_PATH_ZERO_FILL) r.kernels_per_run = 1;
+    r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
+    *info = r;
+    return HGEMM_OK;
+}
+
+hgemm_status_t hgemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t strideA,
+                     int64_t strideB, int64_t strideC, hgemm_dtype_t dtype_in,
+                     hgemm_dtype_t dtype_out, void *stream) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    CacheKey key{dev, M, N, K, lda, ldb, ldc, batch, batch > 1 ? strideA : 0,
+                 batch > 1 ? strideB : 0, batch > 1 ? strideC : 0, static_cast<int>(dtype_in),
+                 static_cast<int>(dtype_out)};
+    hgemm_plan_s *p = nullptr;
+    {
+        std::lock_guard<std::mutex> g(g_cache_mu);
+        auto it = g_cache.find(key);
+        if (it != g_cache.end()) {
+            p = it->second;
+        } else {
+            hgemm_status_t st = plan_create(&p, M, N, K, lda, ldb, ldc, batch, strideA, strideB,
+                                            strideC, dtype_in, dtype_out, nullptr);
+            if (st != HGEMM_OK) return st;
+            g_cache[key] = p;
+        }
+    }
+    return plan_run(p, A, B, C, static_cast<cudaStream_t>(stream));
+}
+
+hgemm_status_t hgemm_cache_clear(void) {
+    std::lock_guard<std::mutex> g(g_cache_mu);
+    for (auto &kv : g_cache) hgemm_plan_destroy(kv.second);
+    g_cache.clear();
+    return HGEMM_OK;
+}
+
+hgemm_status_t hgemm_watchdog_selftest(uint64_t timeout_ns, void *stream, int32_t *device_code) {
+    if (!device_code) return fail(HGEMM_ERR_INVALID_ARG, "device_code is NULL");
+    *device_code = 0;
+    int32_t *err = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&err), sizeof(int32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(err, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = hg::launch_watchdog_selftest(err, timeout_ns, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(device_code, err, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaFree(err);
+    if (e != cudaSuccess) return cuda_fail(e, "watchdog self-test");
+    if (*device_code != 0) return fail(HGEMM_ERR_TIMEOUT, "watchdog fired (code 0x%08x)", static_cast<uint32_t>(*device_code));
+    return HGEMM_OK;
+}
+
+const char *hgemm_status_string(hgemm_status_t s) {
+    switch (s) {
+        case HGEMM_OK: return "HGEMM_OK";
+        case HGEMM_ERR_INVALID_ARG: return "HGEMM_ERR_INVALID_ARG";
+        case HGEMM_ERR_UNSUPPORTED: return "HGEMM_ERR_UNSUPPORTED";
+        case HGEMM_ERR_NO_DEVICE: return "HGEMM_ERR_NO_DEVICE";
+        case HGEMM_ERR_CUDA: return "HGEMM_ERR_CUDA";
+        case HGEMM_ERR_OOM: return "HGEMM_ERR_OOM";
+        case HGEMM_ERR_TIMEOUT: return "HGEMM_ERR_TIMEOUT";
+        default: return "HGEMM_ERR_UNKNOWN";
+    }
+}
+
+const char *hgemm_last_error_detail(void) { return g_detail.c_str(); }
+
+int32_t hgemm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,405 @@
+// gemm_tiled.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// C_b = A_b . B_b with A (M x K) and B (K x N) row-major, fp16/bf16 inputs,
+// fp32 accumulation in tensor memory, fp32/fp16/bf16 output.
+//
+// Structure (the Blackwell form of "tensor-cores-cutlass-and-cute" section 五.3,
+// warp specialisation with full/empty barrier pairs around a stage ring):
+//   warp 0, one thread   TMA producer: for every 64-deep K block waits until
+//                        the stage is empty, arms full[stage] with the byte
+//                        count (section 五.1) and issues one A box (128 x 64)
+//                        and BN/64 B boxes (64 x 64) into 128-byte-swizzled
+//                        shared memory.
+//   warp 1, one thread   MMA issuer: waits full[stage], issues four
+//                        tcgen05.mma (K = 16 each) that read A and B from
+//                        shared memory through descriptors (section 五.2) and
+//                        accumulate into a TMEM buffer, then tcgen05.commit
+//                        frees the stage.  After a tile's last K block it
+//                        commits tfull[buf].
+//   warps 2-5            epilogue: wait tfull[buf], tcgen05.ld 32-column
+//                        chunks (lane = output row), convert, stage each
+//                        32-row x 128-byte piece in 128-byte-swizzled shared
+//                        memory and TMA-store it (section 四.5's point that
+//                        the epilogue should write full sectors), or write C
+//                        with predicated coalesced stores when C is not
+//                        16-byte aligned.  They release TMEM (tempty[buf]) as
+//                        soon as the last chunk is in registers.
+// Two TMEM accumulator buffers let the epilogue of tile i overlap the main
+// loop of tile i+1 -- the effect "ping-pong" consumers buy on Hopper
+// (section 五.3).  The CTA loops over tiles (persistent; grid <= SM count) in
+// grouped order so that concurrently running CTAs share A and B in L2
+// (section 四.5 lists tile order as one of the gaps).
+//
+// Operand layouts in shared memory (both from TMA with SWIZZLE_128B, which is
+// the hardware form of the XOR swizzle of section 三.5: 16-byte chunk c of row
+// r goes to chunk c ^ (r & 7)):
+//   A: K-major, 128 rows x 128 bytes (64 k); descriptor SBO = 1024.
+//   B: MN-major (B is K x N row-major, so N is contiguous): BN/64 blocks of
+//      64 k-rows x 128 bytes (64 n); descriptor LBO = 8192 (next n block),
+//      SBO = 1024 (next 8 k).  The k-th MMA of a stage starts 16 rows
+//      (2048 bytes) further.
+// Ragged M/N/K edges are handled by TMA: loads zero-fill outside the tensor
+// and stores clip to it.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "watchdog.cuh"
+
+namespace hg {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int NUM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int EPI_WARPS = 4;
+constexpr int STG_BYTES = 4096;   // one staged piece: 32 rows x 128 bytes
+constexpr int STG_BUFS = 2;       // per epilogue warp
+
+template <int BN>
+struct TiledCfg {
+    static_assert(BN == 128 || BN == 256, "tile N");
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr uint32_t A_BYTES = BM * BK * 2;
+    static constexpr uint32_t B_BYTES = BK * BN * 2;
+    static constexpr uint32_t B_BLOCK = BK * 128;  // 64 k-rows x 64 n (128 bytes)
+    static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators
+    static constexpr int SMEM_A = 0;
+    static constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
+    static constexpr int SMEM_C = SMEM_B + STAGES * B_BYTES;
+    static constexpr int SMEM_BAR = SMEM_C + EPI_WARPS * STG_BUFS * STG_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+    static constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_TOTAL = SMEM_MISC + 16 + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ void tile_coords(const TiledParams &p, int t, int &b, int &mt, int &nt) {
+    const int per_batch = p.num_m * p.num_n;
+    b = t / per_batch;
+    const int r = t - b * per_batch;
+    const int span = p.group_m * p.num_n;
+    const int g = r / span;
+    const int first_m = g * p.group_m;
+    const int gsz = min(p.num_m - first_m, p.group_m);
+    const int rr = r - g * span;
+    mt = first_m + rr % gsz;
+    nt = rr / gsz;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
+    const float a = __uint_as_float(lo), b = __uint_as_float(hi);
+    if constexpr (OUT == OUT_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // round to nearest even
+        return *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_one(void *C, int64_t idx, float v) {
+    if constexpr (OUT == OUT_F32) {
+        static_cast<float *>(C)[idx] = v;
+    } else if constexpr (OUT == OUT_BF16) {
+        static_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(v);
+    } else {
+        static_cast<__half *>(C)[idx] = __float2half_rn(v);
+    }
+}
+
+template <int BN, int OUT, bool TMA_STORE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    hgemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC, const TiledParams p) {
+    using Cfg = TiledCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sA = sbase + Cfg::SMEM_A;
+    const uint32_t sB = sbase + Cfg::SMEM_B;
+    const uint32_t sC = sbase + Cfg::SMEM_C;
+    const uint32_t bar0 = sbase + Cfg::SMEM_BAR;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (Cfg::STAGES + s); };
+    auto tfull = [&](int b) { return bar0 + 8u * (2 * Cfg::STAGES + b); };
+    auto tempty = [&](int b) { return bar0 + 8u * (2 * Cfg::STAGES + 2 + b); };
+    const uint32_t drain = bar0 + 8u * (2 * Cfg::STAGES + 4);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Cfg::SMEM_MISC);
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + Cfg::SMEM_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull(b), 1);
+            mbar_init(tempty(b), EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        if (TMA_STORE) prefetch_tmap(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+                int b, mt, nt;
+                tile_coords(p, t, b, mt, nt);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(empty(stage), phase ^ 1u, wc,
+                                      timeout_code(ROLE_PRODUCER, stage))) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full(stage), Cfg::TX_BYTES);
+                    tma_load_3d(sA + stage * Cfg::A_BYTES, &tmA, full(stage), kb * BK, mt * BM, b);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_3d(sB + stage * Cfg::B_BYTES + j * Cfg::B_BLOCK, &tmB, full(stage),
+                                    nt * BN + j * 64, kb * BK, b);
+                    ++issued;
+                    if (++stage == Cfg::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Teardown: no TMA write into this CTA's shared memory may still be
+            // in flight.  On the normal path these phases completed long ago.
+            const int pending = issued < Cfg::STAGES ? issued : Cfg::STAGES;
+            for (int i = 0; i < pending; ++i) {
+                if (stage == 0) {
+                    stage = Cfg::STAGES - 1;
+                    phase ^= 1u;
+                } else {
+                    --stage;
+                }
+                wait_bounded(full(stage), phase, wc, 0, /*honor_abort=*/false);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int local = 0;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++local) {
+                const int buf = local & 1;
+                const uint32_t tph = (local >> 1) & 1;
+                if (!wait_bounded(tempty(buf), tph ^ 1u, wc, timeout_code(ROLE_MMA, 0x100 + buf))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(full(stage), phase, wc, timeout_code(ROLE_MMA, stage))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * Cfg::A_BYTES;
+                    const uint32_t b0 = sB + stage * Cfg::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(b0 + k * 16 * 128, Cfg::B_BLOCK, 1024);
+                        umma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty(stage));
+                    if (++stage == Cfg::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull(buf));
+            }
+            // Teardown: every MMA issued has completed before TMEM is freed.
+            umma_commit(drain);
+            wait_bounded(drain, 0, wc, 0, /*honor_abort=*/false);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;   // TMEM lane quarter this warp may read
+        const int ew = warp - 2;  // staging slot
+        const uint32_t stg = sC + ew * STG_BUFS * STG_BYTES;
+        float *stg_f = reinterpret_cast<float *>(smem + Cfg::SMEM_C + ew * STG_BUFS * STG_BYTES);
+        int sbuf = 0;
+        int local = 0;
+        for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
+            int b, mt, nt;
+            tile_coords(p, t, b, mt, nt);
+            const int buf = local & 1;
+            const uint32_t tph = (local >> 1) & 1;
+            if (!wait_bounded_warp(tfull(buf), tph, wc, timeout_code(ROLE_EPILOGUE, buf))) break;
+            tc_fence_after();
+            const uint32_t tbase =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+            const int row0 = mt * BM + q * 32;
+            const int col0 = nt * BN;
+            if constexpr (TMA_STORE) {
+                constexpr int CW = (OUT == OUT_F32) ? 32 : 64;  // columns per 128-byte row
+                constexpr int NCH = BN / CW;
+#pragma unroll 1
+                for (int c = 0; c < NCH; ++c) {
+                    uint32_t pk[32];
+                    if constexpr (OUT == OUT_F32) {
+                        tmem_ld32(tbase + c * 32, pk);
+                    } else {
+                        uint32_t lo[32], hi[32];
+                        tmem_ld32(tbase + c * 64, lo);
+                        tmem_ld32(tbase + c * 64 + 32, hi);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            pk[i] = pack2<OUT>(lo[2 * i], lo[2 * i + 1]);
+                            pk[16 + i] = pack2<OUT>(hi[2 * i], hi[2 * i + 1]);
+                        }
+                    }
+                    if (c == NCH - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty(buf));
+                    }
+                    if (lane == 0) bulk_wait_read<STG_BUFS - 1>();
+                    __syncwarp();
+                    const uint32_t row_addr = stg + sbuf * STG_BYTES + lane * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4), pk[4 * j], pk[4 * j + 1],
+                                     pk[4 * j + 2], pk[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tmC, stg + sbuf * STG_BYTES, col0 + c * CW, row0, b);
+                        bulk_commit();
+                    }
+                    sbuf ^= 1;
+                }
+            } else {
+                // Predicated coalesced stores: transpose each 32 x 32 chunk
+                // through shared memory (element (r, c) at r*32 + (c ^ r), so
+                // both the row-wise writes and the column-wise reads hit 32
+                // distinct banks), then lane l writes column l of every row.
+                char *Cb = static_cast<char *>(p.C);
+                const int64_t esz = (OUT == OUT_F32) ? 4 : 2;
+                const int64_t base = static_cast<int64_t>(b) * p.strideC;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c * 32, v);
+                    if (c == BN / 32 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty(buf));
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) stg_f[lane * 32 + (j ^ lane)] = __uint_as_float(v[j]);
+                    __syncwarp();
+                    const int col = col0 + c * 32 + lane;
+                    if (col < p.N) {
+                        for (int r = 0; r < 32; ++r) {
+                            const int row = row0 + r;
+                            if (row >= p.M) break;
+                            store_one<OUT>(Cb, base + static_cast<int64_t>(row) * p.ldc + col,
+                                           stg_f[r * 32 + (lane ^ r)]);
+                        }
+                    }
+                    (void)esz;
+                }
+            }
+        }
+        if (TMA_STORE && lane == 0) bulk_wait<0>();
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <int BN, int OUT, bool TS>
+cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                        const TiledParams &p, int grid, cudaStream_t stream) {
+    auto kern = hgemm_tiled_kernel<BN, OUT, TS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TiledCfg<BN>::SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, NUM_THREADS, TiledCfg<BN>::SMEM_TOTAL, stream>>>(tmA, tmB, tmC, p);
+    return cudaGetLastError();
+}
+
+template <int BN, int OUT>
+cudaError_t launch_ts(bool ts, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                      const CUtensorMap &tmC, const TiledParams &p, int grid, cudaStream_t s) {
+    return ts ? launch_impl<BN, OUT, true>(tmA, tmB, tmC, p, grid, s)
+              : launch_impl<BN, OUT, false>(tmA, tmB, tmC, p, grid, s);
+}
+
+template <int BN>
+cudaError_t launch_out(int out, bool ts, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                       const CUtensorMap &tmC, const TiledParams &p, int grid, cudaStream_t s) {
+    switch (out) {
+        case OUT_F16: return launch_ts<BN, OUT_F16>(ts, tmA, tmB, tmC, p, grid, s);
+        case OUT_BF16: return launch_ts<BN, OUT_BF16>(ts, tmA, tmB, tmC, p, grid, s);
+        case OUT_F32: return launch_ts<BN, OUT_F32>(ts, tmA, tmB, tmC, p, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+int tiled_smem_bytes(int bn) {
+    return bn == 256 ? TiledCfg<256>::SMEM_TOTAL : TiledCfg<128>::SMEM_TOTAL;
+}
+
+int tiled_stages(int bn) { return bn == 256 ? TiledCfg<256>::STAGES : TiledCfg<128>::STAGES; }
+
+cudaError_t launch_tiled(int bn, int out, bool tma_store, const CUtensorMap &tmA,
+                         const CUtensorMap &tmB, const CUtensorMap &tmC, const TiledParams &p,
+                         int grid, cudaStream_t stream) {
+    if (bn == 256) return launch_out<256>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
+    if (bn == 128) return launch_out<128>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hg

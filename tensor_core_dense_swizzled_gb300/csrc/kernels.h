@@ -1,0 +1,82 @@
+// kernels.h -- parameter blocks and host launchers of libhgemm's kernels.
+// Shared by the kernel translation units and the C-ABI layer (api.cpp); no
+// device code here.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hg {
+
+enum OutType : int { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
+
+// Instruction descriptor of tcgen05.mma .kind::f16 with an fp32 accumulator:
+//   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16,
+//   1 = bf16), 15 A major (0 = K, 1 = MN), 16 B major, 17-22 N >> 3,
+//   24-28 M >> 4.
+constexpr uint32_t idesc_f16(uint32_t ab_bf16, uint32_t a_mn, uint32_t b_mn,
+                                                 uint32_t m, uint32_t n) {
+    return (1u << 4) | (ab_bf16 << 7) | (ab_bf16 << 10) | (a_mn << 15) | (b_mn << 16) |
+           ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Persistent tiled kernel: 128 x BN output tiles, BK = 64, TMEM accumulators.
+struct TiledParams {
+    int32_t M, N, K, batch;
+    int32_t num_m, num_n, num_kb;  // tiles along M, N; 64-wide K blocks
+    int32_t tiles;                 // batch * num_m * num_n
+    int32_t group_m;               // raster: m-tiles per group (L2 reuse)
+    uint32_t idesc;                // tcgen05 instruction descriptor
+    void *C;                       // generic (non-TMA) epilogue only
+    int64_t ldc, strideC;
+    int32_t *err;                  // device error word
+    uint64_t timeout_ns;
+};
+
+// Skinny kernel: C^T = B^T . A^T, 128 output columns of C per tile, split-K.
+struct SkinnyParams {
+    int32_t M, N, K, batch;
+    int32_t num_n;        // 128-wide n tiles
+    int32_t num_kb;       // 64-wide K blocks in total
+    int32_t split;        // K splits
+    int32_t kb_per_split; // K blocks per split (last split may have fewer)
+    int32_t units;        // batch * split * num_n
+    uint32_t idesc;
+    void *C;
+    int64_t ldc, strideC;
+    float *partials;      // [batch][split][num_n][NU][128] fp32 (split > 1)
+    int32_t *counters;    // [batch][num_n][4] arrival counters (one per epilogue warp), zero between runs
+    int32_t *err;
+    uint64_t timeout_ns;
+};
+
+// Shared memory the tiled kernel needs for a given BN (bytes, incl. alignment slack).
+int tiled_smem_bytes(int bn);
+int tiled_stages(int bn);
+int skinny_smem_bytes(int nu);
+int skinny_stages(int nu);
+
+// Launchers return cudaSuccess or the launch error.  `out` is an OutType.
+cudaError_t launch_tiled(int bn, int out, bool tma_store, const CUtensorMap &tmA,
+                         const CUtensorMap &tmB, const CUtensorMap &tmC, const TiledParams &p,
+                         int grid, cudaStream_t stream);
+
+cudaError_t launch_skinny(int nu, int out, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                          const SkinnyParams &p, int grid, cudaStream_t stream);
+
+// Copies a batch of rows x cols 16-bit matrices (leading dimension ld_src,
+// batch stride stride_src, any alignment) into dst with leading dimension
+// ld_dst (a multiple of 8) and batch stride stride_dst (16-byte aligned).
+cudaError_t launch_repack16(const void *src, int64_t ld_src, int64_t stride_src, void *dst,
+                            int64_t ld_dst, int64_t stride_dst, int64_t rows, int64_t cols,
+                            int64_t batch, int num_sms, cudaStream_t stream);
+
+// Writes zeros into a batch of rows x cols blocks of `elem_bytes`-byte elements.
+cudaError_t launch_zero_fill(void *C, int64_t ldc, int64_t strideC, int64_t rows, int64_t cols,
+                             int64_t batch, int elem_bytes, int num_sms, cudaStream_t stream);
+
+// One-warp kernel waiting on an mbarrier nothing signals (watchdog self-test).
+cudaError_t launch_watchdog_selftest(int32_t *err, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace hg

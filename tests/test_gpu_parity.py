@@ -1,0 +1,492 @@
+"""Parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Acceptance (fixed by the method's statement of the target):
+  * integer-valued inputs whose sums are exact in fp32: bit-exact;
+  * otherwise ``max |C - Cref| / Den <= 1e-3`` for fp32 output and
+    ``<= 4e-3`` for fp16/bf16 output, with ``Den = sum_k |A_ik||B_kj|``
+    (entries with ``Den == 0`` must be exactly zero).
+These are bounds, not fudge: fp32 accumulation of K products in any order is
+within about K * 2^-24 * Den (4.9e-4 at K = 8192) and rounding the result to
+fp16 / bf16 adds at most 2^-11 / 2^-9 relative to |C| <= Den.
+
+Small cases are compared element by element with the full oracle product;
+the full-size workloads, in the launch configuration the bench times, are
+compared on sampled entries the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tensor_core_dense_swizzled_gb300 import hgemm as H
+from tensor_core_dense_swizzled_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f16": H.HGEMM_F16, "bf16": H.HGEMM_BF16, "f32": H.HGEMM_F32}
+ORACLE_DT = {"f16": 0, "bf16": 1}
+TOL = {"f32": 1e-3, "f16": 4e-3, "bf16": 4e-3}
+TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    oracle.build()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+def bits(t):
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16).reshape(-1)
+
+
+def span(rows, cols, ld, batch, stride):
+    if rows == 0 or cols == 0:
+        return 0
+    return (batch - 1) * stride + (rows - 1) * ld + cols
+
+
+def read_c(flat_dev, dout, M, N, ldc, batch, sC, off):
+    """Logical (batch, M, N) view of the device C buffer, as fp64 numpy read
+    with the oracle's decoder for 16-bit outputs."""
+    flat = flat_dev.cpu()
+    view = torch.as_strided(flat, (batch, M, N), (sC, ldc, 1), off)
+    if dout == "f32":
+        return view.double().numpy()
+    return oracle.decode(bits(view), ORACLE_DT[dout]).reshape(batch, M, N)
+
+
+SENTINEL = {"f32": 12345.0, "f16": 1234.0, "bf16": 1234.0}
+
+
+def run_case(dev, M, N, K, din, dout, *, lda=None, ldb=None, ldc=None, batch=1, sA=None,
+             sB=None, sC=None, seed=0, dist_a="normal", dist_b="normal", scale_b=1.0,
+             off_a=0, off_b=0, off_c=0, options=None, A_flat=None, B_flat=None, runs=1):
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    sA = (M * lda if batch > 1 else 0) if sA is None else sA
+    sB = (K * ldb if batch > 1 else 0) if sB is None else sB
+    sC = (M * ldc if batch > 1 else 0) if sC is None else sC
+    nA = off_a + max(span(M, K, lda, batch, sA), 1)
+    nB = off_b + max(span(K, N, ldb, batch, sB), 1)
+    nC = off_c + max(span(M, N, ldc, batch, sC), 1)
+    if A_flat is None:
+        A_flat = inputs.make_random((nA,), din, seed, dist_a)
+    if B_flat is None:
+        B_flat = inputs.make_random((nB,), din, seed + 1, dist_b, scale_b)
+    dA = A_flat.to(dev)
+    dB = B_flat.to(dev)
+    dC = torch.full((nC,), SENTINEL[dout], dtype=TORCH[dout], device=dev)
+    esz_in, esz_out = 2, dC.element_size()
+    plan = H.hgemm_plan_create_ex(M, N, K, lda, ldb, ldc, batch, sA, sB, sC, DT[din], DT[dout],
+                                  options)
+    try:
+        info = H.hgemm_plan_get_info(plan)
+        outs = []
+        for _ in range(runs):
+            H.hgemm_run(plan, dA.data_ptr() + off_a * esz_in, dB.data_ptr() + off_b * esz_in,
+                        dC.data_ptr() + off_c * esz_out)
+            st = H.hgemm_check(plan)
+            assert st == 0, f"hgemm_check: {H.STATUS.get(st)} {H.hgemm_last_error_detail()}"
+            outs.append(dC.clone())
+    finally:
+        H.hgemm_plan_destroy(plan)
+    Cref, Den = oracle.gemm(bits(A_flat)[off_a:], bits(B_flat)[off_b:], ORACLE_DT[din], M, N, K,
+                            lda, ldb, batch, sA, sB)
+    got = read_c(dC, dout, M, N, ldc, batch, sC, off_c)
+    # elements of the C buffer outside the logical matrices are untouched
+    mask = torch.ones(nC, dtype=torch.bool)
+    if M and N:
+        idx = torch.as_strided(torch.arange(nC), (batch, M, N), (sC, ldc, 1), off_c).reshape(-1)
+        mask[idx] = False
+    outside = dC.cpu()[mask]
+    assert torch.all(outside == SENTINEL[dout]), "kernel wrote outside C"
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0]), "repeated runs differ"
+    return got, Cref, Den, info
+
+
+def check(got, Cref, Den, dout, exact=False):
+    if exact:
+        assert np.array_equal(got, Cref), f"max |diff| {np.max(np.abs(got - Cref))}"
+        return 0.0
+    err = oracle.normalized_error(got, Cref, Den)
+    assert err <= TOL[dout], f"normalised error {err:.3e} > {TOL[dout]}"
+    return err
+
+
+# ---------------------------------------------------------------- worked example
+
+@pytest.mark.parametrize("din", ["f16", "bf16"])
+@pytest.mark.parametrize("dout", ["f32", "f16", "bf16"])
+def test_worked_example(dev, din, dout):
+    """A[i][k] = i, B[k][j] = j on a 16 x 8 x 16 tile gives D[i][j] = 16*i*j
+    ("post_1787550000", section 6.1); every value is exact in every output
+    type, so the result must match bit for bit."""
+    A = torch.arange(16, dtype=torch.float32).repeat_interleave(16).to(TORCH[din])
+    B = torch.arange(8, dtype=torch.float32).repeat(16).to(TORCH[din])
+    got, Cref, Den, _ = run_case(dev, 16, 8, 16, din, dout, A_flat=A, B_flat=B)
+    check(got, Cref, Den, dout, exact=True)
+    assert got[0, 3, 5] == 240 and got[0, 15, 7] == 1680
+
+
+@pytest.mark.parametrize("path", [H.HGEMM_PATH_TILED, H.HGEMM_PATH_SKINNY])
+def test_worked_example_both_paths(dev, path):
+    A = torch.arange(16, dtype=torch.float32).repeat_interleave(16).to(torch.float16)
+    B = torch.arange(8, dtype=torch.float32).repeat(16).to(torch.float16)
+    got, Cref, Den, info = run_case(dev, 16, 8, 16, "f16", "f32", A_flat=A, B_flat=B,
+                                    options=H.Options(force_path=path))
+    assert info["path"] == path
+    check(got, Cref, Den, "f32", exact=True)
+
+
+# ---------------------------------------------------------------- layout locators
+
+@pytest.mark.parametrize("din", ["f16", "bf16"])
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_identity_B_returns_A(dev, din, tile_n):
+    """B = I: C must equal A exactly (fp32 out).  A wrong descriptor stride,
+    swizzle or major-ness scrambles rows or columns of C."""
+    M = K = N = 320
+    A = inputs.make_random((M * K,), din, 3)
+    B = torch.eye(K, dtype=torch.float32).reshape(-1).to(TORCH[din])
+    got, Cref, Den, _ = run_case(dev, M, N, K, din, "f32", A_flat=A, B_flat=B,
+                                 options=H.Options(tile_n=tile_n))
+    check(got, Cref, Den, "f32", exact=True)
+
+
+@pytest.mark.parametrize("din", ["f16", "bf16"])
+def test_one_hot_rows(dev, din):
+    """A[i][k] = [k == i mod K]: row i of C is row (i mod K) of B exactly."""
+    M, N, K = 256, 384, 192
+    A = torch.zeros(M, K)
+    A[torch.arange(M), torch.arange(M) % K] = 1.0
+    B = inputs.make_random((K * N,), din, 4)
+    got, Cref, Den, _ = run_case(dev, M, N, K, din, "f32", A_flat=A.reshape(-1).to(TORCH[din]),
+                                 B_flat=B)
+    check(got, Cref, Den, "f32", exact=True)
+
+
+# ---------------------------------------------------------------- integer workload
+
+def test_int512_bit_exact(dev):
+    """512^3 fp16 integers in [-4, 4] (seed 0), fp32 out: every partial sum is
+    an integer below 2^24, so any summation order is exact."""
+    w = inputs.WORKLOADS["int512"]
+    A, B = inputs.make_inputs(w)
+    got, Cref, Den, info = run_case(dev, w.M, w.N, w.K, w.dtype_in, w.dtype_out,
+                                    A_flat=A.reshape(-1), B_flat=B.reshape(-1))
+    assert info["path"] == H.HGEMM_PATH_TILED
+    check(got, Cref, Den, "f32", exact=True)
+
+
+@pytest.mark.parametrize("dout", ["f16", "bf16"])
+def test_int_small_exact_16bit_out(dev, dout):
+    """Small integer products whose results fit the output format exactly."""
+    M, N, K = 200, 136, 24  # |C| <= 24*16 = 384: an integer, exact in fp16 (not always in bf16)
+    A = inputs.make_random((M * K,), "f16", 9, "int4")
+    B = inputs.make_random((K * N,), "f16", 10, "int4")
+    got, Cref, Den, _ = run_case(dev, M, N, K, "f16", dout, A_flat=A, B_flat=B)
+    if dout == "f16":
+        check(got, Cref, Den, dout, exact=True)
+    else:
+        check(got, Cref, Den, dout)
+
+
+# ---------------------------------------------------------------- random ragged shapes
+
+SHAPES = [(33, 40, 17), (128, 256, 64), (129, 257, 65), (300, 520, 200), (511, 383, 130),
+          (256, 512, 1024), (640, 1000, 333), (1024, 768, 2048)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f16", "f32"), ("bf16", "f32"),
+                                      ("f16", "f16")])
+def test_random_shapes(dev, shape, din, dout):
+    M, N, K = shape
+    got, Cref, Den, info = run_case(dev, M, N, K, din, dout, seed=M + N + K)
+    assert info["path"] == H.HGEMM_PATH_TILED
+    check(got, Cref, Den, dout)
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("dout", ["f32", "bf16"])
+def test_tile_variants(dev, tile_n, dout):
+    M, N, K = 390, 700, 300
+    got, Cref, Den, info = run_case(dev, M, N, K, "bf16", dout, seed=5,
+                                    options=H.Options(tile_n=tile_n))
+    assert info["tile_n"] == tile_n
+    check(got, Cref, Den, dout)
+
+
+def test_many_tiles_per_cta(dev):
+    """More tiles than SMs: every CTA loops, both TMEM buffers and the stage
+    ring wrap many times."""
+    M, N, K = 2560, 2304, 256
+    got, Cref, Den, info = run_case(dev, M, N, K, "f16", "f16", seed=6)
+    assert info["grid"] < (M // 128) * (N // 256)  # 180 tiles
+    check(got, Cref, Den, "f16")
+
+
+# ---------------------------------------------------------------- strides, alignment, batches
+
+@pytest.mark.parametrize("dout", ["f32", "f16"])
+def test_padded_leading_dimensions(dev, dout):
+    M, N, K = 200, 300, 150
+    got, Cref, Den, info = run_case(dev, M, N, K, "f16", dout, lda=K + 40, ldb=N + 24,
+                                    ldc=N + 8, seed=11)
+    assert not info["repack_a"] and not info["repack_b"]
+    check(got, Cref, Den, dout)
+
+
+@pytest.mark.parametrize("dout", ["f32", "f16", "bf16"])
+def test_misaligned_leading_dimensions(dev, dout):
+    """Odd leading dimensions: A and B are copied to aligned workspace and C
+    is written with predicated stores."""
+    M, N, K = 255, 257, 129
+    din = "bf16" if dout == "bf16" else "f16"
+    got, Cref, Den, info = run_case(dev, M, N, K, din, dout, lda=K, ldb=N, ldc=N, seed=12)
+    assert info["repack_a"] and info["repack_b"] and not info["tma_store"]
+    check(got, Cref, Den, dout)
+
+
+def test_misaligned_base_pointers(dev):
+    """Aligned leading dimensions but base pointers off by one element."""
+    M, N, K = 256, 264, 136
+    got, Cref, Den, _ = run_case(dev, M, N, K, "bf16", "f32", off_a=1, off_b=3, off_c=1, seed=13)
+    check(got, Cref, Den, "f32")
+
+
+@pytest.mark.parametrize("opt", [H.Options(force_repack=1), H.Options(force_generic_store=1),
+                                 H.Options(force_repack=1, force_generic_store=1)])
+def test_forced_fallbacks_match(dev, opt):
+    M, N, K = 333, 444, 222
+    got, Cref, Den, _ = run_case(dev, M, N, K, "bf16", "bf16", seed=14, options=opt)
+    check(got, Cref, Den, "bf16")
+
+
+@pytest.mark.parametrize("dout", ["f32", "bf16"])
+def test_batched_strided(dev, dout):
+    M, N, K, batch = 130, 200, 96, 5
+    lda, ldb, ldc = K + 8, N + 16, N + 8
+    sA, sB, sC = M * lda + 64, K * ldb + 8, M * ldc + 24
+    got, Cref, Den, _ = run_case(dev, M, N, K, "bf16", dout, lda=lda, ldb=ldb, ldc=ldc, batch=batch,
+                                 sA=sA, sB=sB, sC=sC, seed=15)
+    check(got, Cref, Den, dout)
+
+
+def test_batched_misaligned_strides(dev):
+    M, N, K, batch = 70, 90, 50, 3
+    got, Cref, Den, info = run_case(dev, M, N, K, "f16", "f32", batch=batch,
+                                    sA=M * K + 1, sB=K * N + 3, sC=M * N + 1, seed=16)
+    assert info["repack_a"] and info["repack_b"]
+    check(got, Cref, Den, "f32")
+
+
+def test_batch_stride_zero_broadcasts_B(dev):
+    """strideB = 0 reuses one B for every batch."""
+    M, N, K, batch = 128, 256, 64, 4
+    got, Cref, Den, _ = run_case(dev, M, N, K, "bf16", "f32", batch=batch, sB=0, seed=17)
+    check(got, Cref, Den, "f32")
+
+
+# ---------------------------------------------------------------- degenerate sizes
+
+@pytest.mark.parametrize("dout", ["f32", "f16", "bf16"])
+def test_k_zero_writes_zeros(dev, dout):
+    got, Cref, Den, info = run_case(dev, 37, 53, 0, "f16", dout, lda=1, ldb=53)
+    assert info["path"] == H.HGEMM_PATH_ZERO_FILL
+    assert np.all(got == 0)
+    check(got, Cref, Den, dout, exact=True)
+
+
+@pytest.mark.parametrize("M,N", [(0, 10), (10, 0), (0, 0)])
+def test_empty_output_is_a_no_op(dev, M, N):
+    got, Cref, Den, info = run_case(dev, M, N, 16, "f16", "f32", lda=16, ldb=max(N, 1),
+                                    ldc=max(N, 1))
+    assert info["path"] == H.HGEMM_PATH_EMPTY and info["kernels_per_run"] == 0
+
+
+def test_zero_rows_give_exact_zeros(dev):
+    """A zero row and a zero column make Den == 0 entries: they must be 0."""
+    M, N, K = 150, 270, 80
+    A = inputs.make_random((M * K,), "bf16", 18).reshape(M, K)
+    A[7] = 0
+    B = inputs.make_random((K * N,), "bf16", 19).reshape(K, N)
+    B[:, 100] = 0
+    got, Cref, Den, _ = run_case(dev, M, N, K, "bf16", "bf16", A_flat=A.reshape(-1),
+                                 B_flat=B.reshape(-1))
+    assert np.all(got[0, 7] == 0) and np.all(got[0, :, 100] == 0)
+    check(got, Cref, Den, "bf16")
+
+
+def test_single_element(dev):
+    got, Cref, Den, _ = run_case(dev, 1, 1, 1, "f16", "f32", seed=20)
+    check(got, Cref, Den, "f32")
+
+
+def test_k_not_multiple_of_16(dev):
+    for K in (1, 7, 15, 17, 63, 65):
+        got, Cref, Den, _ = run_case(dev, 140, 130, K, "f16", "f32", lda=K + (-K) % 8,
+                                     seed=21 + K)
+        check(got, Cref, Den, "f32")
+
+
+# ---------------------------------------------------------------- skinny path
+
+@pytest.mark.parametrize("M", [1, 8, 16, 17, 32])
+@pytest.mark.parametrize("dout", ["bf16", "f32"])
+def test_skinny_shapes(dev, M, dout):
+    N, K = 1000, 640
+    got, Cref, Den, info = run_case(dev, M, N, K, "bf16", dout, seed=30 + M, scale_b=0.02)
+    assert info["path"] == H.HGEMM_PATH_SKINNY
+    check(got, Cref, Den, dout)
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 5, 10])
+def test_skinny_split_k(dev, split):
+    M, N, K = 8, 777, 640
+    got, Cref, Den, info = run_case(dev, M, N, K, "bf16", "bf16", seed=40,
+                                    options=H.Options(split_k=split), runs=3)
+    assert info["split_k"] == split
+    check(got, Cref, Den, "bf16")
+
+
+def test_skinny_batched_and_misaligned(dev):
+    M, N, K, batch = 5, 300, 200, 3
+    got, Cref, Den, info = run_case(dev, M, N, K, "f16", "f16", batch=batch, ldb=N + 1,
+                                    sB=K * (N + 1) + 5, seed=41)
+    assert info["path"] == H.HGEMM_PATH_SKINNY and info["repack_b"]
+    check(got, Cref, Den, "f16")
+
+
+def test_skinny_matches_tiled(dev):
+    """The two paths compute the same product: both within the bound, and
+    equal to each other within twice the bound."""
+    M, N, K = 16, 640, 512
+    g1, Cref, Den, _ = run_case(dev, M, N, K, "bf16", "f32", seed=42,
+                                options=H.Options(force_path=H.HGEMM_PATH_SKINNY))
+    g2, _, _, _ = run_case(dev, M, N, K, "bf16", "f32", seed=42,
+                           options=H.Options(force_path=H.HGEMM_PATH_TILED))
+    check(g1, Cref, Den, "f32")
+    check(g2, Cref, Den, "f32")
+
+
+# ---------------------------------------------------------------- full-size workloads (sampled)
+
+def sample_entries(batch, M, N, n, seed):
+    rng = np.random.default_rng(seed)
+    eb = list(rng.integers(0, batch, n))
+    ei = list(rng.integers(0, M, n))
+    ej = list(rng.integers(0, N, n))
+    for b in {0, batch - 1}:  # corners and the ragged last row/column
+        for i in (0, M - 1):
+            for j in (0, N - 1):
+                eb.append(b); ei.append(i); ej.append(j)
+        for j in rng.integers(0, N, 32):
+            eb.append(b); ei.append(M - 1); ej.append(int(j))
+        for i in rng.integers(0, M, 32):
+            eb.append(b); ei.append(int(i)); ej.append(N - 1)
+    return np.array(eb), np.array(ei), np.array(ej)
+
+
+@pytest.mark.parametrize("name", ["square4096", "square8192", "batched_qk", "ragged4095",
+                                  "ragged4095_h", "skinny"])
+def test_workload_full_size_sampled(dev, name):
+    w = inputs.WORKLOADS[name]
+    A, B = inputs.make_inputs(w)
+    dA, dB = A.to(dev), B.to(dev)
+    shape = (w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N)
+    C = torch.empty(shape, dtype=TORCH[w.dtype_out], device=dev)
+    plan = H.hgemm_plan_create(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, w.batch, w.strideA, w.strideB,
+                               w.strideC, DT[w.dtype_in], DT[w.dtype_out])
+    try:
+        H.hgemm_run(plan, dA, dB, C)
+        st = H.hgemm_check(plan)
+        assert st == 0, H.hgemm_last_error_detail()
+    finally:
+        H.hgemm_plan_destroy(plan)
+    Cc = C.reshape(w.batch, w.M, w.N).cpu()
+    eb, ei, ej = sample_entries(w.batch, w.M, w.N, 3000, 99)
+    cref, den = oracle.gemm_entries(bits(A), bits(B), ORACLE_DT[w.dtype_in], w.K, w.lda, w.ldb,
+                                    eb, ei, ej, w.strideA, w.strideB)
+    vals = Cc[torch.as_tensor(eb), torch.as_tensor(ei), torch.as_tensor(ej)]
+    if w.dtype_out == "f32":
+        got = vals.double().numpy()
+    else:
+        got = oracle.decode(bits(vals), ORACLE_DT[w.dtype_out])
+    err = oracle.normalized_error(got, cref, den)
+    assert err <= TOL[w.dtype_out], f"{name}: normalised error {err:.3e}"
+    # properties that hold everywhere: finite output
+    assert torch.isfinite(Cc.float()).all()
+
+
+def test_batched_qk_full_compare(dev):
+    """The batched attention-shaped workload is small enough for the full
+    oracle product: every element is checked."""
+    w = inputs.WORKLOADS["batched_qk"]
+    A, B = inputs.make_inputs(w)
+    got, Cref, Den, info = run_case(dev, w.M, w.N, w.K, w.dtype_in, w.dtype_out, batch=w.batch,
+                                    A_flat=A.reshape(-1), B_flat=B.reshape(-1))
+    check(got, Cref, Den, w.dtype_out)
+
+
+# ---------------------------------------------------------------- API surface
+
+def test_one_shot_and_matmul(dev):
+    from tensor_core_dense_swizzled_gb300 import matmul
+    A = inputs.make_random((300, 200), "bf16", 50)
+    B = inputs.make_random((200, 260), "bf16", 51)
+    C1 = matmul(A.to(dev), B.to(dev), out_dtype=torch.float32)
+    C2 = matmul(A.to(dev), B.to(dev), out_dtype=torch.float32)  # cached plan
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    Cref, Den = oracle.gemm(bits(A), bits(B), 1, 300, 260, 200, 200, 260)
+    check(C1.cpu().double().numpy()[None], Cref, Den, "f32")
+    # batched front end
+    Ab = inputs.make_random((3, 64, 80), "f16", 52)
+    Bb = inputs.make_random((3, 80, 48), "f16", 53)
+    Cb = matmul(Ab.to(dev), Bb.to(dev))
+    Cref, Den = oracle.gemm(bits(Ab), bits(Bb), 0, 64, 48, 80, 80, 48, 3, 64 * 80, 80 * 48)
+    check(oracle.decode(bits(Cb), 0).reshape(3, 64, 48), Cref, Den, "f16")
+    H.hgemm_cache_clear()
+
+
+def test_run_host_end_to_end(dev):
+    M, N, K = 257, 320, 130
+    A = inputs.make_random((M, K), "f16", 60).pin_memory()
+    B = inputs.make_random((K, N), "f16", 61).pin_memory()
+    C = torch.full((M, N + 8), -7.0, dtype=torch.float32).pin_memory()
+    plan = H.hgemm_plan_create(M, N, K, K, N, N + 8, 1, 0, 0, 0, H.HGEMM_F16, H.HGEMM_F32)
+    try:
+        H.hgemm_run_host(plan, A, B, C)
+    finally:
+        H.hgemm_plan_destroy(plan)
+    assert torch.all(C[:, N:] == -7.0)
+    Cref, Den = oracle.gemm(bits(A), bits(B), 0, M, N, K, K, N)
+    check(C[:, :N].double().numpy()[None], Cref, Den, "f32")
+
+
+def test_watchdog_selftest(dev):
+    """A wait that can never complete gives up after its limit and reports
+    HGEMM_ERR_TIMEOUT; the context stays usable afterwards."""
+    st, code = H.hgemm_watchdog_selftest(2_000_000)  # 2 ms
+    assert st == 6
+    assert code & 0x80000000 and ((code >> 16) & 0xFF) == 5
+    got, Cref, Den, _ = run_case(dev, 64, 64, 64, "f16", "f32", seed=70)
+    check(got, Cref, Den, "f32")
+
+
+def test_plan_rejects_wrong_device_pointer_use(dev):
+    plan = H.hgemm_plan_create(64, 64, 64, 64, 64, 64, 1, 0, 0, 0, H.HGEMM_F16, H.HGEMM_F32)
+    try:
+        with pytest.raises(H.HgemmError):
+            H.hgemm_run(plan, None, None, None)
+    finally:
+        H.hgemm_plan_destroy(plan)
