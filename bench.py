@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--workload", default="square4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--probe-seconds", type=float, default=1.0,
+                    help="untimed load after the timed region so the clock sampler sees the GPU busy")
     return ap.parse_args()
 
 
@@ -195,14 +197,6 @@ def committed_traffic(workload: str):
     except Exception:
         pass
     return None
-
-
-def workload_numbers(w):
-    import oracle  # only for the FLOP / byte formulas used in the report
-    flops = oracle.flops(w.M, w.N, w.K, w.batch)
-    ob = 4 if w.dtype_out == "f32" else 2
-    nbytes = oracle.min_bytes(w.M, w.N, w.K, 2, ob, w.batch)
-    return flops, nbytes, ob
 
 
 def flops_of(w):
@@ -357,7 +351,7 @@ def run_ours(args, w, world, rank, local, pg):
     region_ms = starts[0].elapsed_time(ends[-1])
     per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     # keep the GPU busy (untimed) long enough for the clock sampler to see it
-    probe_until = t_wall0 + 1.0
+    probe_until = t_wall0 + args.probe_seconds
     j = 0
     while time.time() < probe_until:
         for _ in range(50):

@@ -76,7 +76,7 @@ typedef struct {
     int force_path;           /* 0: automatic; HGEMM_PATH_TILED or HGEMM_PATH_SKINNY to force */
     int force_generic_store;  /* 1: predicated st.global epilogue even when C suits TMA */
     int force_repack;         /* 1: copy A and B to aligned workspace even when aligned */
-    int tile_n;               /* 0: automatic; 128 or 256 (tiled path) */
+    int tile_n;               /* 0: automatic; 128, 192, 224 or 256 (tiled path) */
     int split_k;              /* 0: automatic; >= 1 (skinny path) */
     uint64_t timeout_ns;      /* 0: default (2 s); device watchdog for each pipeline wait */
 } hgemm_options_t;

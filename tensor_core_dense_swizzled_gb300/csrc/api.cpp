@@ -69,7 +69,8 @@ inline int out_type(hgemm_dtype_t d) {
 // given element size, leading dimension and batch stride (elements).
 hgemm_status_t encode_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dt, int esize,
                          int64_t cols, int64_t rows, int64_t batch, int64_t ld, int64_t stride,
-                         uint32_t box_cols, uint32_t box_rows) {
+                         uint32_t box_cols, uint32_t box_rows,
+                         CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = encode_fn();
     if (!fn) return fail(HGEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     int64_t bstride = stride * esize;
@@ -80,8 +81,8 @@ hgemm_status_t encode_3d(CUtensorMap *map, const void *base, CUtensorMapDataType
     cuuint32_t box[3] = {box_cols, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(HGEMM_ERR_CUDA,
                     "cuTensorMapEncodeTiled failed (%d): dims %lld x %lld x %lld, ld %lld, "
@@ -184,6 +185,29 @@ int choose_split(int64_t work_tiles, int num_kb, int num_sms) {
     return best;
 }
 
+// Picks the tile width of the tiled path.  A persistent CTA processes its
+// tiles in rounds ("waves") of one tile per SM; the time is about
+// waves x (BN + overhead), where the overhead (pipeline fill and drain, the
+// last tile's epilogue) is worth about 16 columns of main loop.  A tile
+// width that makes the tile count a multiple of the SM count wins: 4096^2
+// gives 608 tiles of 128 x 224 = 4 waves exactly, against 512 tiles of
+// 128 x 256 = 3.4 waves that take 4.
+int choose_tile_n(int64_t batch, int64_t M, int64_t N, int sms) {
+    static const int cands[] = {256, 224, 192, 128};
+    int best = 256;
+    double best_t = 1e300;
+    for (int bn : cands) {
+        const int64_t tiles = batch * ceil_div(M, 128) * ceil_div(N, bn);
+        const int64_t waves = ceil_div(tiles, sms);
+        const double t = static_cast<double>(waves) * (bn + 16);
+        if (t < best_t - 1e-9) {
+            best_t = t;
+            best = bn;
+        }
+    }
+    return best;
+}
+
 hgemm_status_t alloc_workspace(hgemm_plan_s *p) {
     size_t off = 256;  // error word (+ padding)
     p->off_counters = off;
@@ -279,8 +303,9 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
     if (options) opt = *options;
     if (opt.force_path != 0 && opt.force_path != HGEMM_PATH_TILED && opt.force_path != HGEMM_PATH_SKINNY)
         return fail(HGEMM_ERR_INVALID_ARG, "force_path must be 0, HGEMM_PATH_TILED or HGEMM_PATH_SKINNY");
-    if (opt.tile_n != 0 && opt.tile_n != 128 && opt.tile_n != 256)
-        return fail(HGEMM_ERR_INVALID_ARG, "tile_n must be 0, 128 or 256");
+    if (opt.tile_n != 0 && opt.tile_n != 128 && opt.tile_n != 192 && opt.tile_n != 224 &&
+        opt.tile_n != 256)
+        return fail(HGEMM_ERR_INVALID_ARG, "tile_n must be 0, 128, 192, 224 or 256");
     if (opt.split_k < 0) return fail(HGEMM_ERR_INVALID_ARG, "split_k must be >= 0");
     if (opt.force_path == HGEMM_PATH_SKINNY && M > 32)
         return fail(HGEMM_ERR_UNSUPPORTED, "the skinny path handles M <= 32 (got %lld)", static_cast<long long>(M));
@@ -321,11 +346,16 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
     const int ob = out_bytes(dout);
     p->ld_repack_a = (lda * 2) % 16 != 0 || (batch > 1 && (p->sA * 2) % 16 != 0);
     p->ld_repack_b = (ldb * 2) % 16 != 0 || (batch > 1 && (p->sB * 2) % 16 != 0);
-    p->ldc_tma = (ldc * ob) % 16 == 0 && (batch == 1 || (p->sC * ob) % 16 == 0) && !opt.force_generic_store;
+    // TMA stores write whole 16-byte chunks: a row whose byte length is not a
+    // multiple of 16 would have the elements after column N-1 overwritten (up
+    // to the next 16-byte boundary, past the end of the last row too), so the
+    // TMA-store epilogue also needs N * sizeof(out) to be a multiple of 16.
+    p->ldc_tma = (ldc * ob) % 16 == 0 && (N * ob) % 16 == 0 &&
+                 (batch == 1 || (p->sC * ob) % 16 == 0) && !opt.force_generic_store;
 
     const int num_kb = static_cast<int>(ceil_div(K, 64));
     if (p->path == HGEMM_PATH_TILED) {
-        p->bn = opt.tile_n ? opt.tile_n : (N <= 128 ? 128 : 256);
+        p->bn = opt.tile_n ? opt.tile_n : choose_tile_n(batch, M, N, sms);
         const int64_t tiles = batch * ceil_div(M, 128) * ceil_div(N, p->bn);
         p->grid = static_cast<int>(tiles < sms ? tiles : sms);
     } else if (p->path == HGEMM_PATH_SKINNY) {
@@ -369,9 +399,10 @@ hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *
             const CUtensorMapDataType ct = p->dout == HGEMM_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                            : p->dout == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+            // 32 x 32 pieces: 128-byte rows (fp32) or 64-byte rows (fp16/bf16)
             const int ob = out_bytes(p->dout);
-            st = encode_3d(&p->tmC, C, ct, ob, p->N, p->M, p->batch, p->ldc, p->sC,
-                           static_cast<uint32_t>(128 / ob), 32);
+            st = encode_3d(&p->tmC, C, ct, ob, p->N, p->M, p->batch, p->ldc, p->sC, 32, 32,
+                           ob == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
             if (st != HGEMM_OK) return st;
         } else {
             std::memset(&p->tmC, 0, sizeof(p->tmC));

@@ -8,8 +8,8 @@
 //   warp 0, one thread   TMA producer: for every 64-deep K block waits until
 //                        the stage is empty, arms full[stage] with the byte
 //                        count (section 五.1) and issues one A box (128 x 64)
-//                        and BN/64 B boxes (64 x 64) into 128-byte-swizzled
-//                        shared memory.
+//                        and ceil(BN/64) B boxes (64 x 64) into 128-byte-
+//                        swizzled shared memory.
 //   warp 1, one thread   MMA issuer: waits full[stage], issues four
 //                        tcgen05.mma (K = 16 each) that read A and B from
 //                        shared memory through descriptors (section 五.2) and
@@ -34,7 +34,7 @@
 // the hardware form of the XOR swizzle of section 三.5: 16-byte chunk c of row
 // r goes to chunk c ^ (r & 7)):
 //   A: K-major, 128 rows x 128 bytes (64 k); descriptor SBO = 1024.
-//   B: MN-major (B is K x N row-major, so N is contiguous): BN/64 blocks of
+//   B: MN-major (B is K x N row-major, so N is contiguous): ceil(BN/64) blocks of
 //      64 k-rows x 128 bytes (64 n); descriptor LBO = 8192 (next n block),
 //      SBO = 1024 (next 8 k).  The k-th MMA of a stage starts 16 rows
 //      (2048 bytes) further.
@@ -59,20 +59,25 @@ constexpr int STG_BUFS = 2;       // per epilogue warp
 
 template <int BN>
 struct TiledCfg {
-    static_assert(BN == 128 || BN == 256, "tile N");
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static_assert(BN == 128 || BN == 192 || BN == 224 || BN == 256, "tile N");
+    static constexpr int B_BLOCKS = (BN + 63) / 64;  // 64-column blocks of B per stage
     static constexpr uint32_t A_BYTES = BM * BK * 2;
-    static constexpr uint32_t B_BYTES = BK * BN * 2;
     static constexpr uint32_t B_BLOCK = BK * 128;  // 64 k-rows x 64 n (128 bytes)
+    static constexpr uint32_t B_BYTES = B_BLOCKS * B_BLOCK;
     static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t TMEM_COLS = 2 * BN;  // two fp32 accumulators
+    static constexpr int STG_TOTAL = EPI_WARPS * STG_BUFS * STG_BYTES;
+    // as many stages as fit next to the epilogue staging (227 KB per CTA)
+    static constexpr int STAGES = (232448 - STG_TOTAL - 2048) / (A_BYTES + B_BYTES);
+    static constexpr uint32_t TMEM_STRIDE = BN <= 128 ? 128 : 256;  // column offset of buffer 1
+    static constexpr uint32_t TMEM_COLS = 2 * TMEM_STRIDE;          // two fp32 accumulators
     static constexpr int SMEM_A = 0;
     static constexpr int SMEM_B = SMEM_A + STAGES * A_BYTES;
     static constexpr int SMEM_C = SMEM_B + STAGES * B_BYTES;
-    static constexpr int SMEM_BAR = SMEM_C + EPI_WARPS * STG_BUFS * STG_BYTES;
+    static constexpr int SMEM_BAR = SMEM_C + STG_TOTAL;
     static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
     static constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_TOTAL = SMEM_MISC + 16 + 1024;  // + alignment slack
+    static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 };
 
 __device__ __forceinline__ void tile_coords(const TiledParams &p, int t, int &b, int &mt, int &nt) {
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_arrive_expect_tx(full(stage), Cfg::TX_BYTES);
                     tma_load_3d(sA + stage * Cfg::A_BYTES, &tmA, full(stage), kb * BK, mt * BM, b);
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
+                    for (int j = 0; j < Cfg::B_BLOCKS; ++j)
                         tma_load_3d(sB + stage * Cfg::B_BYTES + j * Cfg::B_BLOCK, &tmB, full(stage),
                                     nt * BN + j * 64, kb * BK, b);
                     ++issued;
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                const uint32_t d_tmem = tmem_base + buf * Cfg::TMEM_STRIDE;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bounded(full(stage), phase, wc, timeout_code(ROLE_MMA, stage))) {
                         ok = false;
@@ -270,27 +275,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!wait_bounded_warp(tfull(buf), tph, wc, timeout_code(ROLE_EPILOGUE, buf))) break;
             tc_fence_after();
             const uint32_t tbase =
-                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::TMEM_STRIDE;
             const int row0 = mt * BM + q * 32;
             const int col0 = nt * BN;
             if constexpr (TMA_STORE) {
-                constexpr int CW = (OUT == OUT_F32) ? 32 : 64;  // columns per 128-byte row
-                constexpr int NCH = BN / CW;
+                // 32 columns per piece: 128-byte rows (fp32, 128-byte swizzle:
+                // chunk j of row r at j ^ (r & 7)) or 64-byte rows (fp16/bf16,
+                // 64-byte swizzle: chunk j at j ^ ((r >> 1) & 3), the pattern
+                // of section 三.5); both keep the row-per-thread writes free
+                // of bank conflicts and match the C tensor map's swizzle.
+                constexpr int NCH = BN / 32;
 #pragma unroll 1
                 for (int c = 0; c < NCH; ++c) {
-                    uint32_t pk[32];
-                    if constexpr (OUT == OUT_F32) {
-                        tmem_ld32(tbase + c * 32, pk);
-                    } else {
-                        uint32_t lo[32], hi[32];
-                        tmem_ld32(tbase + c * 64, lo);
-                        tmem_ld32(tbase + c * 64 + 32, hi);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            pk[i] = pack2<OUT>(lo[2 * i], lo[2 * i + 1]);
-                            pk[16 + i] = pack2<OUT>(hi[2 * i], hi[2 * i + 1]);
-                        }
-                    }
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c * 32, v);
                     if (c == NCH - 1) {
                         tc_fence_before();
                         __syncwarp();
@@ -298,15 +296,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     if (lane == 0) bulk_wait_read<STG_BUFS - 1>();
                     __syncwarp();
-                    const uint32_t row_addr = stg + sbuf * STG_BYTES + lane * 128;
+                    const uint32_t piece = stg + sbuf * STG_BYTES;
+                    if constexpr (OUT == OUT_F32) {
+                        const uint32_t row_addr = piece + lane * 128;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4), pk[4 * j], pk[4 * j + 1],
-                                     pk[4 * j + 2], pk[4 * j + 3]);
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1],
+                                         v[4 * j + 2], v[4 * j + 3]);
+                    } else {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pk[i] = pack2<OUT>(v[2 * i], v[2 * i + 1]);
+                        const uint32_t row_addr = piece + lane * 64;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), pk[4 * j],
+                                         pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(&tmC, stg + sbuf * STG_BYTES, col0 + c * CW, row0, b);
+                        tma_store_3d(&tmC, piece, col0 + c * 32, row0, b);
                         bulk_commit();
                     }
                     sbuf ^= 1;
@@ -389,17 +399,35 @@ cudaError_t launch_out(int out, bool ts, const CUtensorMap &tmA, const CUtensorM
 }  // namespace
 
 int tiled_smem_bytes(int bn) {
-    return bn == 256 ? TiledCfg<256>::SMEM_TOTAL : TiledCfg<128>::SMEM_TOTAL;
+    switch (bn) {
+        case 128: return TiledCfg<128>::SMEM_TOTAL;
+        case 192: return TiledCfg<192>::SMEM_TOTAL;
+        case 224: return TiledCfg<224>::SMEM_TOTAL;
+        case 256: return TiledCfg<256>::SMEM_TOTAL;
+        default: return 0;
+    }
 }
 
-int tiled_stages(int bn) { return bn == 256 ? TiledCfg<256>::STAGES : TiledCfg<128>::STAGES; }
+int tiled_stages(int bn) {
+    switch (bn) {
+        case 128: return TiledCfg<128>::STAGES;
+        case 192: return TiledCfg<192>::STAGES;
+        case 224: return TiledCfg<224>::STAGES;
+        case 256: return TiledCfg<256>::STAGES;
+        default: return 0;
+    }
+}
 
 cudaError_t launch_tiled(int bn, int out, bool tma_store, const CUtensorMap &tmA,
                          const CUtensorMap &tmB, const CUtensorMap &tmC, const TiledParams &p,
                          int grid, cudaStream_t stream) {
-    if (bn == 256) return launch_out<256>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
-    if (bn == 128) return launch_out<128>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
-    return cudaErrorInvalidValue;
+    switch (bn) {
+        case 128: return launch_out<128>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
+        case 192: return launch_out<192>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
+        case 224: return launch_out<224>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
+        case 256: return launch_out<256>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace hg

@@ -82,7 +82,9 @@ def run_case(dev, M, N, K, din, dout, *, lda=None, ldb=None, ldc=None, batch=1, 
         B_flat = inputs.make_random((nB,), din, seed + 1, dist_b, scale_b)
     dA = A_flat.to(dev)
     dB = B_flat.to(dev)
-    dC = torch.full((nC,), SENTINEL[dout], dtype=TORCH[dout], device=dev)
+    tail = 64  # elements after the last row: must stay untouched too
+    dC_full = torch.full((nC + tail,), SENTINEL[dout], dtype=TORCH[dout], device=dev)
+    dC = dC_full[:nC]
     esz_in, esz_out = 2, dC.element_size()
     plan = H.hgemm_plan_create_ex(M, N, K, lda, ldb, ldc, batch, sA, sB, sC, DT[din], DT[dout],
                                   options)
@@ -107,6 +109,7 @@ def run_case(dev, M, N, K, din, dout, *, lda=None, ldb=None, ldc=None, batch=1, 
         mask[idx] = False
     outside = dC.cpu()[mask]
     assert torch.all(outside == SENTINEL[dout]), "kernel wrote outside C"
+    assert torch.all(dC_full[nC:].cpu() == SENTINEL[dout]), "kernel wrote past the end of C"
     for o in outs[1:]:
         assert torch.equal(o, outs[0]), "repeated runs differ"
     return got, Cref, Den, info
@@ -149,7 +152,7 @@ def test_worked_example_both_paths(dev, path):
 # ---------------------------------------------------------------- layout locators
 
 @pytest.mark.parametrize("din", ["f16", "bf16"])
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tile_n", [128, 192, 224, 256])
 def test_identity_B_returns_A(dev, din, tile_n):
     """B = I: C must equal A exactly (fp32 out).  A wrong descriptor stride,
     swizzle or major-ness scrambles rows or columns of C."""
@@ -215,8 +218,8 @@ def test_random_shapes(dev, shape, din, dout):
     check(got, Cref, Den, dout)
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
-@pytest.mark.parametrize("dout", ["f32", "bf16"])
+@pytest.mark.parametrize("tile_n", [128, 192, 224, 256])
+@pytest.mark.parametrize("dout", ["f32", "bf16", "f16"])
 def test_tile_variants(dev, tile_n, dout):
     M, N, K = 390, 700, 300
     got, Cref, Den, info = run_case(dev, M, N, K, "bf16", dout, seed=5,
@@ -239,9 +242,22 @@ def test_many_tiles_per_cta(dev):
 @pytest.mark.parametrize("dout", ["f32", "f16"])
 def test_padded_leading_dimensions(dev, dout):
     M, N, K = 200, 300, 150
-    got, Cref, Den, info = run_case(dev, M, N, K, "f16", dout, lda=K + 40, ldb=N + 24,
-                                    ldc=N + 8, seed=11)
+    got, Cref, Den, info = run_case(dev, M, N, K, "f16", dout, lda=K + 50, ldb=N + 20,
+                                    ldc=N + 12, seed=11)  # 200, 320, 312: 16-byte rows
     assert not info["repack_a"] and not info["repack_b"]
+    check(got, Cref, Den, dout)
+
+
+@pytest.mark.parametrize("N,ldc,dout", [(300, 312, "f16"), (300, 304, "bf16"), (258, 272, "f32"),
+                                         (260, 272, "f16"), (296, 312, "f16"), (260, 272, "f32")])
+def test_row_end_not_on_16_bytes(dev, N, ldc, dout):
+    """A TMA store writes whole 16-byte chunks, so a row whose length is not a
+    multiple of 16 bytes must not take the TMA-store epilogue: nothing after
+    column N-1 (nor past the last row) may change."""
+    M, K = 200, 96
+    got, Cref, Den, info = run_case(dev, M, N, K, "f16", dout, ldc=ldc, seed=N + ldc)
+    ob = 4 if dout == "f32" else 2
+    assert info["tma_store"] == (1 if (N * ob) % 16 == 0 else 0)
     check(got, Cref, Den, dout)
 
 
