@@ -165,6 +165,31 @@ hgemm_status_t hgemm_cache_clear(void);
  * watchdog fired) and the status is HGEMM_ERR_TIMEOUT in that case. */
 hgemm_status_t hgemm_watchdog_selftest(uint64_t timeout_ns, void *stream, int32_t *device_code);
 
+/* Allocation-free product for small M (no counterpart on the source pages:
+ * it exists for callers, not for the method).  The same swap-AB split-K
+ * kernel as the planned skinny path, for callers that may not allocate
+ * device memory: a host framework that owns every allocation and hands over
+ * only input and output buffers, a process whose device memory is budgeted
+ * at start-up, or a latency-critical loop where cudaMalloc's implicit
+ * synchronisation is not acceptable.  It calls no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *   A: M x K (lda), B: K x N (ldb), C: M x N (ldc), row-major, batch 1,
+ *   device pointers; M <= 32; A and B 16-byte aligned with lda and ldb
+ *   multiples of 8 elements (no aligned copies can be made);
+ *   dtype_in in {F16, BF16}, dtype_out in {F32, F16, BF16}; enqueued on
+ *   `stream`, asynchronous.
+ * Its split-K partial sums, counters and error word live in one 8 MiB
+ * __device__ array inside the library, held by every GPU that loads it until
+ * the process exits.  The first call on each device looks up that array's
+ * device address; make the first call before any stream capture.  Every call
+ * shares the array: calls that overlap on the GPU race and must be ordered.
+ * The split count is lowered to fit the array; a request that does not fit
+ * even unsplit returns HGEMM_ERR_UNSUPPORTED, as do misaligned operands and
+ * M > 32.  Watchdog timeouts are not reported by this entry point. */
+hgemm_status_t hgemm_skinny_noalloc(const void *A, const void *B, void *C, int64_t M, int64_t N,
+                                    int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                    hgemm_dtype_t dtype_in, hgemm_dtype_t dtype_out, void *stream);
+
 const char *hgemm_status_string(hgemm_status_t status);
 const char *hgemm_last_error_detail(void);
 

@@ -711,3 +711,23 @@ const char *hgemm_last_error_detail(void) { return g_detail.c_str(); }
 int32_t hgemm_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- internal helpers
+// Thin wrappers over the helpers above for other translation units of the
+// library (noalloc.cu); declared in internal.h.
+namespace hg {
+
+hgemm_status_t encode_map_3d(CUtensorMap *map, const void *base, int bf16, int64_t cols,
+                             int64_t rows, int64_t ld, uint32_t box_cols, uint32_t box_rows) {
+    return encode_3d(map, base,
+                     bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                     cols, rows, 1, ld, 0, box_cols, box_rows);
+}
+
+int pick_split(int64_t work_tiles, int num_kb, int num_sms) {
+    return choose_split(work_tiles, num_kb, num_sms);
+}
+
+hgemm_status_t set_error_detail(hgemm_status_t s, const char *msg) { return fail(s, "%s", msg); }
+
+}  // namespace hg

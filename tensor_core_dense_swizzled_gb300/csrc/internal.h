@@ -1,0 +1,23 @@
+// internal.h -- host helpers shared between the C-ABI translation units
+// (defined in api.cpp).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "hgemm.h"
+
+namespace hg {
+
+// 2-D (batch 1) tiled, 128-byte-swizzled map over a row-major fp16/bf16
+// array of `rows` x `cols` with leading dimension `ld` (elements).
+hgemm_status_t encode_map_3d(CUtensorMap *map, const void *base, int bf16, int64_t cols,
+                             int64_t rows, int64_t ld, uint32_t box_cols, uint32_t box_rows);
+
+// The skinny path's split-K choice (units per wave >= 90% when possible).
+int pick_split(int64_t work_tiles, int num_kb, int num_sms);
+
+// Records `msg` as the calling thread's hgemm_last_error_detail() and returns s.
+hgemm_status_t set_error_detail(hgemm_status_t s, const char *msg);
+
+}  // namespace hg

@@ -17,7 +17,8 @@ __all__ = [
     "HGEMM_PATH_TILED", "HGEMM_PATH_SKINNY", "HgemmError", "Options", "PlanInfo", "lib_path",
     "load", "hgemm_plan_create", "hgemm_plan_create_ex", "hgemm_run", "hgemm_run_host",
     "hgemm_check", "hgemm_plan_destroy", "hgemm_plan_get_info", "hgemm", "hgemm_cache_clear",
-    "hgemm_watchdog_selftest", "hgemm_status_string", "hgemm_last_error_detail", "hgemm_version",
+    "hgemm_watchdog_selftest", "hgemm_skinny_noalloc", "hgemm_status_string",
+    "hgemm_last_error_detail", "hgemm_version",
     "STATUS",
 ]
 
@@ -100,9 +101,11 @@ def load():
                               ctypes.c_int, ctypes.c_int, p]
         lib.hgemm_cache_clear.argtypes = []
         lib.hgemm_watchdog_selftest.argtypes = [ctypes.c_uint64, p, ctypes.POINTER(ctypes.c_int32)]
+        lib.hgemm_skinny_noalloc.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int,
+                                             ctypes.c_int, p]
         for name in ("hgemm_plan_create", "hgemm_plan_create_ex", "hgemm_run", "hgemm_run_host",
                      "hgemm_check", "hgemm_plan_destroy", "hgemm_plan_get_info", "hgemm",
-                     "hgemm_cache_clear", "hgemm_watchdog_selftest"):
+                     "hgemm_cache_clear", "hgemm_watchdog_selftest", "hgemm_skinny_noalloc"):
             getattr(lib, name).restype = st
         lib.hgemm_status_string.argtypes = [ctypes.c_int]
         lib.hgemm_status_string.restype = ctypes.c_char_p
@@ -201,6 +204,14 @@ def hgemm_watchdog_selftest(timeout_ns: int, stream=None) -> tuple[int, int]:
     code = ctypes.c_int32(0)
     st = load().hgemm_watchdog_selftest(timeout_ns, _stream(stream), ctypes.byref(code))
     return st, code.value
+
+
+def hgemm_skinny_noalloc(A, B, C, M, N, K, lda, ldb, ldc, dtype_in, dtype_out, stream=None):
+    """Small-M product that allocates no device memory (its scratch is a fixed
+    array inside the library); see include/hgemm.h for its limits."""
+    _check(load().hgemm_skinny_noalloc(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc,
+                                       dtype_in, dtype_out, _stream(stream)),
+           "hgemm_skinny_noalloc")
 
 
 def hgemm_status_string(status: int) -> str:
