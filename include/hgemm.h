@@ -79,6 +79,10 @@ typedef struct {
     int tile_n;               /* 0: automatic; 128, 192, 224 or 256 (tiled path) */
     int split_k;              /* 0: automatic; >= 1 (skinny path) */
     uint64_t timeout_ns;      /* 0: default (2 s); device watchdog for each pipeline wait */
+    int cta_pair;             /* tiled path: 0 automatic, 1 force 256 x 256 tiles on CTA pairs
+                                 (tcgen05 cta_group::2), 2 force single-CTA 128 x tile_n tiles */
+    int skinny_tile_n;        /* skinny path: 0 automatic, or 128 / 256 / 512 columns of C per
+                                 work unit */
 } hgemm_options_t;
 
 /* Read-only description of what a plan will launch. */

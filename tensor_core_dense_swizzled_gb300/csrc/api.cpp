@@ -19,6 +19,7 @@
 #include <tuple>
 
 #include "hgemm.h"
+#include "internal.h"
 #include "kernels.h"
 
 namespace {
@@ -103,8 +104,9 @@ struct hgemm_plan_s {
     int path;
     // tiled path
     int bn;
+    bool pair;  // 256 x 256 tiles on CTA pairs (cta_group::2)
     // skinny path
-    int nu, split, kb_per;
+    int nu, nt, split, kb_per;  // padded M, 128-column sub-tiles per unit, K splits
     int grid;
     bool ld_repack_a, ld_repack_b;  // forced by leading dimension / stride
     bool ldc_tma;                   // C's ld / stride allow TMA stores
@@ -165,7 +167,14 @@ hgemm_status_t validate(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
 
 // Picks the split count for the skinny path: the smallest split whose units
 // fill the persistent grid to >= 90% (units per wave), else the best found.
+// Splitting K is a last resort: on GB300 the 8 x 28672 x 4096 product ran at
+// 39.4 us unsplit (112 CTAs, 256-column units) against 60-95 us with 2 to 8
+// splits over all 152 SMs.  Unsplit, the CTAs sweep the same K rows of B
+// together and consume whole DRAM rows; split, they read several distant K
+// ranges at once.  So K is split only when the unsplit units would leave
+// more than 40 % of the SMs idle (small N), and then just enough.
 int choose_split(int64_t work_tiles, int num_kb, int num_sms) {
+    if (work_tiles * 10 >= static_cast<int64_t>(num_sms) * 6) return 1;
     int best = 1;
     double best_eff = 0;
     for (int s = 1; s <= 16 && s <= num_kb; ++s) {
@@ -186,12 +195,12 @@ int choose_split(int64_t work_tiles, int num_kb, int num_sms) {
 }
 
 // Picks the tile width of the tiled path.  A persistent CTA processes its
-// tiles in rounds ("waves") of one tile per SM; the time is about
-// waves x (BN + overhead), where the overhead (pipeline fill and drain, the
-// last tile's epilogue) is worth about 16 columns of main loop.  A tile
-// width that makes the tile count a multiple of the SM count wins: 4096^2
-// gives 608 tiles of 128 x 224 = 4 waves exactly, against 512 tiles of
-// 128 x 256 = 3.4 waves that take 4.
+// tiles in rounds ("waves") of one tile per SM.  The main loop is bound by
+// delivering operands to shared memory, so a tile costs about the bytes it
+// stages per K block (16 KB of A plus 8 KB per 64-column block of B), not
+// its width: on GB300 at 4096^3, 128 x 224 tiles (4 B blocks, 4 waves) ran
+// at 98.3 us against 91.1 us for 128 x 256 (3.4 waves), and 128 x 192 at
+// 104.5 us.  Ties go to the wider tile.
 int choose_tile_n(int64_t batch, int64_t M, int64_t N, int sms) {
     static const int cands[] = {256, 224, 192, 128};
     int best = 256;
@@ -199,7 +208,7 @@ int choose_tile_n(int64_t batch, int64_t M, int64_t N, int sms) {
     for (int bn : cands) {
         const int64_t tiles = batch * ceil_div(M, 128) * ceil_div(N, bn);
         const int64_t waves = ceil_div(tiles, sms);
-        const double t = static_cast<double>(waves) * (bn + 16);
+        const double t = static_cast<double>(waves) * (16 + 8 * ((bn + 63) / 64));
         if (t < best_t - 1e-9) {
             best_t = t;
             best = bn;
@@ -307,6 +316,13 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         opt.tile_n != 256)
         return fail(HGEMM_ERR_INVALID_ARG, "tile_n must be 0, 128, 192, 224 or 256");
     if (opt.split_k < 0) return fail(HGEMM_ERR_INVALID_ARG, "split_k must be >= 0");
+    if (opt.skinny_tile_n != 0 && opt.skinny_tile_n != 128 && opt.skinny_tile_n != 256 &&
+        opt.skinny_tile_n != 512)
+        return fail(HGEMM_ERR_INVALID_ARG, "skinny_tile_n must be 0, 128, 256 or 512");
+    if (opt.cta_pair < 0 || opt.cta_pair > 2)
+        return fail(HGEMM_ERR_INVALID_ARG, "cta_pair must be 0, 1 or 2");
+    if (opt.cta_pair == 1 && opt.tile_n != 0 && opt.tile_n != 256 && opt.tile_n != 224)
+        return fail(HGEMM_ERR_INVALID_ARG, "CTA-pair tiles are 256 x 256 or 256 x 224 (tile_n 0, 256 or 224)");
     if (opt.force_path == HGEMM_PATH_SKINNY && M > 32)
         return fail(HGEMM_ERR_UNSUPPORTED, "the skinny path handles M <= 32 (got %lld)", static_cast<long long>(M));
 
@@ -331,7 +347,8 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
     p->din = din; p->dout = dout; p->opt = opt;
     p->device = dev; p->num_sms = sms;
     p->timeout_ns = opt.timeout_ns ? opt.timeout_ns : kDefaultTimeoutNs;
-    p->bn = 0; p->nu = 0; p->split = 1; p->kb_per = 0; p->grid = 0;
+    p->bn = 0; p->nu = 0; p->nt = 1; p->split = 1; p->kb_per = 0; p->grid = 0;
+    p->pair = false;
 
     if (M == 0 || N == 0) {
         p->path = HGEMM_PATH_EMPTY;
@@ -358,9 +375,38 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         p->bn = opt.tile_n ? opt.tile_n : choose_tile_n(batch, M, N, sms);
         const int64_t tiles = batch * ceil_div(M, 128) * ceil_div(N, p->bn);
         p->grid = static_cast<int>(tiles < sms ? tiles : sms);
+        p->pair = false;
+        if (opt.cta_pair == 1 || (opt.cta_pair == 0 && (opt.tile_n == 0 || opt.tile_n == 256))) {
+            const int max_pairs = hg::pair_max_active_pairs();
+            if (opt.cta_pair == 1 && max_pairs < 1) {
+                delete p;
+                return fail(HGEMM_ERR_UNSUPPORTED, "no 2-CTA cluster fits on this device");
+            }
+            // 256 x 224 pair tiles (4 exact waves at 4096^2) measured no
+            // faster than 256 x 256 (87.5 us both): they stage the same bytes.
+            // They stay available through tile_n = 224.
+            const int pn = opt.tile_n == 224 ? 224 : 256;
+            const int64_t ptiles = batch * ceil_div(M, 256) * ceil_div(N, pn);
+            // Against single CTAs (see choose_tile_n): a pair tile stages
+            // 32 KB per CTA per K block for 128 x pn outputs per SM; a
+            // single-CTA tile 16 KB + 8 KB per 64 columns.  Pairs win on a
+            // strict gain and only for K long enough to be tensor-bound (a
+            // short K leaves the product bound by writing C, where smaller
+            // single-CTA tiles spread the stores better).
+            const double t_single = static_cast<double>(ceil_div(tiles, sms)) *
+                                    (16 + 8 * ((p->bn + 63) / 64));
+            const double t_pair = max_pairs > 0 ? static_cast<double>(ceil_div(ptiles, max_pairs)) * 32
+                                                : 1e300;
+            if (opt.cta_pair == 1 || (t_pair < t_single && M > 128 && N > 128 && K >= 512)) {
+                p->pair = true;
+                p->bn = pn;
+                p->grid = static_cast<int>(2 * (ptiles < max_pairs ? ptiles : max_pairs));
+            }
+        }
     } else if (p->path == HGEMM_PATH_SKINNY) {
         p->nu = M <= 16 ? 16 : 32;
-        const int64_t work = batch * ceil_div(N, 128);
+        p->nt = opt.skinny_tile_n ? opt.skinny_tile_n / 128 : hg::pick_skinny_nt(N);
+        const int64_t work = batch * ceil_div(N, 128 * p->nt);
         int split = opt.split_k ? opt.split_k : choose_split(work, num_kb, sms);
         if (split > num_kb) split = num_kb;
         if (split < 1) split = 1;
@@ -467,18 +513,21 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.N = static_cast<int32_t>(p->N);
         tp.K = static_cast<int32_t>(p->K);
         tp.batch = static_cast<int32_t>(p->batch);
-        tp.num_m = static_cast<int32_t>(ceil_div(p->M, 128));
+        tp.num_m = static_cast<int32_t>(ceil_div(p->M, p->pair ? 256 : 128));
         tp.num_n = static_cast<int32_t>(ceil_div(p->N, p->bn));
         tp.num_kb = static_cast<int32_t>(ceil_div(p->K, 64));
         tp.tiles = tp.batch * tp.num_m * tp.num_n;
         tp.group_m = 16;
-        tp.idesc = hg::idesc_f16(bf, 0, 1, 128, static_cast<uint32_t>(p->bn));
+        tp.idesc = hg::idesc_f16(bf, 0, 1, p->pair ? 256 : 128, static_cast<uint32_t>(p->bn));
         tp.C = C;
         tp.ldc = p->ldc;
         tp.strideC = p->sC;
         tp.err = err;
         tp.timeout_ns = p->timeout_ns;
-        e = hg::launch_tiled(p->bn, out_type(p->dout), ts, p->tmA, p->tmB, p->tmC, tp, p->grid, s);
+        if (p->pair)
+            e = hg::launch_pair(p->bn, out_type(p->dout), ts, p->tmA, p->tmB, p->tmC, tp, p->grid, s);
+        else
+            e = hg::launch_tiled(p->bn, out_type(p->dout), ts, p->tmA, p->tmB, p->tmC, tp, p->grid, s);
         return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "tiled kernel launch");
     }
     // skinny
@@ -489,11 +538,11 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     sp.N = static_cast<int32_t>(p->N);
     sp.K = static_cast<int32_t>(p->K);
     sp.batch = static_cast<int32_t>(p->batch);
-    sp.num_n = static_cast<int32_t>(ceil_div(p->N, 128));
+    sp.num_tiles = static_cast<int32_t>(ceil_div(p->N, 128 * p->nt));
     sp.num_kb = static_cast<int32_t>(ceil_div(p->K, 64));
     sp.split = p->split;
     sp.kb_per_split = p->kb_per;
-    sp.units = sp.batch * sp.split * sp.num_n;
+    sp.units = sp.batch * sp.split * sp.num_tiles;
     sp.idesc = hg::idesc_f16(bf, 1, 0, 128, static_cast<uint32_t>(p->nu));
     sp.C = C;
     sp.ldc = p->ldc;
@@ -502,7 +551,7 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     sp.counters = reinterpret_cast<int32_t *>(p->ws + p->off_counters);
     sp.err = err;
     sp.timeout_ns = p->timeout_ns;
-    e = hg::launch_skinny(p->nu, out_type(p->dout), p->tmA, p->tmB, sp, p->grid, s);
+    e = hg::launch_skinny(p->nu, p->nt, out_type(p->dout), p->tmA, p->tmB, sp, p->grid, s);
     return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "skinny kernel launch");
 }
 
@@ -623,14 +672,14 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     r.tile_k = 64;
     r.split_k = 1;
     if (plan->path == HGEMM_PATH_TILED) {
-        r.tile_m = 128;
+        r.tile_m = plan->pair ? 256 : 128;
         r.tile_n = plan->bn;
-        r.stages = hg::tiled_stages(plan->bn);
+        r.stages = plan->pair ? hg::pair_stages() : hg::tiled_stages(plan->bn);
         r.tma_store = plan->ldc_tma ? 1 : 0;
     } else if (plan->path == HGEMM_PATH_SKINNY) {
         r.tile_m = plan->nu;
-        r.tile_n = 128;
-        r.stages = hg::skinny_stages(plan->nu);
+        r.tile_n = 128 * plan->nt;
+        r.stages = hg::skinny_stages(plan->nu, plan->nt);
         r.split_k = plan->split;
     }
     r.grid = plan->grid;
@@ -726,6 +775,15 @@ hgemm_status_t encode_map_3d(CUtensorMap *map, const void *base, int bf16, int64
 
 int pick_split(int64_t work_tiles, int num_kb, int num_sms) {
     return choose_split(work_tiles, num_kb, num_sms);
+}
+
+int pick_skinny_nt(int64_t N) {
+    // 256 columns per work unit: 512 contiguous bytes per K row of B (see
+    // gemm_skinny.cu).  Measured on 8 x 28672 x 4096: 256-column units
+    // unsplit 39.4 us, 128-column units unsplit 49.4 us (224 units = 1.5
+    // waves), 512-column units 49.5 us (only 56 CTAs busy).  Narrow products
+    // keep 128 columns so that more units exist.
+    return N >= 4096 ? 2 : 1;
 }
 
 hgemm_status_t set_error_detail(hgemm_status_t s, const char *msg) { return fail(s, "%s", msg); }

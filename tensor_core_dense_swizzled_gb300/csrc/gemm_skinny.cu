@@ -5,77 +5,79 @@
 // kernel is bound by streaming B from HBM ("tensor-cores-cutlass-and-cute",
 // section 四.1 and the self-test of section 九 classify kernels by intensity
 // against the ridge point).  The tensor core still does the arithmetic, but
-// the design goal is bytes in flight, not MMA rate:
+// the design goal is bytes in flight and DRAM-friendly access, not MMA rate:
 //
 //   * swap A and B: compute C^T = B^T . A^T so that the large dimension N
 //     fills the 128-row side of the MMA and M (padded to NU = 16 or 32 with
 //     TMA zero fill) is the MMA's N.  B^T is read MN-major straight from the
-//     row-major K x N B (two 64-column blocks per 128-column tile); A^T is
-//     read K-major from the row-major M x K A.
-//   * split K into `split` ranges so that batch * split * ceil(N/128) work
-//     units fill every SM with a balanced number of units; each persistent CTA
-//     runs a deep ring of stages (about 200 KB of B in flight per SM).
-//   * fixup: every unit writes its fp32 partial (NU x 128) to workspace; for
-//     each 32-column quarter of a tile, the epilogue warp that arrives last at
-//     that quarter's counter sums the partials in split order 0, 1, ... (so
-//     the result does not depend on arrival order), converts, writes C and
-//     resets the counter for the next run.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
+//     row-major K x N B (64-column blocks); A^T is read K-major from the
+//     row-major M x K A.
+//   * a work unit covers NT x 128 consecutive columns of C (NT MMAs per
+//     16-deep K step), so every K row of B is read in runs of NT x 256
+//     contiguous bytes;
+//   * split K into `split` ranges so that batch * split * ceil(N / (128 NT))
+//     work units fill every SM with a balanced number of units; each
+//     persistent CTA runs a deep ring of stages (about 200 KB in flight).
+//   * fixup: every unit writes its fp32 partials (NU x 128 per 128-column
+//     sub-tile) to workspace; for each 32-column quarter of a sub-tile, the
+//     epilogue warp that arrives last at that quarter's counter sums the
+//     partials in split order 0, 1, ... (so the result does not depend on
+//     arrival order), converts, writes C and resets the counter for the next
+//     run.  No warp waits on another at an unbounded barrier.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tile_common.cuh"
 #include "watchdog.cuh"
 
 namespace hg {
 namespace {
 
 constexpr int BK = 64;
-constexpr int TN = 128;  // output columns of C per tile = MMA M
+constexpr int TN = 128;  // columns of C per MMA (= MMA M)
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARPS = 4;
 
-template <int NU>
+constexpr uint32_t pow2_at_least(uint32_t x) {
+    uint32_t p = 32;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+template <int NU, int NT>
 struct SkinnyCfg {
     static_assert(NU == 16 || NU == 32, "padded M");
-    static constexpr int STAGES = (NU == 16) ? 12 : 10;
-    static constexpr uint32_t W_BYTES = BK * TN * 2;  // B tile: 2 blocks of 64 k x 64 n
-    static constexpr uint32_t W_BLOCK = BK * 128;
+    static_assert(NT == 1 || NT == 2 || NT == 4, "128-column sub-tiles per unit");
+    static constexpr int W_BLOCKS = 2 * NT;          // 64-column blocks of B per stage
+    static constexpr uint32_t W_BLOCK = BK * 128;    // 64 k x 64 n
+    static constexpr uint32_t W_BYTES = W_BLOCKS * W_BLOCK;
     static constexpr uint32_t X_BYTES = NU * BK * 2;  // A tile: NU rows x 64 k
     static constexpr uint32_t TX_BYTES = W_BYTES + X_BYTES;
-    static constexpr uint32_t TMEM_COLS = (2 * NU < 32) ? 32 : 2 * NU;
+    static constexpr int STAGES_FIT = (232448 - 2048) / (W_BYTES + X_BYTES);
+    static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
+    static constexpr uint32_t TMEM_STRIDE = NT * NU;  // columns per accumulator buffer
+    static constexpr uint32_t TMEM_COLS = pow2_at_least(2 * TMEM_STRIDE);
     static constexpr int SMEM_W = 0;
     static constexpr int SMEM_X = SMEM_W + STAGES * W_BYTES;
     static constexpr int SMEM_BAR = SMEM_X + STAGES * X_BYTES;
     static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
     static constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
     static constexpr int SMEM_TOTAL = SMEM_MISC + 16 + 1024;
+    static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 };
 
 __device__ __forceinline__ void unit_coords(const SkinnyParams &p, int u, int &b, int &s, int &nt) {
-    const int per_batch = p.split * p.num_n;
+    const int per_batch = p.split * p.num_tiles;
     b = u / per_batch;
     const int r = u - b * per_batch;
-    s = r / p.num_n;  // split index varies slowest: concurrent units read adjacent columns
-    nt = r - s * p.num_n;
+    s = r / p.num_tiles;  // split index varies slowest: concurrent units read adjacent columns
+    nt = r - s * p.num_tiles;
 }
 
-template <int OUT>
-__device__ __forceinline__ void store_one(void *C, int64_t idx, float v) {
-    if constexpr (OUT == OUT_F32) {
-        static_cast<float *>(C)[idx] = v;
-    } else if constexpr (OUT == OUT_BF16) {
-        static_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(v);
-    } else {
-        static_cast<__half *>(C)[idx] = __float2half_rn(v);
-    }
-}
-
-template <int NU, int OUT>
+template <int NU, int NT, int OUT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     hgemm_skinny_kernel(const __grid_constant__ CUtensorMap tmX,
                         const __grid_constant__ CUtensorMap tmW, const SkinnyParams p) {
-    using Cfg = SkinnyCfg<NU>;
+    using Cfg = SkinnyCfg<NU, NT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -138,9 +140,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full(stage), Cfg::TX_BYTES);
-                    tma_load_3d(sW + stage * Cfg::W_BYTES, &tmW, full(stage), nt * TN, kb * BK, b);
-                    tma_load_3d(sW + stage * Cfg::W_BYTES + Cfg::W_BLOCK, &tmW, full(stage),
-                                nt * TN + 64, kb * BK, b);
+#pragma unroll
+                    for (int j = 0; j < Cfg::W_BLOCKS; ++j)
+                        tma_load_3d(sW + stage * Cfg::W_BYTES + j * Cfg::W_BLOCK, &tmW, full(stage),
+                                    nt * (NT * TN) + j * 64, kb * BK, b);
                     tma_load_3d(sX + stage * Cfg::X_BYTES, &tmX, full(stage), kb * BK, 0, b);
                     ++issued;
                     if (++stage == Cfg::STAGES) {
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * NU);
+                const uint32_t d0 = tmem_base + buf * Cfg::TMEM_STRIDE;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(full(stage), phase, wc, timeout_code(ROLE_MMA, stage))) {
                         ok = false;
@@ -190,10 +193,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t x0 = sX + stage * Cfg::X_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        // MMA A = B^T (MN-major), MMA B = A^T (K-major)
-                        const uint64_t ad = sdesc_sw128(w0 + k * 16 * 128, Cfg::W_BLOCK, 1024);
-                        const uint64_t bd = sdesc_sw128(x0 + k * 32, 16, 1024);
-                        umma_f16(d_tmem, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        const uint64_t bd = sdesc_sw128(x0 + k * 32, 16, 1024);  // MMA B = A^T, K-major
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) {
+                            // MMA A = columns j*128 .. j*128+127 of the B tile, MN-major
+                            const uint64_t ad = sdesc_sw128(
+                                w0 + 2 * j * Cfg::W_BLOCK + k * 16 * 128, Cfg::W_BLOCK, 1024);
+                            umma_f16(d0 + j * NU, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit(empty(stage));
                     if (++stage == Cfg::STAGES) {
@@ -211,6 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------ epilogue + fixup
         const int q = warp & 3;
         int local = 0;
+        const int num_n128 = (p.N + TN - 1) / TN;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++local) {
             int b, s, nt;
             unit_coords(p, u, b, s, nt);
@@ -218,59 +226,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t tph = (local >> 1) & 1;
             if (!wait_bounded_warp(tfull(buf), tph, wc, timeout_code(ROLE_EPILOGUE, buf))) break;
             tc_fence_after();
-            const uint32_t taddr =
-                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * NU);
-            uint32_t v[NU];
-            if constexpr (NU == 16) {
-                tmem_ld16(taddr, v);
-            } else {
-                tmem_ld32(taddr, v);
+            const uint32_t tq =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::TMEM_STRIDE;
+            uint32_t v[NT][NU];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                if constexpr (NU == 16) {
+                    tmem_ld16(tq + j * NU, v[j]);
+                } else {
+                    tmem_ld32(tq + j * NU, v[j]);
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(buf));
 
-            const int nl = q * 32 + lane;  // column within the tile
-            const int n = nt * TN + nl;
+            const int nl = q * 32 + lane;  // column within a 128-column sub-tile
             const int64_t cbase = static_cast<int64_t>(b) * p.strideC;
-            if (p.split == 1) {
-                if (n < p.N) {
 #pragma unroll
-                    for (int m = 0; m < NU; ++m)
-                        if (m < p.M)
-                            store_one<OUT>(p.C, cbase + static_cast<int64_t>(m) * p.ldc + n,
-                                           __uint_as_float(v[m]));
-                }
-                continue;
-            }
-            // split-K: publish this unit's partial, then count arrivals.  Each
-            // epilogue warp owns 32 columns of the tile and its own counter,
-            // so the fixup needs no barrier across warps (a warp that gave up
-            // on a wait can never leave the others blocked).
-            const int64_t ctr = (static_cast<int64_t>(b) * p.num_n + nt) * EPI_WARPS + q;
-            float *part = p.partials + ((static_cast<int64_t>(b) * p.split + s) * p.num_n + nt) *
-                                           (static_cast<int64_t>(NU) * TN);
+            for (int j = 0; j < NT; ++j) {
+                const int n128 = nt * NT + j;
+                if (n128 >= num_n128) break;  // sub-tile entirely past N (warp-uniform)
+                const int n = n128 * TN + nl;
+                if (p.split == 1) {
+                    if (n < p.N) {
 #pragma unroll
-            for (int m = 0; m < NU; ++m) __stcg(part + m * TN + nl, __uint_as_float(v[m]));
-            __threadfence();
-            __syncwarp();
-            int last = 0;
-            if (lane == 0) last = (atomicAdd(p.counters + ctr, 1) == p.split - 1) ? 1 : 0;
-            last = __shfl_sync(0xFFFFFFFFu, last, 0);
-            if (last) {
-                __threadfence();
-                const int64_t stride_split = static_cast<int64_t>(p.num_n) * NU * TN;
-                const float *p0 = p.partials +
-                                  (static_cast<int64_t>(b) * p.split * p.num_n + nt) * (NU * TN);
-                if (n < p.N) {
-                    for (int m = 0; m < p.M && m < NU; ++m) {
-                        float acc = 0.f;
-                        for (int ss = 0; ss < p.split; ++ss)
-                            acc += __ldcg(p0 + ss * stride_split + m * TN + nl);
-                        store_one<OUT>(p.C, cbase + static_cast<int64_t>(m) * p.ldc + n, acc);
+                        for (int m = 0; m < NU; ++m)
+                            if (m < p.M)
+                                store_one<OUT>(p.C, cbase + static_cast<int64_t>(m) * p.ldc + n,
+                                               __uint_as_float(v[j][m]));
                     }
+                    continue;
                 }
-                if (lane == 0) p.counters[ctr] = 0;  // ready for the next run
+                const int64_t ctr = (static_cast<int64_t>(b) * num_n128 + n128) * EPI_WARPS + q;
+                float *part = p.partials +
+                              ((static_cast<int64_t>(b) * p.split + s) * num_n128 + n128) *
+                                  (static_cast<int64_t>(NU) * TN);
+#pragma unroll
+                for (int m = 0; m < NU; ++m) __stcg(part + m * TN + nl, __uint_as_float(v[j][m]));
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) last = (atomicAdd(p.counters + ctr, 1) == p.split - 1) ? 1 : 0;
+                last = __shfl_sync(0xFFFFFFFFu, last, 0);
+                if (last) {
+                    __threadfence();
+                    const int64_t stride_split = static_cast<int64_t>(num_n128) * NU * TN;
+                    const float *p0 = p.partials +
+                                      (static_cast<int64_t>(b) * p.split * num_n128 + n128) * (NU * TN);
+                    if (n < p.N) {
+                        for (int m = 0; m < p.M && m < NU; ++m) {
+                            float acc = 0.f;
+                            for (int ss = 0; ss < p.split; ++ss)
+                                acc += __ldcg(p0 + ss * stride_split + m * TN + nl);
+                            store_one<OUT>(p.C, cbase + static_cast<int64_t>(m) * p.ldc + n, acc);
+                        }
+                    }
+                    if (lane == 0) p.counters[ctr] = 0;  // ready for the next run
+                }
             }
         }
     }
@@ -284,40 +297,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int NU, int OUT>
+template <int NU, int NT, int OUT>
 cudaError_t launch_impl(const CUtensorMap &tmX, const CUtensorMap &tmW, const SkinnyParams &p,
                         int grid, cudaStream_t stream) {
-    auto kern = hgemm_skinny_kernel<NU, OUT>;
+    auto kern = hgemm_skinny_kernel<NU, NT, OUT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SkinnyCfg<NU>::SMEM_TOTAL);
+                                         SkinnyCfg<NU, NT>::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, SkinnyCfg<NU>::SMEM_TOTAL, stream>>>(tmX, tmW, p);
+    kern<<<grid, NUM_THREADS, SkinnyCfg<NU, NT>::SMEM_TOTAL, stream>>>(tmX, tmW, p);
     return cudaGetLastError();
 }
 
-template <int NU>
+template <int NU, int NT>
 cudaError_t launch_out(int out, const CUtensorMap &tmX, const CUtensorMap &tmW,
                        const SkinnyParams &p, int grid, cudaStream_t s) {
     switch (out) {
-        case OUT_F16: return launch_impl<NU, OUT_F16>(tmX, tmW, p, grid, s);
-        case OUT_BF16: return launch_impl<NU, OUT_BF16>(tmX, tmW, p, grid, s);
-        case OUT_F32: return launch_impl<NU, OUT_F32>(tmX, tmW, p, grid, s);
+        case OUT_F16: return launch_impl<NU, NT, OUT_F16>(tmX, tmW, p, grid, s);
+        case OUT_BF16: return launch_impl<NU, NT, OUT_BF16>(tmX, tmW, p, grid, s);
+        case OUT_F32: return launch_impl<NU, NT, OUT_F32>(tmX, tmW, p, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int NU>
+cudaError_t launch_nt(int nt, int out, const CUtensorMap &tmX, const CUtensorMap &tmW,
+                      const SkinnyParams &p, int grid, cudaStream_t s) {
+    switch (nt) {
+        case 1: return launch_out<NU, 1>(out, tmX, tmW, p, grid, s);
+        case 2: return launch_out<NU, 2>(out, tmX, tmW, p, grid, s);
+        case 4: return launch_out<NU, 4>(out, tmX, tmW, p, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-int skinny_smem_bytes(int nu) {
-    return nu == 16 ? SkinnyCfg<16>::SMEM_TOTAL : SkinnyCfg<32>::SMEM_TOTAL;
+int skinny_stages(int nu, int nt) {
+    if (nu == 16)
+        return nt == 1 ? SkinnyCfg<16, 1>::STAGES
+                       : (nt == 2 ? SkinnyCfg<16, 2>::STAGES : SkinnyCfg<16, 4>::STAGES);
+    return nt == 1 ? SkinnyCfg<32, 1>::STAGES
+                   : (nt == 2 ? SkinnyCfg<32, 2>::STAGES : SkinnyCfg<32, 4>::STAGES);
 }
 
-int skinny_stages(int nu) { return nu == 16 ? SkinnyCfg<16>::STAGES : SkinnyCfg<32>::STAGES; }
-
-cudaError_t launch_skinny(int nu, int out, const CUtensorMap &tmX, const CUtensorMap &tmW,
+cudaError_t launch_skinny(int nu, int nt, int out, const CUtensorMap &tmX, const CUtensorMap &tmW,
                           const SkinnyParams &p, int grid, cudaStream_t stream) {
-    if (nu == 16) return launch_out<16>(out, tmX, tmW, p, grid, stream);
-    if (nu == 32) return launch_out<32>(out, tmX, tmW, p, grid, stream);
+    if (nu == 16) return launch_nt<16>(nt, out, tmX, tmW, p, grid, stream);
+    if (nu == 32) return launch_nt<32>(nt, out, tmX, tmW, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -45,6 +45,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tile_common.cuh"
 #include "watchdog.cuh"
 
 namespace hg {
@@ -54,8 +55,8 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int NUM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int EPI_WARPS = 4;
-constexpr int STG_BYTES = 4096;   // one staged piece: 32 rows x 128 bytes
-constexpr int STG_BUFS = 2;       // per epilogue warp
+constexpr int STG_BYTES = EPI_STG_BYTES;
+constexpr int STG_BUFS = EPI_STG_BUFS;
 
 template <int BN>
 struct TiledCfg {
@@ -81,46 +82,7 @@ struct TiledCfg {
 };
 
 __device__ __forceinline__ void tile_coords(const TiledParams &p, int t, int &b, int &mt, int &nt) {
-    const int per_batch = p.num_m * p.num_n;
-    b = t / per_batch;
-    const int r = t - b * per_batch;
-    const int span = p.group_m * p.num_n;
-    const int g = r / span;
-    const int first_m = g * p.group_m;
-    const int gsz = min(p.num_m - first_m, p.group_m);
-    const int rr = r - g * span;
-    mt = first_m + rr % gsz;
-    nt = rr / gsz;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
-template <int OUT>
-__device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
-    const float a = __uint_as_float(lo), b = __uint_as_float(hi);
-    if constexpr (OUT == OUT_BF16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // round to nearest even
-        return *reinterpret_cast<uint32_t *>(&h);
-    } else {
-        __half2 h = __floats2half2_rn(a, b);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-}
-
-template <int OUT>
-__device__ __forceinline__ void store_one(void *C, int64_t idx, float v) {
-    if constexpr (OUT == OUT_F32) {
-        static_cast<float *>(C)[idx] = v;
-    } else if constexpr (OUT == OUT_BF16) {
-        static_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(v);
-    } else {
-        static_cast<__half *>(C)[idx] = __float2half_rn(v);
-    }
+    grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);
 }
 
 template <int BN, int OUT, bool TMA_STORE>
@@ -265,6 +227,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int ew = warp - 2;  // staging slot
         const uint32_t stg = sC + ew * STG_BUFS * STG_BYTES;
         float *stg_f = reinterpret_cast<float *>(smem + Cfg::SMEM_C + ew * STG_BUFS * STG_BYTES);
+        const EpiArgs epi{&tmC, p.C, p.ldc, p.strideC, p.M, p.N};
         int sbuf = 0;
         int local = 0;
         for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
@@ -278,82 +241,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::TMEM_STRIDE;
             const int row0 = mt * BM + q * 32;
             const int col0 = nt * BN;
-            if constexpr (TMA_STORE) {
-                // 32 columns per piece: 128-byte rows (fp32, 128-byte swizzle:
-                // chunk j of row r at j ^ (r & 7)) or 64-byte rows (fp16/bf16,
-                // 64-byte swizzle: chunk j at j ^ ((r >> 1) & 3), the pattern
-                // of section 三.5); both keep the row-per-thread writes free
-                // of bank conflicts and match the C tensor map's swizzle.
-                constexpr int NCH = BN / 32;
-#pragma unroll 1
-                for (int c = 0; c < NCH; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tbase + c * 32, v);
-                    if (c == NCH - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(tempty(buf));
-                    }
-                    if (lane == 0) bulk_wait_read<STG_BUFS - 1>();
-                    __syncwarp();
-                    const uint32_t piece = stg + sbuf * STG_BYTES;
-                    if constexpr (OUT == OUT_F32) {
-                        const uint32_t row_addr = piece + lane * 128;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1],
-                                         v[4 * j + 2], v[4 * j + 3]);
-                    } else {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) pk[i] = pack2<OUT>(v[2 * i], v[2 * i + 1]);
-                        const uint32_t row_addr = piece + lane * 64;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), pk[4 * j],
-                                         pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_3d(&tmC, piece, col0 + c * 32, row0, b);
-                        bulk_commit();
-                    }
-                    sbuf ^= 1;
-                }
-            } else {
-                // Predicated coalesced stores: transpose each 32 x 32 chunk
-                // through shared memory (element (r, c) at r*32 + (c ^ r), so
-                // both the row-wise writes and the column-wise reads hit 32
-                // distinct banks), then lane l writes column l of every row.
-                char *Cb = static_cast<char *>(p.C);
-                const int64_t esz = (OUT == OUT_F32) ? 4 : 2;
-                const int64_t base = static_cast<int64_t>(b) * p.strideC;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tbase + c * 32, v);
-                    if (c == BN / 32 - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(tempty(buf));
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) stg_f[lane * 32 + (j ^ lane)] = __uint_as_float(v[j]);
-                    __syncwarp();
-                    const int col = col0 + c * 32 + lane;
-                    if (col < p.N) {
-                        for (int r = 0; r < 32; ++r) {
-                            const int row = row0 + r;
-                            if (row >= p.M) break;
-                            store_one<OUT>(Cb, base + static_cast<int64_t>(row) * p.ldc + col,
-                                           stg_f[r * 32 + (lane ^ r)]);
-                        }
-                    }
-                    (void)esz;
-                }
-            }
+            drain_accumulator<OUT, TMA_STORE, BN>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
+                                                  [&] {
+                                                      if (lane == 0) mbar_arrive(tempty(buf));
+                                                  });
         }
         if (TMA_STORE && lane == 0) bulk_wait<0>();
     }

@@ -34,19 +34,21 @@ struct TiledParams {
     uint64_t timeout_ns;
 };
 
-// Skinny kernel: C^T = B^T . A^T, 128 output columns of C per tile, split-K.
+// Skinny kernel: C^T = B^T . A^T, NT x 128 output columns of C per work
+// unit, split-K.  Partials and counters are indexed by 128-column sub-tile
+// (num_n128 = ceil(N / 128)).
 struct SkinnyParams {
     int32_t M, N, K, batch;
-    int32_t num_n;        // 128-wide n tiles
+    int32_t num_tiles;    // NT x 128-wide column tiles: ceil(N / (128 NT))
     int32_t num_kb;       // 64-wide K blocks in total
     int32_t split;        // K splits
     int32_t kb_per_split; // K blocks per split (last split may have fewer)
-    int32_t units;        // batch * split * num_n
+    int32_t units;        // batch * split * num_tiles
     uint32_t idesc;
     void *C;
     int64_t ldc, strideC;
-    float *partials;      // [batch][split][num_n][NU][128] fp32 (split > 1)
-    int32_t *counters;    // [batch][num_n][4] arrival counters (one per epilogue warp), zero between runs
+    float *partials;      // [batch][split][num_n128][NU][128] fp32 (split > 1)
+    int32_t *counters;    // [batch][num_n128][4] arrival counters (one per epilogue warp), zero between runs
     int32_t *err;
     uint64_t timeout_ns;
 };
@@ -54,16 +56,25 @@ struct SkinnyParams {
 // Shared memory the tiled kernel needs for a given BN (bytes, incl. alignment slack).
 int tiled_smem_bytes(int bn);
 int tiled_stages(int bn);
-int skinny_smem_bytes(int nu);
-int skinny_stages(int nu);
+int skinny_stages(int nu, int nt);
 
 // Launchers return cudaSuccess or the launch error.  `out` is an OutType.
 cudaError_t launch_tiled(int bn, int out, bool tma_store, const CUtensorMap &tmA,
                          const CUtensorMap &tmB, const CUtensorMap &tmC, const TiledParams &p,
                          int grid, cudaStream_t stream);
 
-cudaError_t launch_skinny(int nu, int out, const CUtensorMap &tmA, const CUtensorMap &tmB,
+// nu = padded M (16 or 32); nt = 128-column sub-tiles per work unit (1, 2, 4).
+cudaError_t launch_skinny(int nu, int nt, int out, const CUtensorMap &tmA, const CUtensorMap &tmB,
                           const SkinnyParams &p, int grid, cudaStream_t stream);
+
+// CTA-pair kernel (cta_group::2): 256 x pn tiles, TiledParams with num_m
+// counting 256-row tiles and num_n pn-column tiles; `grid` = 2 x pairs.
+int pair_stages();
+int pair_max_active_pairs();  // co-resident 2-CTA clusters on the current device (0 on error)
+// pn = columns per pair tile: 256 or 224 (112 B columns per CTA).
+cudaError_t launch_pair(int pn, int out, bool tma_store, const CUtensorMap &tmA,
+                        const CUtensorMap &tmB, const CUtensorMap &tmC, const TiledParams &p,
+                        int grid, cudaStream_t stream);
 
 // Copies a batch of rows x cols 16-bit matrices (leading dimension ld_src,
 // batch stride stride_src, any alignment) into dst with leading dimension

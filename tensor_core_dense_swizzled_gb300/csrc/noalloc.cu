@@ -124,11 +124,14 @@ extern "C" hgemm_status_t hgemm_skinny_noalloc(const void *A, const void *B, voi
                                 "dimensions a multiple of 8 elements (it cannot make aligned copies)");
 
     // scratch layout: [error word][counters: num_n x 4][partials: split x num_n x NU x 128 fp32]
+    // (num_n = 128-column sub-tiles; a work unit covers nt of them)
     const int nu = M <= 16 ? 16 : 32;
+    const int nt = hg::pick_skinny_nt(N);
     const int64_t num_n = ceil_div(N, 128);
+    const int64_t num_tiles = ceil_div(N, 128 * nt);
     const int num_kb = static_cast<int>(ceil_div(K, 64));
     const int64_t counter_bytes = round256(num_n * 4 * static_cast<int64_t>(sizeof(int32_t)));
-    int split = hg::pick_split(num_n, num_kb, sms);
+    int split = hg::pick_split(num_tiles, num_kb, sms);
     auto partial_bytes = [&](int sp) -> int64_t {
         return sp > 1 ? sp * num_n * nu * 128 * static_cast<int64_t>(sizeof(float)) : 0;
     };
@@ -162,11 +165,11 @@ extern "C" hgemm_status_t hgemm_skinny_noalloc(const void *A, const void *B, voi
     sp.N = static_cast<int32_t>(N);
     sp.K = static_cast<int32_t>(K);
     sp.batch = 1;
-    sp.num_n = static_cast<int32_t>(num_n);
+    sp.num_tiles = static_cast<int32_t>(num_tiles);
     sp.num_kb = num_kb;
     sp.split = split;
     sp.kb_per_split = kb_per;
-    sp.units = static_cast<int32_t>(num_n * split);
+    sp.units = static_cast<int32_t>(num_tiles * split);
     sp.idesc = hg::idesc_f16(static_cast<uint32_t>(bf), 1, 0, 128, static_cast<uint32_t>(nu));
     sp.C = C;
     sp.ldc = ldc;
@@ -176,7 +179,7 @@ extern "C" hgemm_status_t hgemm_skinny_noalloc(const void *A, const void *B, voi
     sp.partials = reinterpret_cast<float *>(scratch + kErrBytes + counter_bytes);
     sp.timeout_ns = kTimeoutNs;
     const int grid = static_cast<int>(sp.units < sms ? sp.units : sms);
-    e = hg::launch_skinny(nu, out, tmX, tmW, sp, grid, s);
+    e = hg::launch_skinny(nu, nt, out, tmX, tmW, sp, grid, s);
     if (e != cudaSuccess) return set_error_detail(HGEMM_ERR_CUDA, cudaGetErrorString(e));
     return HGEMM_OK;
 }

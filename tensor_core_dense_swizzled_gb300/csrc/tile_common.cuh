@@ -1,0 +1,155 @@
+// tile_common.cuh -- device helpers shared by the tiled GEMM kernels: the
+// grouped tile raster, 16-byte shared-memory stores for the epilogue staging,
+// and the fp32 -> fp16/bf16 conversions (round to nearest even, as the
+// "tensor-cores-cutlass-and-cute" Ampere epilogue does with
+// __floats2bfloat162_rn, section 四.3).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace hg {
+
+// Tile t of a batch of num_m x num_n tiles, in groups of `group_m` m-tiles:
+// within a group the m index runs fastest, so the tiles that concurrently
+// running CTAs work on share a few rows of A and columns of B in L2
+// (tile order is one of the gaps listed in "tensor-cores-cutlass-and-cute"
+// section 四.5).
+__device__ __forceinline__ void grouped_tile(int t, int num_m, int num_n, int group_m, int &b,
+                                             int &mt, int &nt) {
+    const int per_batch = num_m * num_n;
+    b = t / per_batch;
+    const int r = t - b * per_batch;
+    const int span = group_m * num_n;
+    const int g = r / span;
+    const int first_m = g * group_m;
+    const int gsz = min(num_m - first_m, group_m);
+    const int rr = r - g * span;
+    mt = first_m + rr % gsz;
+    nt = rr / gsz;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
+    const float a = __uint_as_float(lo), b = __uint_as_float(hi);
+    if constexpr (OUT == OUT_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_one(void *C, int64_t idx, float v) {
+    if constexpr (OUT == OUT_F32) {
+        static_cast<float *>(C)[idx] = v;
+    } else if constexpr (OUT == OUT_BF16) {
+        static_cast<__nv_bfloat16 *>(C)[idx] = __float2bfloat16_rn(v);
+    } else {
+        static_cast<__half *>(C)[idx] = __float2half_rn(v);
+    }
+}
+
+// Epilogue staging: each epilogue warp owns EPI_STG_BUFS pieces of
+// EPI_STG_BYTES (32 rows x 128 bytes) of shared memory.
+constexpr int EPI_STG_BYTES = 4096;
+constexpr int EPI_STG_BUFS = 2;
+
+struct EpiArgs {
+    const CUtensorMap *tmC;  // TMA-store path
+    void *C;                 // predicated-store path
+    int64_t ldc, strideC;
+    int32_t M, N;
+};
+
+// One epilogue warp drains its 32 TMEM lanes (output rows row0..row0+31) x
+// NCOLS fp32 columns of one accumulator, starting at TMEM address `tbase`,
+// into C columns col0.. of batch b.  `release()` runs once the last column
+// is in registers, so the MMA issuer can reuse the accumulator while the
+// stores drain.
+//
+// TMA_STORE: 32-column pieces go through the warp's swizzled staging pieces
+// (fp32 rows of 128 bytes: chunk j of row r at j ^ (r & 7); fp16/bf16 rows of
+// 64 bytes: chunk j at j ^ ((r >> 1) & 3), the 64-byte-row swizzle of
+// "tensor-cores-cutlass-and-cute" section 三.5), one thread TMA-stores each
+// piece; the C map clips rows >= M and columns >= N (it is only used when
+// N * sizeof(out) is a multiple of 16 bytes).
+// Otherwise each 32 x 32 piece is transposed through shared memory (element
+// (r, c) at r*32 + (c ^ r): conflict-free both ways) and lane l writes column
+// l of every row with predicated, coalesced stores.
+template <int OUT, bool TMA_STORE, int NCOLS, typename Release>
+__device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, float *stg_f,
+                                                  int &sbuf, int row0, int col0, int b,
+                                                  const EpiArgs &e, Release release) {
+    static_assert(NCOLS % 32 == 0, "32-column pieces");
+    constexpr int NCH = NCOLS / 32;
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int c = 0; c < NCH; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + c * 32, v);
+        if (c == NCH - 1) {
+            tc_fence_before();
+            __syncwarp();
+            release();
+        }
+        if constexpr (TMA_STORE) {
+            if (lane == 0) bulk_wait_read<EPI_STG_BUFS - 1>();
+            __syncwarp();
+            const uint32_t piece = stg + sbuf * EPI_STG_BYTES;
+            if constexpr (OUT == OUT_F32) {
+                const uint32_t row_addr = piece + lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1],
+                                 v[4 * j + 2], v[4 * j + 3]);
+            } else {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) pk[i] = pack2<OUT>(v[2 * i], v[2 * i + 1]);
+                const uint32_t row_addr = piece + lane * 64;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), pk[4 * j], pk[4 * j + 1],
+                                 pk[4 * j + 2], pk[4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(e.tmC, piece, col0 + c * 32, row0, b);
+                bulk_commit();
+            }
+            sbuf ^= 1;
+        } else {
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg_f[lane * 32 + (j ^ lane)] = __uint_as_float(v[j]);
+            __syncwarp();
+            const int col = col0 + c * 32 + lane;
+            if (col < e.N) {
+                const int64_t base = static_cast<int64_t>(b) * e.strideC;
+                for (int r = 0; r < 32; ++r) {
+                    const int row = row0 + r;
+                    if (row >= e.M) break;
+                    store_one<OUT>(e.C, base + static_cast<int64_t>(row) * e.ldc + col,
+                                   stg_f[r * 32 + (lane ^ r)]);
+                }
+            }
+        }
+    }
+}
+
+}  // namespace hg

@@ -53,6 +53,8 @@ class Options(ctypes.Structure):
         ("tile_n", ctypes.c_int),
         ("split_k", ctypes.c_int),
         ("timeout_ns", ctypes.c_uint64),
+        ("cta_pair", ctypes.c_int),
+        ("skinny_tile_n", ctypes.c_int),
     ]
 
 

@@ -165,6 +165,58 @@ def test_identity_B_returns_A(dev, din, tile_n):
 
 
 @pytest.mark.parametrize("din", ["f16", "bf16"])
+@pytest.mark.parametrize("dout", ["f32", "bf16"])
+@pytest.mark.parametrize("pn", [256, 224])
+def test_identity_B_returns_A_on_cta_pairs(dev, din, dout, pn):
+    """The same locator on 256 x 256 tiles computed by CTA pairs: each CTA
+    holds half of B's columns and half of the accumulator rows, so a wrong
+    half split shows up as swapped or zeroed column/row blocks."""
+    M, K, N = 640, 320, 576
+    A = inputs.make_random((M * K,), din, 23)
+    B = torch.eye(K, N, dtype=torch.float32).reshape(-1).to(TORCH[din])
+    got, Cref, Den, info = run_case(dev, M, N, K, din, dout, A_flat=A, B_flat=B,
+                                    options=H.Options(cta_pair=1, tile_n=pn))
+    assert info["tile_m"] == 256 and info["tile_n"] == pn
+    check(got, Cref, Den, dout, exact=(dout == "f32"))
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 64), (300, 520, 200), (513, 700, 1000), (1024, 768, 2048),
+                                   (2560, 2304, 256), (130, 260, 70)])
+@pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f16", "f32"), ("f16", "f16")])
+@pytest.mark.parametrize("pn", [256, 224])
+def test_cta_pair_random_shapes(dev, shape, din, dout, pn):
+    M, N, K = shape
+    got, Cref, Den, info = run_case(dev, M, N, K, din, dout, seed=M + 2 * N + K,
+                                    options=H.Options(cta_pair=1, tile_n=pn))
+    assert info["tile_m"] == 256 and info["grid"] % 2 == 0
+    check(got, Cref, Den, dout)
+
+
+@pytest.mark.parametrize("opt", [H.Options(cta_pair=1, force_generic_store=1),
+                                 H.Options(cta_pair=1, force_repack=1)])
+def test_cta_pair_fallback_paths(dev, opt):
+    M, N, K = 333, 444, 222
+    got, Cref, Den, _ = run_case(dev, M, N, K, "bf16", "f32", seed=24, options=opt, runs=2)
+    check(got, Cref, Den, "f32")
+
+
+def test_cta_pair_batched(dev):
+    M, N, K, batch = 300, 260, 96, 3
+    got, Cref, Den, info = run_case(dev, M, N, K, "bf16", "f32", batch=batch, seed=25,
+                                    options=H.Options(cta_pair=1))
+    check(got, Cref, Den, "f32")
+
+
+def test_cta_pair_int_exact(dev):
+    M, N, K = 512, 512, 512
+    A = inputs.make_random((M * K,), "f16", 0, "int4")
+    B = inputs.make_random((K * N,), "f16", 1, "int4")
+    got, Cref, Den, _ = run_case(dev, M, N, K, "f16", "f32", A_flat=A, B_flat=B,
+                                 options=H.Options(cta_pair=1))
+    check(got, Cref, Den, "f32", exact=True)
+
+
+@pytest.mark.parametrize("din", ["f16", "bf16"])
 def test_one_hot_rows(dev, din):
     """A[i][k] = [k == i mod K]: row i of C is row (i mod K) of B exactly."""
     M, N, K = 256, 384, 192
@@ -371,6 +423,17 @@ def test_skinny_split_k(dev, split):
     got, Cref, Den, info = run_case(dev, M, N, K, "bf16", "bf16", seed=40,
                                     options=H.Options(split_k=split), runs=3)
     assert info["split_k"] == split
+    check(got, Cref, Den, "bf16")
+
+
+@pytest.mark.parametrize("cols", [128, 256, 512])
+@pytest.mark.parametrize("M,N,K,split", [(8, 1000, 640, 3), (1, 5000, 1024, 4), (32, 700, 256, 1),
+                                         (17, 4096, 512, 2)])
+def test_skinny_unit_widths(dev, cols, M, N, K, split):
+    """Work units of 128, 256 or 512 columns (ragged last unit included)."""
+    got, Cref, Den, info = run_case(dev, M, N, K, "bf16", "bf16", seed=M + N + cols, scale_b=0.02,
+                                    options=H.Options(skinny_tile_n=cols, split_k=split), runs=2)
+    assert info["path"] == H.HGEMM_PATH_SKINNY and info["tile_n"] == cols
     check(got, Cref, Den, "bf16")
 
 
