@@ -100,6 +100,12 @@ def barrier(pg):
         pg.barrier()
 
 
+def whole_job_tflops(flops_per_step: int, steps: int, world: int, slowest_region_ms: float) -> float:
+    """Replicas: every rank runs `steps` products; the job's throughput is all
+    ranks' FLOPs over the slowest rank's timed region."""
+    return flops_per_step * steps * world / (slowest_region_ms * 1e-3) / 1e12
+
+
 def max_over_ranks(pg, x: float, device) -> float:
     if pg is None:
         return x
@@ -367,7 +373,7 @@ def run_ours(args, w, world, rank, local, pg):
         raise RuntimeError(f"timed run failed: {H.STATUS.get(st)} {H.hgemm_last_error_detail()}")
 
     region_ms = max_over_ranks(pg, region_ms, dev)
-    value = flops * args.steps * world / (region_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops, args.steps, world, region_ms)
     avg_launch_ms = statistics.mean(per_launch)
     bound = roofline_bound(w)
     peaks = load_peaks()

@@ -83,6 +83,8 @@ typedef struct {
                                  (tcgen05 cta_group::2), 2 force single-CTA 128 x tile_n tiles */
     int skinny_tile_n;        /* skinny path: 0 automatic, or 128 / 256 / 512 columns of C per
                                  work unit */
+    int no_tail_split;        /* CTA pairs: 1 keeps the last partial wave of tiles whole instead of
+                                 splitting each tail tile into two K halves */
 } hgemm_options_t;
 
 /* Read-only description of what a plan will launch. */
@@ -97,6 +99,7 @@ typedef struct {
     int tma_store;        /* 1: TMA-store epilogue; 0: predicated st.global */
     int kernels_per_run;  /* kernel launches one hgemm_run makes */
     int64_t workspace_bytes;
+    int tail_split;       /* CTA pairs: 2 when the last partial wave's tiles run as two K halves */
 } hgemm_plan_info_t;
 
 /* Creates a plan for C_b = A_b . B_b, b < batch.

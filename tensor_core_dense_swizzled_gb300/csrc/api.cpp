@@ -105,6 +105,9 @@ struct hgemm_plan_s {
     // tiled path
     int bn;
     bool pair;  // 256 x 256 tiles on CTA pairs (cta_group::2)
+    // pair path: tiles [0, full_tiles) whole, the tail split in tail_split K halves
+    int64_t ptiles = 0, full_tiles = 0, units = 0;
+    int tail_split = 1;
     // skinny path
     int nu, nt, split, kb_per;  // padded M, 128-column sub-tiles per unit, K splits
     int grid;
@@ -226,6 +229,14 @@ hgemm_status_t alloc_workspace(hgemm_plan_s *p) {
         counters = static_cast<size_t>(p->batch * num_n) * 4 * sizeof(int32_t);
         if (p->split > 1)
             partials = static_cast<size_t>(p->batch) * p->split * num_n * p->nu * 128 * sizeof(float);
+    }
+    if (p->path == HGEMM_PATH_TILED && p->pair && p->tail_split > 1) {
+        // per tail tile: 2 CTAs x 4 epilogue warps, each with two flags and two
+        // regions of up to 4 chunks of 32 rows x 32 fp32 columns (one region
+        // per K half, holding the chunks that half stores)
+        const int64_t tail = p->ptiles - p->full_tiles;
+        counters = static_cast<size_t>(tail * 2 * 4 * 2) * sizeof(int32_t);
+        partials = static_cast<size_t>(tail * 2 * 4 * 2 * 4 * 1024) * sizeof(float);
     }
     off = static_cast<size_t>(round_up(static_cast<int64_t>(off + counters), 256));
     p->off_partials = off;
@@ -400,7 +411,24 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
             if (opt.cta_pair == 1 || (t_pair < t_single && M > 128 && N > 128 && K >= 512)) {
                 p->pair = true;
                 p->bn = pn;
-                p->grid = static_cast<int>(2 * (ptiles < max_pairs ? ptiles : max_pairs));
+                p->ptiles = ptiles;
+                p->full_tiles = ptiles;
+                p->units = ptiles;
+                p->tail_split = 1;
+                // Tail: the last, partial wave of T = ptiles mod pairs tiles
+                // would leave the other pairs idle for a whole tile time.
+                // When 2T <= pairs, each tail tile is split in two K halves
+                // (run concurrently by two pairs) so the wave takes half a
+                // tile time: 4096^3 has 256 tiles on 76 pairs, 3 full waves
+                // and 28 tail tiles -> 3.5 tile times instead of 4.
+                const int64_t T = ptiles % max_pairs;
+                const int num_kb_all = static_cast<int>(ceil_div(K, 64));
+                if (!opt.no_tail_split && T > 0 && 2 * T <= max_pairs && num_kb_all >= 2) {
+                    p->tail_split = 2;
+                    p->full_tiles = ptiles - T;
+                    p->units = p->full_tiles + 2 * T;
+                }
+                p->grid = static_cast<int>(2 * (p->units < max_pairs ? p->units : max_pairs));
             }
         }
     } else if (p->path == HGEMM_PATH_SKINNY) {
@@ -524,6 +552,11 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.strideC = p->sC;
         tp.err = err;
         tp.timeout_ns = p->timeout_ns;
+        tp.full_tiles = static_cast<int32_t>(p->pair ? p->full_tiles : tp.tiles);
+        tp.tail_split = p->pair ? p->tail_split : 1;
+        tp.units = static_cast<int32_t>(p->pair ? p->units : tp.tiles);
+        tp.partials = reinterpret_cast<float *>(p->ws + p->off_partials);
+        tp.tail_sync = reinterpret_cast<int32_t *>(p->ws + p->off_counters);
         if (p->pair)
             e = hg::launch_pair(p->bn, out_type(p->dout), ts, p->tmA, p->tmB, p->tmC, tp, p->grid, s);
         else
@@ -689,6 +722,7 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     r.kernels_per_run = plan->path == HGEMM_PATH_EMPTY ? 0 : 1 + r.repack_a + r.repack_b;
     if (plan->path == HGEMM_PATH_ZERO_FILL) r.kernels_per_run = 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
+    r.tail_split = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->tail_split : 1;
     *info = r;
     return HGEMM_OK;
 }

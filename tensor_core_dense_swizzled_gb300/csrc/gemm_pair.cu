@@ -68,6 +68,41 @@ struct PairCfg {
     static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 };
 
+// Work unit u -> tile t and K-block range [kb0, kb1).  `half` is -1 for a
+// whole tile, else the K half (0 or 1) of a split tail tile.
+__device__ __forceinline__ void pair_unit(const TiledParams &p, int u, int &t, int &kb0, int &kb1,
+                                          int &half) {
+    if (u < p.full_tiles || p.tail_split == 1) {
+        t = u;
+        kb0 = 0;
+        kb1 = p.num_kb;
+        half = -1;
+        return;
+    }
+    const int v = u - p.full_tiles;
+    t = p.full_tiles + (v >> 1);
+    half = v & 1;
+    const int mid = p.num_kb >> 1;
+    kb0 = half ? mid : 0;
+    kb1 = half ? p.num_kb : mid;
+}
+
+// Bounded spin on a global flag set (with release) by another CTA.
+__device__ __forceinline__ bool wait_flag_bounded(const int32_t *flag, const WaitCtl &c,
+                                                  int32_t code) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0; it < kMaxWaitIterations; ++it) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v) return true;
+        if (*c.abort_flag) return false;
+        if (globaltimer_ns() - t0 > c.timeout_ns) break;
+    }
+    atomicCAS(c.err, 0, code);
+    *c.abort_flag = 1;
+    return false;
+}
+
 // Bounded wait with cluster-scope acquire (for barriers the peer CTA arrives on).
 __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, const WaitCtl &c,
                                                      int32_t code) {
@@ -144,12 +179,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int t = pair; ok && t < p.tiles; t += npairs) {
+            for (int u = pair; ok && u < p.units; u += npairs) {
+                int t, kb0, kb1, half;
+                pair_unit(p, u, t, kb0, kb1, half);
                 int b, mt, nt;
                 grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);
                 const int m0 = mt * (2 * BM) + static_cast<int>(rank) * BM;
                 const int n0 = nt * PN + static_cast<int>(rank) * BNH;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty(stage), phase ^ 1u, wc,
                                       timeout_code(ROLE_PRODUCER, stage))) {
                         ok = false;
@@ -194,7 +231,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int t = pair; ok && t < p.tiles; t += npairs, ++local) {
+            for (int u = pair; ok && u < p.units; u += npairs, ++local) {
+                int t, kb0, kb1, half;
+                pair_unit(p, u, t, kb0, kb1, half);
                 const int buf = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
                 if (!wait_bounded_cluster(tempty(buf), tph ^ 1u, wc,
@@ -204,7 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * Cfg::TMEM_STRIDE;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(full(stage), phase, wc, timeout_code(ROLE_MMA, stage))) {
                         ok = false;
                         break;
@@ -216,7 +255,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(b0 + k * 16 * 128, Cfg::B_BLOCK, 1024);
-                        umma_f16_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                        umma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     umma_commit_pair(empty(stage), 0x3);
                     if (++stage == Cfg::STAGES) {
@@ -240,7 +279,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const EpiArgs epi{&tmC, p.C, p.ldc, p.strideC, p.M, p.N};
         int sbuf = 0;
         int local = 0;
-        for (int t = pair; t < p.tiles; t += npairs, ++local) {
+        for (int u = pair; u < p.units; u += npairs, ++local) {
+            int t, kb0, kb1, half;
+            pair_unit(p, u, t, kb0, kb1, half);
             int b, mt, nt;
             grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);
             const int buf = local & 1;
@@ -252,10 +293,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int row0 = mt * (2 * BM) + static_cast<int>(rank) * BM + q * 32;
             const int col0 = nt * PN;
             const uint32_t release_bar = mapa_shared(tempty(buf), 0);
-            drain_accumulator<OUT, TMA_STORE, PN>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
-                                                  [&] {
-                                                      if (lane == 0) mbar_arrive_cluster(release_bar);
-                                                  });
+            auto release = [&] {
+                if (lane == 0) mbar_arrive_cluster(release_bar);
+            };
+            if (half < 0) {
+                drain_accumulator<OUT, TMA_STORE, PN>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
+                                                      release);
+                continue;
+            }
+            // Split tail tile: its two K halves run on two pairs at the same
+            // time.  Each half owns half of the 32-column chunks of every warp's
+            // 32 rows: it spills the chunks the other half owns (fp32) and
+            // raises that half's flag, then waits (bounded) for its own flag and
+            // stores own + other for the chunks it owns.  Neither side waits
+            // before spilling, so both waits end; every output element is one
+            // two-term fp32 sum, which commutes, so the result does not depend
+            // on which half finishes first.  The reader clears its flag.
+            constexpr int NCH = PN / 32;
+            constexpr int HCH = (NCH + 1) / 2;  // chunks owned by half 0
+            const int slot = ((t - p.full_tiles) * 2 + static_cast<int>(rank)) * EPI_WARPS + q;
+            int32_t *flags = p.tail_sync + 2 * slot;          // flags[h]: region of half h ready
+            float *region = p.partials + static_cast<int64_t>(slot) * (2 * 4 * 1024);
+            const int other = half ^ 1;
+            const int own_lo = half ? HCH : 0, own_hi = half ? NCH : HCH;
+            const int oth_lo = other ? HCH : 0, oth_hi = other ? NCH : HCH;
+            spill_accumulator(tbase, region + other * (4 * 1024), oth_lo, oth_hi);
+            __threadfence();
+            __syncwarp();
+            if (lane == 0)
+                asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flags + other), "r"(1)
+                             : "memory");
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_flag_bounded(flags + half, wc, timeout_code(ROLE_EPILOGUE, 0x200 + slot)) ? 1 : 0;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            __syncwarp();
+            if (!ok) {
+                tc_fence_before();
+                release();
+                break;
+            }
+            drain_accumulator<OUT, TMA_STORE, PN, true>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
+                                                        release, region + half * (4 * 1024),
+                                                        own_lo, own_hi);
+            if (lane == 0) flags[half] = 0;  // read: ready for the next run
         }
         if (TMA_STORE && lane == 0) bulk_wait<0>();
     }

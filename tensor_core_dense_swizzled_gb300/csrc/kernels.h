@@ -32,6 +32,13 @@ struct TiledParams {
     int64_t ldc, strideC;
     int32_t *err;                  // device error word
     uint64_t timeout_ns;
+    // Pair kernel only: work units.  Tiles [0, full_tiles) are one unit each;
+    // each of the remaining tiles - full_tiles "tail" tiles is split into
+    // tail_split (1 or 2) K halves, so that the last, partial wave finishes
+    // in half a tile time.  units = full_tiles + (tiles - full_tiles) * tail_split.
+    int32_t full_tiles, tail_split, units;
+    float *partials;               // [tail][rank][warp][chunk][32 rows][32 cols] fp32
+    int32_t *tail_sync;            // [tail][rank][warp][2]: arrival counter, ready flag (zero between runs)
 };
 
 // Skinny kernel: C^T = B^T . A^T, NT x 128 output columns of C per work

@@ -90,21 +90,54 @@ struct EpiArgs {
 // Otherwise each 32 x 32 piece is transposed through shared memory (element
 // (r, c) at r*32 + (c ^ r): conflict-free both ways) and lane l writes column
 // l of every row with predicated, coalesced stores.
-template <int OUT, bool TMA_STORE, int NCOLS, typename Release>
+//
+// ADD: `addend` holds another fp32 partial of the same 32 rows in the layout
+// spill_accumulator writes; it is added to the accumulator (own + addend)
+// before the conversion.
+template <int OUT, bool TMA_STORE, int NCOLS, bool ADD = false, typename Release>
 __device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, float *stg_f,
                                                   int &sbuf, int row0, int col0, int b,
-                                                  const EpiArgs &e, Release release) {
+                                                  const EpiArgs &e, Release release,
+                                                  const float *addend = nullptr, int c_lo = 0,
+                                                  int c_hi = NCOLS / 32) {
     static_assert(NCOLS % 32 == 0, "32-column pieces");
-    constexpr int NCH = NCOLS / 32;
     const int lane = threadIdx.x & 31;
+    // Chunks [c_lo, c_hi) of the accumulator; `addend` holds chunk c_lo first.
+    // ADD: the addend of chunk c+1 is loaded while chunk c is processed, so
+    // only the first L2 round trip is exposed.
+    float4 nxt[ADD ? 8 : 1];
+    if constexpr (ADD) {
+        const float4 *src = reinterpret_cast<const float4 *>(addend) + lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) nxt[j] = __ldcg(src + j * 32);
+    }
 #pragma unroll 1
-    for (int c = 0; c < NCH; ++c) {
+    for (int c = c_lo; c < c_hi; ++c) {
         uint32_t v[32];
         tmem_ld32(tbase + c * 32, v);
-        if (c == NCH - 1) {
+        if (c == c_hi - 1) {
             tc_fence_before();
             __syncwarp();
             release();
+        }
+        if constexpr (ADD) {
+            float4 cur[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+            if (c + 1 < c_hi) {
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(addend + (c + 1 - c_lo) * 1024) + lane;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) nxt[j] = __ldcg(src + j * 32);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 a = cur[j];
+                v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + a.x);
+                v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + a.y);
+                v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + a.z);
+                v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a.w);
+            }
         }
         if constexpr (TMA_STORE) {
             if (lane == 0) bulk_wait_read<EPI_STG_BUFS - 1>();
@@ -149,6 +182,27 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, 
                 }
             }
         }
+    }
+}
+
+// Writes one warp's 32 TMEM lanes x NCOLS fp32 columns to global memory,
+// bypassing L1, as float4s indexed [chunk][j][lane] (chunk = 32 columns,
+// j = which 4 of them, lane = row): every warp-wide store covers 512
+// contiguous bytes.  (A row-per-lane layout made each store touch 32 cache
+// lines and took twice as long as the whole epilogue.)  Only chunks
+// [c_lo, c_hi) are written, chunk c_lo first; TMEM is not released (the
+// caller still reads its other chunks).
+__device__ __forceinline__ void spill_accumulator(uint32_t tbase, float *dst, int c_lo, int c_hi) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int c = c_lo; c < c_hi; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + c * 32, v);
+        float4 *out = reinterpret_cast<float4 *>(dst + (c - c_lo) * 1024) + lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            __stcg(out + j * 32, make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                        __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
     }
 }
 

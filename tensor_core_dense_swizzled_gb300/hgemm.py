@@ -55,6 +55,7 @@ class Options(ctypes.Structure):
         ("timeout_ns", ctypes.c_uint64),
         ("cta_pair", ctypes.c_int),
         ("skinny_tile_n", ctypes.c_int),
+        ("no_tail_split", ctypes.c_int),
     ]
 
 
@@ -72,6 +73,7 @@ class PlanInfo(ctypes.Structure):
         ("tma_store", ctypes.c_int),
         ("kernels_per_run", ctypes.c_int),
         ("workspace_bytes", ctypes.c_int64),
+        ("tail_split", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

@@ -200,6 +200,36 @@ def test_cta_pair_fallback_paths(dev, opt):
     check(got, Cref, Den, "f32")
 
 
+@pytest.mark.parametrize("shape", [(512, 1024, 512), (300, 520, 200), (1024, 768, 96), (640, 1000, 333)])
+@pytest.mark.parametrize("dout", ["f32", "bf16", "f16"])
+def test_cta_pair_split_tail(dev, shape, dout):
+    """Fewer pair tiles than half the pairs: every tile is a tail tile whose two
+    K halves run on two pairs and meet in the two-arriver fixup.  Three runs
+    in a row must agree bit for bit (counters and flags reset, and the
+    two-term sum does not depend on which half arrives first)."""
+    M, N, K = shape
+    got, Cref, Den, info = run_case(dev, M, N, K, "bf16", dout, seed=M + N + K + 7,
+                                    options=H.Options(cta_pair=1), runs=3)
+    assert info["tile_m"] == 256 and info["tail_split"] == 2
+    check(got, Cref, Den, dout)
+
+
+@pytest.mark.parametrize("opt", [H.Options(cta_pair=1, force_generic_store=1),
+                                 H.Options(cta_pair=1, no_tail_split=1)])
+def test_cta_pair_split_tail_variants(dev, opt):
+    M, N, K = 520, 700, 300
+    got, Cref, Den, info = run_case(dev, M, N, K, "f16", "f16", seed=31, options=opt, runs=2)
+    assert info["tail_split"] == (1 if opt.no_tail_split else 2)
+    check(got, Cref, Den, "f16")
+
+
+def test_cta_pair_single_k_block_is_not_split(dev):
+    got, Cref, Den, info = run_case(dev, 512, 512, 64, "bf16", "f32", seed=32,
+                                    options=H.Options(cta_pair=1))
+    assert info["tail_split"] == 1
+    check(got, Cref, Den, "f32")
+
+
 def test_cta_pair_batched(dev):
     M, N, K, batch = 300, 260, 96, 3
     got, Cref, Den, info = run_case(dev, M, N, K, "bf16", "f32", batch=batch, seed=25,
