@@ -171,10 +171,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
+    // The next kernel of the stream may be scheduled now; it waits for this
+    // one to complete before it reads memory (griddep_wait below).
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
+            // Nothing this kernel reads may be read before the previous kernel
+            // of the stream has completed (dependent launches).
+            griddep_wait();
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
@@ -362,13 +368,15 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = PairCfg<PN>::SMEM_TOTAL;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
 }
 

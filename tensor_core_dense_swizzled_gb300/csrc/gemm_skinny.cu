@@ -120,10 +120,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
+    // The next kernel of the stream may be scheduled now; it waits for this
+    // one to complete before it reads memory (griddep_wait below).
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            // Nothing this kernel reads may be read before the previous kernel
+            // of the stream has completed (dependent launches).
+            griddep_wait();
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
@@ -304,8 +310,8 @@ cudaError_t launch_impl(const CUtensorMap &tmX, const CUtensorMap &tmW, const Sk
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SkinnyCfg<NU, NT>::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, SkinnyCfg<NU, NT>::SMEM_TOTAL, stream>>>(tmX, tmW, p);
-    return cudaGetLastError();
+    return launch_dependent(kern, grid, NUM_THREADS, SkinnyCfg<NU, NT>::SMEM_TOTAL, stream, tmX,
+                            tmW, p);
 }
 
 template <int NU, int NT>

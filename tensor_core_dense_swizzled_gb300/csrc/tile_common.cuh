@@ -63,6 +63,25 @@ __device__ __forceinline__ void store_one(void *C, int64_t idx, float v) {
     }
 }
 
+// Launches `kern` on `stream` with programmatic stream serialization: the
+// kernel may be scheduled while the previous kernel of the stream finishes;
+// it calls griddep_wait() before reading memory (see ptx.cuh).
+template <typename Kernel, typename... Args>
+cudaError_t launch_dependent(Kernel kern, int grid, int threads, int smem, cudaStream_t stream,
+                             const Args &...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Epilogue staging: each epilogue warp owns EPI_STG_BUFS pieces of
 // EPI_STG_BYTES (32 rows x 128 bytes) of shared memory.
 constexpr int EPI_STG_BYTES = 4096;
@@ -111,11 +130,18 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, 
 #pragma unroll
         for (int j = 0; j < 8; ++j) nxt[j] = __ldcg(src + j * 32);
     }
+    // TMEM loads run one chunk ahead: chunk c+1 is in flight while chunk c is
+    // converted, staged and stored.
+    uint32_t v[32], vn[32];
+    tmem_ld32_issue(tbase + c_lo * 32, vn);
 #pragma unroll 1
     for (int c = c_lo; c < c_hi; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + c * 32, v);
-        if (c == c_hi - 1) {
+        tmem_ld32_wait(vn);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = vn[i];
+        if (c + 1 < c_hi) {
+            tmem_ld32_issue(tbase + (c + 1) * 32, vn);
+        } else {
             tc_fence_before();
             __syncwarp();
             release();
@@ -174,6 +200,7 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, 
             const int col = col0 + c * 32 + lane;
             if (col < e.N) {
                 const int64_t base = static_cast<int64_t>(b) * e.strideC;
+#pragma unroll 4
                 for (int r = 0; r < 32; ++r) {
                     const int row = row0 + r;
                     if (row >= e.M) break;

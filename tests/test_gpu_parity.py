@@ -546,6 +546,49 @@ def test_batched_qk_full_compare(dev):
     check(got, Cref, Den, w.dtype_out)
 
 
+# ---------------------------------------------------------------- dependent launches
+
+@pytest.mark.parametrize("opt2", [None, H.Options(cta_pair=2), H.Options(force_path=H.HGEMM_PATH_SKINNY)])
+def test_back_to_back_dependent_products(dev, opt2):
+    """The kernels may be scheduled while the previous kernel of the stream
+    finishes; they must still wait for it before touching memory.  Chain on
+    one stream, no synchronisation in between:
+      1. C1 = A1 . B1            (pair kernel)
+      2. C2 = C1[:M2] . B2       (reads C1: read-after-write)
+      3. A1 <- C3 = A3 . B3      (overwrites product 1's input: write-after-read)
+    and check 2 against the oracle on C1's actual bits."""
+    M, N, K = 1024, 768, 2048
+    M2 = 16 if opt2 is not None and opt2.force_path == H.HGEMM_PATH_SKINNY else 512
+    N2 = 512
+    A1 = inputs.make_random((M, K), "bf16", 90).to(dev)
+    B1 = inputs.make_random((K, N), "bf16", 91).to(dev)
+    B2 = inputs.make_random((N, N2), "bf16", 92).to(dev)
+    C1 = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    C2 = torch.empty(M2, N2, dtype=torch.float32, device=dev)
+    A3 = inputs.make_random((M, 256), "bf16", 93).to(dev)
+    B3 = inputs.make_random((256, K), "bf16", 94).to(dev)
+    A1_bits = bits(A1)
+    p1 = H.hgemm_plan_create(M, N, K, K, N, N, 1, 0, 0, 0, H.HGEMM_BF16, H.HGEMM_BF16)
+    p2 = H.hgemm_plan_create_ex(M2, N2, N, N, N2, N2, 1, 0, 0, 0, H.HGEMM_BF16, H.HGEMM_F32, opt2)
+    p3 = H.hgemm_plan_create(M, K, 256, 256, K, K, 1, 0, 0, 0, H.HGEMM_BF16, H.HGEMM_BF16)
+    try:
+        for _ in range(3):
+            A1.copy_(torch.from_numpy(A1_bits.view(np.int16).reshape(M, K)).view(torch.bfloat16))
+            H.hgemm_run(p1, A1, B1, C1)
+            H.hgemm_run(p2, C1, B2, C2)
+            H.hgemm_run(p3, A3, B3, A1)
+        assert H.hgemm_check(p1) == 0 and H.hgemm_check(p2) == 0 and H.hgemm_check(p3) == 0
+    finally:
+        for p in (p1, p2, p3):
+            H.hgemm_plan_destroy(p)
+    Cref1, Den1 = oracle.gemm(A1_bits, bits(B1), 1, M, N, K, K, N)
+    check(oracle.decode(bits(C1), 1).reshape(1, M, N), Cref1, Den1, "bf16")
+    Cref2, Den2 = oracle.gemm(bits(C1)[: M2 * N], bits(B2), 1, M2, N2, N, N, N2)
+    check(C2.cpu().double().numpy()[None], Cref2, Den2, "f32")
+    Cref3, Den3 = oracle.gemm(bits(A3), bits(B3), 1, M, K, 256, 256, K)
+    check(oracle.decode(bits(A1), 1).reshape(1, M, K), Cref3, Den3, "bf16")
+
+
 # ---------------------------------------------------------------- API surface
 
 def test_one_shot_and_matmul(dev):
