@@ -518,17 +518,21 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     if (st != HGEMM_OK) return st;
     const void *Ae = A;
     const void *Be = B;
+    hg::Repack16Job jobs[2];
+    int njobs = 0;
     if (pack_a) {
-        e = hg::launch_repack16(A, p->lda, p->sA, p->ws + p->off_apack, p->lda_p, p->sA_p, p->M,
-                                p->K, p->batch, p->num_sms, s);
-        if (e != cudaSuccess) return cuda_fail(e, "repack(A) launch");
+        jobs[njobs++] = hg::Repack16Job{A, p->lda, p->sA, p->ws + p->off_apack, p->lda_p,
+                                        p->sA_p, p->M, p->K, p->batch};
         Ae = p->ws + p->off_apack;
     }
     if (pack_b) {
-        e = hg::launch_repack16(B, p->ldb, p->sB, p->ws + p->off_bpack, p->ldb_p, p->sB_p, p->K,
-                                p->N, p->batch, p->num_sms, s);
-        if (e != cudaSuccess) return cuda_fail(e, "repack(B) launch");
+        jobs[njobs++] = hg::Repack16Job{B, p->ldb, p->sB, p->ws + p->off_bpack, p->ldb_p,
+                                        p->sB_p, p->K, p->N, p->batch};
         Be = p->ws + p->off_bpack;
+    }
+    if (njobs > 0) {  // both copies in one launch
+        e = hg::launch_repack16(jobs, njobs, p->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, "operand copy launch");
     }
     int32_t *err = reinterpret_cast<int32_t *>(p->ws);
     const uint32_t bf = p->din == HGEMM_BF16 ? 1u : 0u;
@@ -719,7 +723,7 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     const bool busy = plan->path == HGEMM_PATH_TILED || plan->path == HGEMM_PATH_SKINNY;
     r.repack_a = (busy && (plan->ld_repack_a || plan->opt.force_repack)) ? 1 : 0;
     r.repack_b = (busy && (plan->ld_repack_b || plan->opt.force_repack)) ? 1 : 0;
-    r.kernels_per_run = plan->path == HGEMM_PATH_EMPTY ? 0 : 1 + r.repack_a + r.repack_b;
+    r.kernels_per_run = plan->path == HGEMM_PATH_EMPTY ? 0 : 1 + ((r.repack_a || r.repack_b) ? 1 : 0);
     if (plan->path == HGEMM_PATH_ZERO_FILL) r.kernels_per_run = 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
     r.tail_split = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->tail_split : 1;

@@ -16,35 +16,75 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tile_common.cuh"
 #include "watchdog.cuh"
 
 namespace hg {
 namespace {
 
-// One thread writes one aligned 16-byte chunk (8 elements) of a destination
-// row; the source reads are 2-byte loads with no alignment assumption.
-__global__ void repack16_kernel(const uint16_t *__restrict__ src, int64_t ld_src, int64_t stride_src,
-                                uint16_t *__restrict__ dst, int64_t ld_dst, int64_t stride_dst,
-                                int64_t rows, int64_t cols, int64_t batch) {
-    const int64_t chunks = ld_dst / 8;
-    const int64_t total = batch * rows * chunks;
-    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t c8 = idx % chunks;
-        const int64_t rb = idx / chunks;
-        const int64_t r = rb % rows;
-        const int64_t b = rb / rows;
-        const uint16_t *s = src + b * stride_src + r * ld_src + c8 * 8;
-        uint32_t w[4];
+__device__ __forceinline__ uint32_t select8(const uint32_t (&w)[8], int k) {
+    uint32_t r = w[0];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int64_t col = c8 * 8 + 2 * e;
-            const uint32_t lo = (col < cols) ? s[2 * e] : 0u;
-            const uint32_t hi = (col + 1 < cols) ? s[2 * e + 1] : 0u;
-            w[e] = lo | (hi << 16);
+    for (int t = 1; t < 8; ++t) r = (k == t) ? w[t] : r;
+    return r;
+}
+
+// Copies rows of up to two 16-bit operands (one launch for A and B) into
+// 16-byte aligned rows.  One warp per row; lane l writes destination chunks
+// l, l+32, ... of 8 elements (16 bytes).  Counting aligned 16-byte granules
+// from the one holding the row's first element, destination chunk c is
+// source granules c and c+1 shifted right by the row's misalignment (0..7
+// elements), so every load and store is a full 16 bytes.  A granule is read
+// only if it holds at least one element of the row, so nothing outside the
+// row's own granules is touched.  Elements past `cols` in the last chunk are
+// written as zero (row padding that TMA never reads).
+__global__ void repack16_kernel(const Repack16Job j0, const Repack16Job j1, int njobs) {
+    griddep_wait();  // the source may be the previous kernel's output
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    const int64_t rows0 = j0.batch * j0.rows;
+    const int64_t total = rows0 + (njobs > 1 ? j1.batch * j1.rows : 0);
+    const int wpb = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * wpb + (threadIdx.x >> 5); row < total;
+         row += static_cast<int64_t>(gridDim.x) * wpb) {
+        const bool second = row >= rows0;
+        const int64_t rr = second ? row - rows0 : row;
+        const int64_t rows = second ? j1.rows : j0.rows;
+        const int64_t cols = second ? j1.cols : j0.cols;
+        const int64_t ld_dst = second ? j1.ld_dst : j0.ld_dst;
+        const int64_t b = rr / rows, r = rr - (rr / rows) * rows;
+        const uint16_t *s = static_cast<const uint16_t *>(second ? j1.src : j0.src) +
+                            b * (second ? j1.stride_src : j0.stride_src) +
+                            r * (second ? j1.ld_src : j0.ld_src);
+        uint16_t *d = static_cast<uint16_t *>(second ? j1.dst : j0.dst) +
+                      b * (second ? j1.stride_dst : j0.stride_dst) + r * ld_dst;
+        const uintptr_t sa = reinterpret_cast<uintptr_t>(s);
+        const int mis = static_cast<int>((sa & 15u) >> 1);
+        const uint4 *g = reinterpret_cast<const uint4 *>(sa - (sa & 15u));
+        const int64_t last = (mis + cols - 1) >> 3;  // granule of the row's last element
+        const int ws = mis >> 1, odd = mis & 1;
+        const int64_t nch = ld_dst >> 3;
+        for (int64_t c = lane; c < nch; c += 32) {
+            uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (c <= last) {
+                const uint4 x = __ldg(g + c);
+                w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+            }
+            if (c + 1 <= last) {
+                const uint4 y = __ldg(g + c + 1);
+                w[4] = y.x; w[5] = y.y; w[6] = y.z; w[7] = y.w;
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t lo = select8(w, i + ws), hi = select8(w, i + ws + 1);
+                o[i] = odd ? __funnelshift_r(lo, hi, 16) : lo;
+                const int64_t e = c * 8 + 2 * i;  // column of o[i]'s low half
+                if (e >= cols) o[i] = 0;
+                else if (e + 1 >= cols) o[i] &= 0xFFFFu;
+            }
+            *reinterpret_cast<uint4 *>(d + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        uint4 *d = reinterpret_cast<uint4 *>(dst + b * stride_dst + r * ld_dst + c8 * 8);
-        *d = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -90,17 +130,23 @@ int grid_for(int64_t total, int threads, int num_sms) {
 
 }  // namespace
 
-cudaError_t launch_repack16(const void *src, int64_t ld_src, int64_t stride_src, void *dst,
-                            int64_t ld_dst, int64_t stride_dst, int64_t rows, int64_t cols,
-                            int64_t batch, int num_sms, cudaStream_t stream) {
-    if (ld_dst % 8 != 0 || (reinterpret_cast<uintptr_t>(dst) & 15) != 0 || stride_dst % 8 != 0)
-        return cudaErrorInvalidValue;
-    const int64_t total = batch * rows * (ld_dst / 8);
-    if (total == 0) return cudaSuccess;
-    repack16_kernel<<<grid_for(total, 256, num_sms), 256, 0, stream>>>(
-        static_cast<const uint16_t *>(src), ld_src, stride_src, static_cast<uint16_t *>(dst),
-        ld_dst, stride_dst, rows, cols, batch);
-    return cudaGetLastError();
+cudaError_t launch_repack16(const Repack16Job *jobs, int njobs, int num_sms, cudaStream_t stream) {
+    if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
+    int64_t rows = 0;
+    for (int i = 0; i < njobs; ++i) {
+        const Repack16Job &j = jobs[i];
+        if (j.ld_dst % 8 != 0 || (reinterpret_cast<uintptr_t>(j.dst) & 15) != 0 ||
+            j.stride_dst % 8 != 0 || (reinterpret_cast<uintptr_t>(j.src) & 1) != 0 || j.rows < 1 ||
+            j.cols < 1 || j.ld_dst < j.cols)
+            return cudaErrorInvalidValue;
+        rows += j.batch * j.rows;
+    }
+    const int threads = 256;  // 8 warps, one row each
+    const int64_t blocks = (rows + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    const int grid = static_cast<int>(blocks < cap ? blocks : cap);
+    return launch_dependent(repack16_kernel, grid, threads, 0, stream, jobs[0],
+                            njobs > 1 ? jobs[1] : jobs[0], njobs);
 }
 
 cudaError_t launch_zero_fill(void *C, int64_t ldc, int64_t strideC, int64_t rows, int64_t cols,

@@ -83,12 +83,19 @@ cudaError_t launch_pair(int pn, int out, bool tma_store, const CUtensorMap &tmA,
                         const CUtensorMap &tmB, const CUtensorMap &tmC, const TiledParams &p,
                         int grid, cudaStream_t stream);
 
-// Copies a batch of rows x cols 16-bit matrices (leading dimension ld_src,
-// batch stride stride_src, any alignment) into dst with leading dimension
-// ld_dst (a multiple of 8) and batch stride stride_dst (16-byte aligned).
-cudaError_t launch_repack16(const void *src, int64_t ld_src, int64_t stride_src, void *dst,
-                            int64_t ld_dst, int64_t stride_dst, int64_t rows, int64_t cols,
-                            int64_t batch, int num_sms, cudaStream_t stream);
+// One operand copy: a batch of rows x cols 16-bit matrices (leading
+// dimension ld_src, batch stride stride_src, any 2-byte alignment) into dst
+// with leading dimension ld_dst (a multiple of 8, >= cols) and batch stride
+// stride_dst (16-byte aligned).
+struct Repack16Job {
+    const void *src;
+    int64_t ld_src, stride_src;
+    void *dst;
+    int64_t ld_dst, stride_dst, rows, cols, batch;
+};
+
+// Runs one or two operand copies in a single launch.
+cudaError_t launch_repack16(const Repack16Job *jobs, int njobs, int num_sms, cudaStream_t stream);
 
 // Writes zeros into a batch of rows x cols blocks of `elem_bytes`-byte elements.
 cudaError_t launch_zero_fill(void *C, int64_t ldc, int64_t strideC, int64_t rows, int64_t cols,

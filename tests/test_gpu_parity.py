@@ -361,6 +361,19 @@ def test_misaligned_base_pointers(dev):
     check(got, Cref, Den, "f32")
 
 
+@pytest.mark.parametrize("off", range(8))
+def test_operand_copy_every_misalignment(dev, off):
+    """The aligned copy reads whole 16-byte granules and shifts them: every
+    start offset 0..7 elements, odd leading dimensions (so the offset changes
+    from row to row) and rows shorter than a granule."""
+    for (M, N, K) in [(45, 29, 37), (130, 7, 3), (9, 300, 1)]:
+        got, Cref, Den, info = run_case(dev, M, N, K, "f16", "f32", lda=K, ldb=N, ldc=N,
+                                        off_a=off, off_b=(off * 3) % 8, seed=100 + off + K,
+                                        options=H.Options(force_path=H.HGEMM_PATH_TILED))
+        assert info["repack_a"] or K % 8 != 0 or off != 0
+        check(got, Cref, Den, "f32")
+
+
 @pytest.mark.parametrize("opt", [H.Options(force_repack=1), H.Options(force_generic_store=1),
                                  H.Options(force_repack=1, force_generic_store=1)])
 def test_forced_fallbacks_match(dev, opt):
