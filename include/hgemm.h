@@ -83,8 +83,15 @@ typedef struct {
                                  (tcgen05 cta_group::2), 2 force single-CTA 128 x tile_n tiles */
     int skinny_tile_n;        /* skinny path: 0 automatic, or 128 / 256 / 512 columns of C per
                                  work unit */
-    int no_tail_split;        /* CTA pairs: 1 keeps the last partial wave of tiles whole instead of
-                                 splitting each tail tile into two K halves */
+    int no_tail_split;        /* CTA pairs: 1 runs whole tiles only, so the last partial wave of
+                                 tiles stays whole (no stream-K, no K halves) */
+    int pair_k_blocks;        /* CTA pairs: 0 automatic (2), or 1 / 2 64-wide K blocks per pipeline
+                                 stage (tile_k of the plan info is 64 x this) */
+    int tail_mode;            /* CTA pairs, the last partial wave of tiles: 0 automatic; 1 whole
+                                 tiles; 2 K halves of each tail tile run by two pairs at once
+                                 (needs 2 x tail tiles <= pairs); 3 stream-K (needs tiles >=
+                                 pairs).  Automatic takes 3, else 2, else 1, the first whose
+                                 condition holds; a forced 3 or 2 falls back the same way. */
 } hgemm_options_t;
 
 /* Read-only description of what a plan will launch. */
@@ -100,6 +107,11 @@ typedef struct {
     int kernels_per_run;  /* kernel launches one hgemm_run makes */
     int64_t workspace_bytes;
     int tail_split;       /* CTA pairs: 2 when the last partial wave's tiles run as two K halves */
+    int wide_boxes;       /* CTA pairs: 1 when each pipeline stage of A and of B is one TMA copy
+                             (4-D views; 256-wide tiles, K and N multiples of 64) */
+    int stream_k;         /* CTA pairs: 1 when the tiles' K steps are dealt to the pairs in equal
+                             contiguous ranges (at least one full wave of tiles, not a whole
+                             number of waves) */
 } hgemm_plan_info_t;
 
 /* Creates a plan for C_b = A_b . B_b, b < batch.

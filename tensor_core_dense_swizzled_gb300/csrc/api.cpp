@@ -94,6 +94,34 @@ hgemm_status_t encode_3d(CUtensorMap *map, const void *base, CUtensorMapDataType
     return HGEMM_OK;
 }
 
+// 4-D view of a row-major rows x cols 16-bit operand (cols a multiple of 64)
+// that splits the contiguous dimension in 64-element blocks: dims (64, rows,
+// cols / 64, batch), strides ld (rows), 128 bytes (blocks), stride (batch);
+// box 64 x box_rows x box_blocks; 128-byte swizzle, zero fill outside.
+// A (M x K) with box_blocks = K blocks per stage and B (K x N) with
+// box_rows = K rows per stage, box_blocks = 64-column blocks per CTA.
+hgemm_status_t encode_split_4d(CUtensorMap *map, const void *base, CUtensorMapDataType dt,
+                               int64_t cols, int64_t rows, int64_t batch, int64_t ld,
+                               int64_t stride, uint32_t box_rows, uint32_t box_blocks) {
+    auto fn = encode_fn();
+    if (!fn) return fail(HGEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const int esize = 2;
+    int64_t bstride = stride * esize;
+    if (batch == 1) bstride = round_up(rows * ld * esize, 16);
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(ld * esize), 128,
+                             static_cast<cuuint64_t>(bstride)};
+    cuuint32_t box[4] = {64, box_rows, box_blocks, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(HGEMM_ERR_CUDA, "cuTensorMapEncodeTiled (4-D view) failed (%d)", static_cast<int>(r));
+    return HGEMM_OK;
+}
+
 }  // namespace
 
 struct hgemm_plan_s {
@@ -108,6 +136,9 @@ struct hgemm_plan_s {
     // pair path: tiles [0, full_tiles) whole, the tail split in tail_split K halves
     int64_t ptiles = 0, full_tiles = 0, units = 0;
     int tail_split = 1;
+    int pair_ks = 2;  // pair path: 64-wide K blocks per pipeline stage
+    bool wide = false;  // pair path: A/B maps are the 4-D one-copy-per-stage views
+    bool stream_k = false;  // pair path: stream-K schedule (see plan_create)
     // skinny path
     int nu, nt, split, kb_per;  // padded M, 128-column sub-tiles per unit, K splits
     int grid;
@@ -230,6 +261,13 @@ hgemm_status_t alloc_workspace(hgemm_plan_s *p) {
         if (p->split > 1)
             partials = static_cast<size_t>(p->batch) * p->split * num_n * p->nu * 128 * sizeof(float);
     }
+    if (p->path == HGEMM_PATH_TILED && p->pair && p->stream_k) {
+        // per pair (the cut at the start of its range): 2 CTAs x 4 epilogue
+        // warps, each with one flag and bn / 32 chunks of 32 x 32 fp32
+        const int64_t slots = p->grid / 2;
+        counters = static_cast<size_t>(slots * 2 * 4) * sizeof(int32_t);
+        partials = static_cast<size_t>(slots * 2 * 4 * (p->bn / 32) * 1024) * sizeof(float);
+    }
     if (p->path == HGEMM_PATH_TILED && p->pair && p->tail_split > 1) {
         // per tail tile: 2 CTAs x 4 epilogue warps, each with two flags and two
         // regions of up to 4 chunks of 32 rows x 32 fp32 columns (one region
@@ -332,6 +370,10 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         return fail(HGEMM_ERR_INVALID_ARG, "skinny_tile_n must be 0, 128, 256 or 512");
     if (opt.cta_pair < 0 || opt.cta_pair > 2)
         return fail(HGEMM_ERR_INVALID_ARG, "cta_pair must be 0, 1 or 2");
+    if (opt.pair_k_blocks < 0 || opt.pair_k_blocks > 2)
+        return fail(HGEMM_ERR_INVALID_ARG, "pair_k_blocks must be 0, 1 or 2");
+    if (opt.tail_mode < 0 || opt.tail_mode > 3)
+        return fail(HGEMM_ERR_INVALID_ARG, "tail_mode must be 0, 1, 2 or 3");
     if (opt.cta_pair == 1 && opt.tile_n != 0 && opt.tile_n != 256 && opt.tile_n != 224)
         return fail(HGEMM_ERR_INVALID_ARG, "CTA-pair tiles are 256 x 256 or 256 x 224 (tile_n 0, 256 or 224)");
     if (opt.force_path == HGEMM_PATH_SKINNY && M > 32)
@@ -417,13 +459,27 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
                 p->tail_split = 1;
                 // Tail: the last, partial wave of T = ptiles mod pairs tiles
                 // would leave the other pairs idle for a whole tile time.
-                // When 2T <= pairs, each tail tile is split in two K halves
-                // (run concurrently by two pairs) so the wave takes half a
-                // tile time: 4096^3 has 256 tiles on 76 pairs, 3 full waves
-                // and 28 tail tiles -> 3.5 tile times instead of 4.
+                //  - 2T <= pairs: those T tiles are split in two K halves run
+                //    by two pairs at once, in the first wave (their exchange
+                //    hides behind the next tile): 4096^3 (256 tiles, 76 pairs)
+                //    runs 3.5 tile times instead of 4.
+                //  - otherwise, with at least one full wave: stream-K (equal
+                //    K-step ranges for the last one-and-a-bit waves).  Where
+                //    both apply, the halves measured faster (4096^3: 85.7 us
+                //    against 88.7 us, interleaved on one GB300): the dealt
+                //    ranges run at unrelated K steps and lose L2 reuse.
                 const int64_t T = ptiles % max_pairs;
-                const int num_kb_all = static_cast<int>(ceil_div(K, 64));
-                if (!opt.no_tail_split && T > 0 && 2 * T <= max_pairs && num_kb_all >= 2) {
+                p->pair_ks = opt.pair_k_blocks ? opt.pair_k_blocks : 2;
+                const int64_t num_steps = ceil_div(ceil_div(K, 64), p->pair_ks);
+                const bool can_sk = T > 0 && ptiles >= max_pairs;
+                const bool can_halves = T > 0 && 2 * T <= max_pairs && num_steps >= 2;
+                int mode = opt.no_tail_split ? 1 : opt.tail_mode;
+                if (mode == 0) mode = can_halves ? 2 : 3;
+                if (mode == 3 && can_sk) {
+                    p->stream_k = true;
+                    // all waves but the last one and a bit run whole tiles
+                    p->full_tiles = (ptiles / max_pairs - 1) * max_pairs;
+                } else if (mode >= 2 && can_halves) {
                     p->tail_split = 2;
                     p->full_tiles = ptiles - T;
                     p->units = p->full_tiles + 2 * T;
@@ -465,10 +521,22 @@ hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *
     const int64_t sB = packed_b ? p->sB_p : p->sB;
     hgemm_status_t st;
     if (p->path == HGEMM_PATH_TILED) {
-        st = encode_3d(&p->tmA, A, dt, 2, p->K, p->M, p->batch, lda, sA, 64, 128);
-        if (st != HGEMM_OK) return st;
-        st = encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64);
-        if (st != HGEMM_OK) return st;
+        // Pair tiles 256 wide with K and N multiples of 64: the 4-D views
+        // (one copy per operand per stage); otherwise, or if the driver
+        // rejects them, the 3-D maps.
+        p->wide = false;
+        if (p->pair && p->bn == 256 && p->K % 64 == 0 && p->N % 64 == 0) {
+            p->wide = encode_split_4d(&p->tmA, A, dt, p->K, p->M, p->batch, lda, sA, 128,
+                                      static_cast<uint32_t>(p->pair_ks)) == HGEMM_OK &&
+                      encode_split_4d(&p->tmB, B, dt, p->N, p->K, p->batch, ldb, sB,
+                                      static_cast<uint32_t>(64 * p->pair_ks), 2) == HGEMM_OK;
+        }
+        if (!p->wide) {
+            st = encode_3d(&p->tmA, A, dt, 2, p->K, p->M, p->batch, lda, sA, 64, 128);
+            if (st != HGEMM_OK) return st;
+            st = encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64);
+            if (st != HGEMM_OK) return st;
+        }
         if (tma_store) {
             const CUtensorMapDataType ct = p->dout == HGEMM_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                            : p->dout == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -559,10 +627,13 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.full_tiles = static_cast<int32_t>(p->pair ? p->full_tiles : tp.tiles);
         tp.tail_split = p->pair ? p->tail_split : 1;
         tp.units = static_cast<int32_t>(p->pair ? p->units : tp.tiles);
+        tp.wide_boxes = p->wide ? 1 : 0;
+        tp.stream_k = p->stream_k ? 1 : 0;
         tp.partials = reinterpret_cast<float *>(p->ws + p->off_partials);
         tp.tail_sync = reinterpret_cast<int32_t *>(p->ws + p->off_counters);
         if (p->pair)
-            e = hg::launch_pair(p->bn, out_type(p->dout), ts, p->tmA, p->tmB, p->tmC, tp, p->grid, s);
+            e = hg::launch_pair(p->bn, p->pair_ks, out_type(p->dout), ts, p->tmA, p->tmB, p->tmC, tp,
+                                p->grid, s);
         else
             e = hg::launch_tiled(p->bn, out_type(p->dout), ts, p->tmA, p->tmB, p->tmC, tp, p->grid, s);
         return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "tiled kernel launch");
@@ -711,7 +782,8 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     if (plan->path == HGEMM_PATH_TILED) {
         r.tile_m = plan->pair ? 256 : 128;
         r.tile_n = plan->bn;
-        r.stages = plan->pair ? hg::pair_stages() : hg::tiled_stages(plan->bn);
+        r.stages = plan->pair ? hg::pair_stages(plan->pair_ks) : hg::tiled_stages(plan->bn);
+        if (plan->pair) r.tile_k = 64 * plan->pair_ks;
         r.tma_store = plan->ldc_tma ? 1 : 0;
     } else if (plan->path == HGEMM_PATH_SKINNY) {
         r.tile_m = plan->nu;
@@ -727,6 +799,11 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     if (plan->path == HGEMM_PATH_ZERO_FILL) r.kernels_per_run = 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
     r.tail_split = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->tail_split : 1;
+    r.stream_k = plan->path == HGEMM_PATH_TILED && plan->pair && plan->stream_k ? 1 : 0;
+    r.wide_boxes = plan->path == HGEMM_PATH_TILED && plan->pair && plan->bn == 256 &&
+                           plan->K % 64 == 0 && plan->N % 64 == 0 && (plan->wide || !plan->maps_ok)
+                       ? 1
+                       : 0;
     *info = r;
     return HGEMM_OK;
 }

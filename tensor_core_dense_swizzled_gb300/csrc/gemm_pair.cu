@@ -44,16 +44,30 @@ constexpr int EPI_WARPS = 4;
 
 // PN = columns per pair tile (256 or 224); each CTA stages PN/2 columns of B
 // in two 64-column blocks (the second partly used when PN = 224).
-template <int PN>
+// KS = 64-wide K blocks per pipeline stage.  One thread issues every MMA of
+// the pair, and each stage costs it a barrier wait and a commit on top of
+// its 4 x KS MMAs; with KS = 1 that overhead (about 240 of 576 cycles per
+// stage, measured on GB300) left the tensor pipe idle about 11 % of the
+// time, so stages hold two K blocks: 3 stages of 64 KB per CTA, the same
+// bytes in flight as 6 of 32 KB.
+template <int PN, int KS>
 struct PairCfg {
     static_assert(PN == 256 || PN == 224, "pair tile N");
+    static_assert(KS == 1 || KS == 2, "K blocks per stage");
     static constexpr int BNH = PN / 2;
     static constexpr int B_BLOCKS = (BNH + 63) / 64;
-    static constexpr uint32_t A_BYTES = BM * BK * 2;     // 16 KB
-    static constexpr uint32_t B_BLOCK = BK * 128;        // 64 k x 64 n
-    static constexpr uint32_t B_BYTES = B_BLOCKS * B_BLOCK;  // 16 KB
+    static constexpr uint32_t A_SUB = BM * BK * 2;            // 16 KB per K block
+    static constexpr uint32_t B_BLOCK = BK * 128;             // 64 k x 64 n
+    static constexpr uint32_t B_SUB = B_BLOCKS * B_BLOCK;     // 16 KB per K block
+    static constexpr uint32_t A_BYTES = KS * A_SUB;
+    static constexpr uint32_t B_BYTES = KS * B_SUB;
+    // B of a stage: 64-column block j holds its KS x 64 K rows contiguously
+    // (128-byte rows), block j at j * B_COLS -- the order a 4-D box
+    // (64 n, KS x 64 k, B_BLOCKS) lands in; K block s of block j is at
+    // j * B_COLS + s * B_BLOCK.
+    static constexpr uint32_t B_COLS = KS * B_BLOCK;
+    static constexpr uint32_t SUB_BYTES = A_SUB + B_SUB;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t TX_BYTES = 2 * STAGE_BYTES;      // both CTAs
     static constexpr int STG_TOTAL = EPI_WARPS * EPI_STG_BUFS * EPI_STG_BYTES;
     static constexpr int STAGES = (232448 - STG_TOTAL - 2048) / STAGE_BYTES;
     static constexpr uint32_t TMEM_STRIDE = 256;
@@ -68,33 +82,104 @@ struct PairCfg {
     static_assert(SMEM_TOTAL <= 232448, "shared memory budget");
 };
 
-// Work unit u -> tile t and K-block range [kb0, kb1).  `half` is -1 for a
-// whole tile, else the K half (0 or 1) of a split tail tile.
-__device__ __forceinline__ void pair_unit(const TiledParams &p, int u, int &t, int &kb0, int &kb1,
-                                          int &half) {
-    if (u < p.full_tiles || p.tail_split == 1) {
-        t = u;
-        kb0 = 0;
-        kb1 = p.num_kb;
-        half = -1;
-        return;
-    }
-    const int v = u - p.full_tiles;
-    t = p.full_tiles + (v >> 1);
-    half = v & 1;
-    const int mid = p.num_kb >> 1;
-    kb0 = half ? mid : 0;
-    kb1 = half ? p.num_kb : mid;
-}
+// One piece of a pair's work: K steps [ks0, ks1) of tile t, and what the
+// epilogue does with the accumulator.
+enum PieceRole : int {
+    PIECE_WHOLE = -1,  // the whole K range: store C
+    PIECE_HALF0 = 0,   // K half 0 / 1 of a split tail tile; the other half runs
+    PIECE_HALF1 = 1,   //   on another pair at the same time (symmetric exchange)
+    PIECE_CLOSE = 2,   // stream-K: the first K steps of a tile whose remaining
+                       //   steps the next pair ran first; add its partial, store C
+    PIECE_SPILL = 3,   // stream-K: the last K steps of a tile; publish the partial
+};
+struct Piece {
+    int t, ks0, ks1, role;
+    int slot;  // PIECE_HALF0/1: index of the split tile among the split tiles
+};
 
-// Bounded spin on a global flag set (with release) by another CTA.
+// The sequence of pieces a pair runs; the producer, the MMA issuer and the
+// epilogue of both CTAs walk the same sequence.
+//
+// Unit mode (p.stream_k == 0): units pair, pair + npairs, ... in raster
+// order, so that the pairs of a wave work on neighbouring tiles at the same
+// K step and share their operand blocks in L2.  With p.tail_split == 2 the
+// T = tiles - full_tiles tiles that do not fill a wave are split in two K
+// halves, and those 2T <= pairs half units come FIRST (units 0 .. 2T - 1,
+// tiles 0 .. T - 1), the whole tiles T .. tiles - 1 after them.  The two
+// halves of a tile run at the same time on two pairs and exchange partials
+// through global memory; a release/acquire hand-over between SMs took about
+// 4.5 us on GB300, which the first wave hides behind the next whole tile
+// (with the halves last it was exposed at the end of the kernel).
+// Stream-K mode (p.stream_k == 1): whole tiles below p.full_tiles first,
+// then the K steps of the last S = tiles -
+// full_tiles tiles (pairs <= S < 2 pairs) are dealt to the pairs as
+// contiguous, equal ranges (to one step), so every pair ends at the same
+// time.  Each range is at least num_ks long, so a tile is cut at most once:
+// its last steps are the FIRST piece of the next pair's range (run at the
+// start, PIECE_SPILL) and its first steps the LAST piece of this pair's range
+// (run at the end, PIECE_CLOSE); the closer finds its partner's partial
+// published long before it needs it.  (Dealing all tiles this way spreads
+// the pairs over the whole raster at unrelated K steps: 8192^3 ran 14 %
+// slower than whole tiles, from L2 misses.)
+struct PairSched {
+    int u;
+    int s, s_end;
+    __device__ __forceinline__ PairSched(const TiledParams &p, int num_ks, int pair, int npairs) {
+        u = pair;
+        s = s_end = 0;
+        if (p.stream_k) {
+            const int total = (p.tiles - p.full_tiles) * num_ks;
+            const int q = total / npairs, r = total % npairs;
+            s = pair * q + min(pair, r);
+            s_end = s + q + (pair < r ? 1 : 0);
+        }
+    }
+    __device__ __forceinline__ bool next(const TiledParams &p, int num_ks, int npairs, Piece &w) {
+        if (p.stream_k && u >= p.full_tiles) {
+            if (s >= s_end) return false;
+            const int r = s / num_ks;
+            w.t = p.full_tiles + r;
+            w.ks0 = s - r * num_ks;
+            w.ks1 = min(num_ks, w.ks0 + (s_end - s));
+            s += w.ks1 - w.ks0;
+            w.role = (w.ks0 == 0 && w.ks1 == num_ks) ? PIECE_WHOLE
+                     : w.ks0 == 0                    ? PIECE_CLOSE
+                                                     : PIECE_SPILL;
+            return true;
+        }
+        if (!p.stream_k && u >= p.units) return false;
+        const int halves = (p.stream_k || p.tail_split == 1) ? 0 : p.units - p.full_tiles;  // 2T
+        if (u < halves) {
+            w.t = u >> 1;
+            w.slot = u >> 1;
+            w.role = u & 1;
+            const int mid = num_ks >> 1;
+            w.ks0 = w.role ? mid : 0;
+            w.ks1 = w.role ? num_ks : mid;
+        } else {
+            w.t = u - (halves >> 1);
+            w.ks0 = 0;
+            w.ks1 = num_ks;
+            w.role = PIECE_WHOLE;
+        }
+        u += npairs;
+        return true;
+    }
+};
+
+// Bounded spin on a global flag set (with release) by another CTA.  Polls
+// with relaxed loads; the fence after the load that sees the flag makes the
+// pair an acquire (one fence instead of one per poll).
 __device__ __forceinline__ bool wait_flag_bounded(const int32_t *flag, const WaitCtl &c,
                                                   int32_t code) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0; it < kMaxWaitIterations; ++it) {
         int32_t v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-        if (v) return true;
+        asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            return true;
+        }
         if (*c.abort_flag) return false;
         if (globaltimer_ns() - t0 > c.timeout_ns) break;
     }
@@ -118,11 +203,11 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t pari
     return false;
 }
 
-template <int PN, int OUT, bool TMA_STORE>
+template <int PN, int KS, int OUT, bool TMA_STORE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     hgemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const TiledParams p) {
-    using Cfg = PairCfg<PN>;
+    using Cfg = PairCfg<PN, KS>;
     constexpr int BNH = Cfg::BNH;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -145,6 +230,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const int pair = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
+    const int num_ks = (p.num_kb + KS - 1) / KS;  // pipeline steps per tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -185,26 +271,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int u = pair; ok && u < p.units; u += npairs) {
-                int t, kb0, kb1, half;
-                pair_unit(p, u, t, kb0, kb1, half);
+            PairSched sched(p, num_ks, pair, npairs);
+            Piece w;
+            while (ok && sched.next(p, num_ks, npairs, w)) {
                 int b, mt, nt;
-                grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);
+                grouped_tile(w.t, p.num_m, p.num_n, p.group_m, b, mt, nt);
                 const int m0 = mt * (2 * BM) + static_cast<int>(rank) * BM;
                 const int n0 = nt * PN + static_cast<int>(rank) * BNH;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int ks = w.ks0; ks < w.ks1; ++ks) {
                     if (!wait_bounded(empty(stage), phase ^ 1u, wc,
                                       timeout_code(ROLE_PRODUCER, stage))) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = mapa_shared(full(stage), 0);  // the leader's full[stage]
-                    if (rank == 0) mbar_arrive_expect_tx(full(stage), Cfg::TX_BYTES);
-                    tma_load_3d_pair(sA + stage * Cfg::A_BYTES, &tmA, fb, kb * BK, m0, b);
+                    const uint32_t dA = sA + stage * Cfg::A_BYTES;
+                    const uint32_t dB = sB + stage * Cfg::B_BYTES;
+                    if (p.wide_boxes) {
+                        // One copy per operand (each TMA instruction costs the
+                        // issuing thread ~90 cycles, which adds to the stage's
+                        // latency).  The boxes are whole even past the last K
+                        // block (zero-filled), so the bytes are the stage's.
+                        if (rank == 0) mbar_arrive_expect_tx(full(stage), 2u * Cfg::STAGE_BYTES);
+                        tma_load_4d_pair(dA, &tmA, fb, 0, m0, ks * KS, b);
+                        tma_load_4d_pair(dB, &tmB, fb, 0, ks * KS * BK, n0 / 64, b);
+                    } else {
+                        // K blocks of this step that exist (the last step of an
+                        // odd count has one); the leader arms for both CTAs' bytes.
+                        const int nsub = min(KS, p.num_kb - ks * KS);
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(full(stage), 2u * nsub * Cfg::SUB_BYTES);
 #pragma unroll
-                    for (int j = 0; j < Cfg::B_BLOCKS; ++j)
-                        tma_load_3d_pair(sB + stage * Cfg::B_BYTES + j * Cfg::B_BLOCK, &tmB, fb,
-                                         n0 + j * 64, kb * BK, b);
+                        for (int s = 0; s < KS; ++s) {
+                            if (s >= nsub) break;
+                            const int kb = ks * KS + s;
+                            tma_load_3d_pair(dA + s * Cfg::A_SUB, &tmA, fb, kb * BK, m0, b);
+#pragma unroll
+                            for (int j = 0; j < Cfg::B_BLOCKS; ++j)
+                                tma_load_3d_pair(dB + j * Cfg::B_COLS + s * Cfg::B_BLOCK, &tmB, fb,
+                                                 n0 + j * 64, kb * BK, b);
+                        }
+                    }
                     ++issued;
                     if (++stage == Cfg::STAGES) {
                         stage = 0;
@@ -237,9 +344,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int u = pair; ok && u < p.units; u += npairs, ++local) {
-                int t, kb0, kb1, half;
-                pair_unit(p, u, t, kb0, kb1, half);
+            PairSched sched(p, num_ks, pair, npairs);
+            Piece w;
+            for (; ok && sched.next(p, num_ks, npairs, w); ++local) {
+                const int ks0 = w.ks0, ks1 = w.ks1;
                 const int buf = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
                 if (!wait_bounded_cluster(tempty(buf), tph ^ 1u, wc,
@@ -249,19 +357,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * Cfg::TMEM_STRIDE;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int ks = ks0; ks < ks1; ++ks) {
                     if (!wait_bounded(full(stage), phase, wc, timeout_code(ROLE_MMA, stage))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = sA + stage * Cfg::A_BYTES;
-                    const uint32_t b0 = sB + stage * Cfg::B_BYTES;
+                    const int nsub = min(KS, p.num_kb - ks * KS);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(b0 + k * 16 * 128, Cfg::B_BLOCK, 1024);
-                        umma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                    for (int s = 0; s < KS; ++s) {
+                        if (s >= nsub) break;
+                        const uint32_t a0 = sA + stage * Cfg::A_BYTES + s * Cfg::A_SUB;
+                        const uint32_t b0 = sB + stage * Cfg::B_BYTES + s * Cfg::B_BLOCK;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+                            const uint64_t bd = sdesc_sw128(b0 + k * 16 * 128, Cfg::B_COLS, 1024);
+                            umma_f16_pair(d_tmem, ad, bd, p.idesc,
+                                          (ks > ks0 || s > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit_pair(empty(stage), 0x3);
                     if (++stage == Cfg::STAGES) {
@@ -285,13 +399,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const EpiArgs epi{&tmC, p.C, p.ldc, p.strideC, p.M, p.N};
         int sbuf = 0;
         int local = 0;
-        for (int u = pair; u < p.units; u += npairs, ++local) {
-            int t, kb0, kb1, half;
-            pair_unit(p, u, t, kb0, kb1, half);
+        constexpr int NCH = PN / 32;  // 32-column chunks of a warp's accumulator rows
+        PairSched sched(p, num_ks, pair, npairs);
+        Piece w;
+        while (sched.next(p, num_ks, npairs, w)) {
+            const int t = w.t;
             int b, mt, nt;
             grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);
             const int buf = local & 1;
             const uint32_t tph = (local >> 1) & 1;
+            ++local;
             if (!wait_bounded_warp(tfull(buf), tph, wc, timeout_code(ROLE_EPILOGUE, buf))) break;
             tc_fence_after();
             const uint32_t tbase =
@@ -302,11 +419,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             auto release = [&] {
                 if (lane == 0) mbar_arrive_cluster(release_bar);
             };
-            if (half < 0) {
+            if (w.role == PIECE_WHOLE) {
                 drain_accumulator<OUT, TMA_STORE, PN>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
                                                       release);
                 continue;
             }
+            if (w.role >= PIECE_CLOSE) {
+                // Stream-K cut tile.  Slot k belongs to the cut at the start of
+                // pair k's range: pair k spills there (its first piece), pair
+                // k - 1 closes from there (its last piece).  One fp32 region of
+                // NCH x 32 x 32 and one flag per (slot, CTA, warp).
+                const int slot = w.role == PIECE_SPILL ? pair : pair + 1;
+                const int idx = (slot * 2 + static_cast<int>(rank)) * EPI_WARPS + q;
+                int32_t *flag = p.tail_sync + idx;
+                float *region = p.partials + static_cast<int64_t>(idx) * (NCH * 1024);
+                if (w.role == PIECE_SPILL) {
+                    spill_accumulator(tbase, region, 0, NCH);
+                    tc_fence_before();
+                    __syncwarp();
+                    release();  // TMEM read: the MMA may move on
+                    // the warp barrier orders every lane's stores before lane
+                    // 0's release (release is cumulative)
+                    __syncwarp();
+                    if (lane == 0)
+                        asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1)
+                                     : "memory");
+                    continue;
+                }
+                int ok = 1;
+                if (lane == 0)
+                    ok = wait_flag_bounded(flag, wc, timeout_code(ROLE_EPILOGUE, 0x200 + idx)) ? 1 : 0;
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                __syncwarp();
+                if (!ok) {
+                    tc_fence_before();
+                    release();
+                    break;
+                }
+                drain_accumulator<OUT, TMA_STORE, PN, true>(tbase, stg, stg_f, sbuf, row0, col0, b,
+                                                            epi, release, region, 0, NCH);
+                if (lane == 0) *flag = 0;  // read: ready for the next run
+                continue;
+            }
+            const int half = w.role;
             // Split tail tile: its two K halves run on two pairs at the same
             // time.  Each half owns half of the 32-column chunks of every warp's
             // 32 rows: it spills the chunks the other half owns (fp32) and
@@ -315,17 +470,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // before spilling, so both waits end; every output element is one
             // two-term fp32 sum, which commutes, so the result does not depend
             // on which half finishes first.  The reader clears its flag.
-            constexpr int NCH = PN / 32;
             constexpr int HCH = (NCH + 1) / 2;  // chunks owned by half 0
-            const int slot = ((t - p.full_tiles) * 2 + static_cast<int>(rank)) * EPI_WARPS + q;
+            const int slot = (w.slot * 2 + static_cast<int>(rank)) * EPI_WARPS + q;
             int32_t *flags = p.tail_sync + 2 * slot;          // flags[h]: region of half h ready
             float *region = p.partials + static_cast<int64_t>(slot) * (2 * 4 * 1024);
             const int other = half ^ 1;
             const int own_lo = half ? HCH : 0, own_hi = half ? NCH : HCH;
             const int oth_lo = other ? HCH : 0, oth_hi = other ? NCH : HCH;
             spill_accumulator(tbase, region + other * (4 * 1024), oth_lo, oth_hi);
-            __threadfence();
-            __syncwarp();
+            __syncwarp();  // every lane's stores before lane 0's release (cumulative)
             if (lane == 0)
                 asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flags + other), "r"(1)
                              : "memory");
@@ -356,17 +509,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int PN, int OUT, bool TS>
+template <int PN, int KS, int OUT, bool TS>
 cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const TiledParams &p, int grid, cudaStream_t stream) {
-    auto kern = hgemm_pair_kernel<PN, OUT, TS>;
+    auto kern = hgemm_pair_kernel<PN, KS, OUT, TS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PairCfg<PN>::SMEM_TOTAL);
+                                         PairCfg<PN, KS>::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = PairCfg<PN>::SMEM_TOTAL;
+    cfg.dynamicSmemBytes = PairCfg<PN, KS>::SMEM_TOTAL;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -380,16 +533,18 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p);
 }
 
+// Both K-step variants use the same shared memory (192 KB of stages), so
+// either gives the co-residency of the other.
 template <int OUT, bool TS>
 int max_pairs_impl() {
-    auto kern = hgemm_pair_kernel<256, OUT, TS>;
+    auto kern = hgemm_pair_kernel<256, 2, OUT, TS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PairCfg<256>::SMEM_TOTAL) != cudaSuccess)
+                             PairCfg<256, 2>::SMEM_TOTAL) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = PairCfg<256>::SMEM_TOTAL;
+    cfg.dynamicSmemBytes = PairCfg<256, 2>::SMEM_TOTAL;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -402,35 +557,40 @@ int max_pairs_impl() {
     return n;
 }
 
-template <int PN, int OUT>
+template <int PN, int KS, int OUT>
 cudaError_t launch_ts(bool ts, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap &tmC, const TiledParams &p, int grid, cudaStream_t s) {
-    return ts ? launch_impl<PN, OUT, true>(tmA, tmB, tmC, p, grid, s)
-              : launch_impl<PN, OUT, false>(tmA, tmB, tmC, p, grid, s);
+    return ts ? launch_impl<PN, KS, OUT, true>(tmA, tmB, tmC, p, grid, s)
+              : launch_impl<PN, KS, OUT, false>(tmA, tmB, tmC, p, grid, s);
 }
 
-template <int PN>
+template <int PN, int KS>
 cudaError_t launch_out(int out, bool ts, const CUtensorMap &tmA, const CUtensorMap &tmB,
                        const CUtensorMap &tmC, const TiledParams &p, int grid, cudaStream_t s) {
     switch (out) {
-        case OUT_F16: return launch_ts<PN, OUT_F16>(ts, tmA, tmB, tmC, p, grid, s);
-        case OUT_BF16: return launch_ts<PN, OUT_BF16>(ts, tmA, tmB, tmC, p, grid, s);
-        case OUT_F32: return launch_ts<PN, OUT_F32>(ts, tmA, tmB, tmC, p, grid, s);
+        case OUT_F16: return launch_ts<PN, KS, OUT_F16>(ts, tmA, tmB, tmC, p, grid, s);
+        case OUT_BF16: return launch_ts<PN, KS, OUT_BF16>(ts, tmA, tmB, tmC, p, grid, s);
+        case OUT_F32: return launch_ts<PN, KS, OUT_F32>(ts, tmA, tmB, tmC, p, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-int pair_stages() { return PairCfg<256>::STAGES; }
+int pair_stages(int ks) { return ks == 1 ? PairCfg<256, 1>::STAGES : PairCfg<256, 2>::STAGES; }
 
 int pair_max_active_pairs() { return max_pairs_impl<OUT_BF16, true>(); }
 
-cudaError_t launch_pair(int pn, int out, bool tma_store, const CUtensorMap &tmA,
+cudaError_t launch_pair(int pn, int ks, int out, bool tma_store, const CUtensorMap &tmA,
                         const CUtensorMap &tmB, const CUtensorMap &tmC, const TiledParams &p,
                         int grid, cudaStream_t stream) {
-    if (pn == 256) return launch_out<256>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
-    if (pn == 224) return launch_out<224>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
+    if (ks != 1 && ks != 2) return cudaErrorInvalidValue;
+    if (pn == 256)
+        return ks == 2 ? launch_out<256, 2>(out, tma_store, tmA, tmB, tmC, p, grid, stream)
+                       : launch_out<256, 1>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
+    if (pn == 224)
+        return ks == 2 ? launch_out<224, 2>(out, tma_store, tmA, tmB, tmC, p, grid, stream)
+                       : launch_out<224, 1>(out, tma_store, tmA, tmB, tmC, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

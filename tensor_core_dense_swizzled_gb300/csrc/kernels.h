@@ -39,6 +39,15 @@ struct TiledParams {
     int32_t full_tiles, tail_split, units;
     float *partials;               // [tail][rank][warp][chunk][32 rows][32 cols] fp32
     int32_t *tail_sync;            // [tail][rank][warp][2]: arrival counter, ready flag (zero between runs)
+    // Pair kernel only: 1 when the A and B maps are the 4-D views that load a
+    // whole stage of each operand with one copy (see launch_pair).
+    int32_t wide_boxes;
+    // Pair kernel only: 1 = stream-K schedule (tiles >= pairs): tiles below
+    // full_tiles run whole, the K steps of the rest (pairs <= rest < 2 pairs)
+    // are dealt to the pairs in equal contiguous ranges; cut tiles meet
+    // through partials / tail_sync slots indexed by pair ([pair][rank][warp]:
+    // PN / 32 chunks of 32 x 32 fp32, one flag).
+    int32_t stream_k;
 };
 
 // Skinny kernel: C^T = B^T . A^T, NT x 128 output columns of C per work
@@ -76,10 +85,19 @@ cudaError_t launch_skinny(int nu, int nt, int out, const CUtensorMap &tmA, const
 
 // CTA-pair kernel (cta_group::2): 256 x pn tiles, TiledParams with num_m
 // counting 256-row tiles and num_n pn-column tiles; `grid` = 2 x pairs.
-int pair_stages();
+// ks = 64-wide K blocks per pipeline stage (1 or 2).
+//
+// Maps: with p.wide_boxes == 0, tmA is the 3-D (K, M, batch) map with
+// 64 x 128 boxes and tmB the 3-D (N, K, batch) map with 64 x 64 boxes (both
+// 128-byte swizzled), loaded box by box.  With p.wide_boxes == 1 (pn = 256,
+// K and N multiples of 64) they are 4-D views that split the contiguous
+// dimension in 64-element blocks: tmA (64, M, K / 64, batch) with boxes
+// 64 x 128 x ks, tmB (64, K, N / 64, batch) with boxes 64 x 64 ks x 2, so one
+// copy per operand fills a stage.
+int pair_stages(int ks);
 int pair_max_active_pairs();  // co-resident 2-CTA clusters on the current device (0 on error)
 // pn = columns per pair tile: 256 or 224 (112 B columns per CTA).
-cudaError_t launch_pair(int pn, int out, bool tma_store, const CUtensorMap &tmA,
+cudaError_t launch_pair(int pn, int ks, int out, bool tma_store, const CUtensorMap &tmA,
                         const CUtensorMap &tmB, const CUtensorMap &tmC, const TiledParams &p,
                         int grid, cudaStream_t stream);
 

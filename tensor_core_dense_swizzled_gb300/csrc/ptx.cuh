@@ -313,6 +313,17 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 4-D form of tma_load_3d_pair (coordinates x innermost).
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *m,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y,
+                                                 int32_t z, int32_t w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster)
+        : "memory");
+}
+
 // Whole warp, in BOTH CTAs of the pair: allocates the same TMEM columns in each.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),

@@ -56,6 +56,8 @@ class Options(ctypes.Structure):
         ("cta_pair", ctypes.c_int),
         ("skinny_tile_n", ctypes.c_int),
         ("no_tail_split", ctypes.c_int),
+        ("pair_k_blocks", ctypes.c_int),
+        ("tail_mode", ctypes.c_int),
     ]
 
 
@@ -74,6 +76,8 @@ class PlanInfo(ctypes.Structure):
         ("kernels_per_run", ctypes.c_int),
         ("workspace_bytes", ctypes.c_int64),
         ("tail_split", ctypes.c_int),
+        ("wide_boxes", ctypes.c_int),
+        ("stream_k", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

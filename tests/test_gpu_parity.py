@@ -181,14 +181,19 @@ def test_identity_B_returns_A_on_cta_pairs(dev, din, dout, pn):
 
 
 @pytest.mark.parametrize("shape", [(256, 256, 64), (300, 520, 200), (513, 700, 1000), (1024, 768, 2048),
-                                   (2560, 2304, 256), (130, 260, 70)])
+                                   (2560, 2304, 256), (130, 260, 70), (384, 512, 130), (512, 512, 320)])
 @pytest.mark.parametrize("din,dout", [("bf16", "bf16"), ("f16", "f32"), ("f16", "f16")])
 @pytest.mark.parametrize("pn", [256, 224])
-def test_cta_pair_random_shapes(dev, shape, din, dout, pn):
+@pytest.mark.parametrize("ks", [1, 2])
+def test_cta_pair_random_shapes(dev, shape, din, dout, pn, ks):
+    """ks = K blocks per pipeline stage; with 2, an odd number of 64-wide K
+    blocks leaves the last stage with one (130 and 320 have 3 and 5)."""
     M, N, K = shape
     got, Cref, Den, info = run_case(dev, M, N, K, din, dout, seed=M + 2 * N + K,
-                                    options=H.Options(cta_pair=1, tile_n=pn))
-    assert info["tile_m"] == 256 and info["grid"] % 2 == 0
+                                    options=H.Options(cta_pair=1, tile_n=pn, pair_k_blocks=ks))
+    assert info["tile_m"] == 256 and info["grid"] % 2 == 0 and info["tile_k"] == 64 * ks
+    # one TMA copy per operand per stage exactly when the 4-D views apply
+    assert info["wide_boxes"] == int(pn == 256 and K % 64 == 0 and N % 64 == 0)
     check(got, Cref, Den, dout)
 
 
@@ -200,17 +205,43 @@ def test_cta_pair_fallback_paths(dev, opt):
     check(got, Cref, Den, "f32")
 
 
-@pytest.mark.parametrize("shape", [(512, 1024, 512), (300, 520, 200), (1024, 768, 96), (640, 1000, 333)])
+@pytest.mark.parametrize("shape", [(2560, 2048, 256, 1), (4096, 2048, 192, 1), (2304, 2304, 130, 1),
+                                   (1280, 2048, 256, 2), (2560, 2000, 320, 1)])
 @pytest.mark.parametrize("dout", ["f32", "bf16", "f16"])
-def test_cta_pair_split_tail(dev, shape, dout):
+@pytest.mark.parametrize("ks", [1, 2])
+def test_cta_pair_stream_k(dev, shape, dout, ks):
+    """At least one full wave of pair tiles but not a whole number of waves:
+    the tiles' K steps are dealt to the pairs in equal contiguous ranges, so
+    some tiles are cut between two pairs (one spills its partial first, the
+    other adds it and stores).  80, 128 and 81 tiles of 256 x 256 on about 76
+    pairs; K = 130 leaves an odd number of 64-wide K blocks; the batched case
+    cuts tiles across batch entries; N = 2000 is not a multiple of 64 (box-by-
+    box loads).  Three runs in a row must agree bit for bit."""
+    M, N, K, batch = shape
+    got, Cref, Den, info = run_case(dev, M, N, K, "bf16", dout, batch=batch, seed=M + N + K + 11,
+                                    options=H.Options(cta_pair=1, pair_k_blocks=ks, tail_mode=3),
+                                    runs=3)
+    assert info["tile_m"] == 256 and info["stream_k"] == 1 and info["tail_split"] == 1
+    check(got, Cref, Den, dout)
+
+
+@pytest.mark.parametrize("shape", [(512, 1024, 512), (300, 520, 200), (1024, 768, 96), (640, 1000, 333),
+                                   (512, 768, 130), (256, 512, 192), (2560, 2048, 256), (4096, 4096, 128)])
+@pytest.mark.parametrize("dout", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("ks", [1, 2])
+def test_cta_pair_split_tail(dev, shape, dout, ks):
     """Fewer pair tiles than half the pairs: every tile is a tail tile whose two
     K halves run on two pairs and meet in the two-arriver fixup.  Three runs
     in a row must agree bit for bit (counters and flags reset, and the
-    two-term sum does not depend on which half arrives first)."""
+    two-term sum does not depend on which half arrives first).  The halves
+    split the tile's pipeline stages (ks K blocks each); a tile of one stage
+    is not split.  With more tiles than pairs (80 and 256 tiles on about 76
+    pairs) the halves of the few left-over tiles run first, whole tiles after."""
     M, N, K = shape
     got, Cref, Den, info = run_case(dev, M, N, K, "bf16", dout, seed=M + N + K + 7,
-                                    options=H.Options(cta_pair=1), runs=3)
-    assert info["tile_m"] == 256 and info["tail_split"] == 2
+                                    options=H.Options(cta_pair=1, pair_k_blocks=ks), runs=3)
+    steps = -(-(-(-K // 64)) // ks)
+    assert info["tile_m"] == 256 and info["tail_split"] == (2 if steps >= 2 else 1)
     check(got, Cref, Den, dout)
 
 
