@@ -81,7 +81,7 @@ typedef struct {
     uint64_t timeout_ns;      /* 0: default (2 s); device watchdog for each pipeline wait */
     int cta_pair;             /* tiled path: 0 automatic, 1 force 256 x 256 tiles on CTA pairs
                                  (tcgen05 cta_group::2), 2 force single-CTA 128 x tile_n tiles */
-    int skinny_tile_n;        /* skinny path: 0 automatic, or 128 / 256 / 512 columns of C per
+    int skinny_tile_n;        /* skinny path: 0 automatic, or 128 / 192 / 256 / 384 / 512 columns of C per
                                  work unit */
     int no_tail_split;        /* CTA pairs: 1 runs whole tiles only, so the last partial wave of
                                  tiles stays whole (no stream-K, no K halves) */
@@ -92,6 +92,10 @@ typedef struct {
                                  (needs 2 x tail tiles <= pairs); 3 stream-K (needs tiles >=
                                  pairs).  Automatic takes 3, else 2, else 1, the first whose
                                  condition holds; a forced 3 or 2 falls back the same way. */
+    int skinny_stream_k;      /* skinny path: 0 automatic (off), 1 off, 2 on: the (tile, K block)
+                                 steps are dealt to the SMs in equal contiguous ranges */
+    int skinny_prefetch;      /* skinny path: stages of B each CTA asks L2 for before it waits on
+                                 the previous kernel of the stream; 0 or -1 none */
 } hgemm_options_t;
 
 /* Read-only description of what a plan will launch. */
@@ -109,9 +113,9 @@ typedef struct {
     int tail_split;       /* CTA pairs: 2 when the last partial wave's tiles run as two K halves */
     int wide_boxes;       /* CTA pairs: 1 when each pipeline stage of A and of B is one TMA copy
                              (4-D views; 256-wide tiles, K and N multiples of 64) */
-    int stream_k;         /* CTA pairs: 1 when the tiles' K steps are dealt to the pairs in equal
-                             contiguous ranges (at least one full wave of tiles, not a whole
-                             number of waves) */
+    int stream_k;         /* 1 when K steps are dealt in equal contiguous ranges: CTA pairs
+                             (tail_mode 3) or the skinny path (skinny_stream_k); on the skinny
+                             path split_k is then the most pieces a column tile is cut into */
 } hgemm_plan_info_t;
 
 /* Creates a plan for C_b = A_b . B_b, b < batch.

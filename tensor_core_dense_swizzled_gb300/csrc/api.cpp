@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -71,7 +72,8 @@ inline int out_type(hgemm_dtype_t d) {
 hgemm_status_t encode_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dt, int esize,
                          int64_t cols, int64_t rows, int64_t batch, int64_t ld, int64_t stride,
                          uint32_t box_cols, uint32_t box_rows,
-                         CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+                         CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B,
+                         CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     auto fn = encode_fn();
     if (!fn) return fail(HGEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     int64_t bstride = stride * esize;
@@ -82,7 +84,7 @@ hgemm_status_t encode_3d(CUtensorMap *map, const void *base, CUtensorMapDataType
     cuuint32_t box[3] = {box_cols, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, promo,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(HGEMM_ERR_CUDA,
@@ -140,7 +142,8 @@ struct hgemm_plan_s {
     bool wide = false;  // pair path: A/B maps are the 4-D one-copy-per-stage views
     bool stream_k = false;  // pair path: stream-K schedule (see plan_create)
     // skinny path
-    int nu, nt, split, kb_per;  // padded M, 128-column sub-tiles per unit, K splits
+    int nu, nb, split, kb_per;  // padded M, 64-column blocks per unit, K splits
+    bool skinny_deal = false;   // stream-K dealing (split = most pieces per tile)
     int grid;
     bool ld_repack_a, ld_repack_b;  // forced by leading dimension / stride
     bool ldc_tma;                   // C's ld / stride allow TMA stores
@@ -256,7 +259,8 @@ hgemm_status_t alloc_workspace(hgemm_plan_s *p) {
     p->off_counters = off;
     size_t counters = 0, partials = 0;
     if (p->path == HGEMM_PATH_SKINNY) {
-        const int64_t num_n = ceil_div(p->N, 128);
+        // 128-column sub-tiles: ceil(nb / 2) per work unit
+        const int64_t num_n = ceil_div(p->N, 64 * p->nb) * ((p->nb + 1) / 2);
         counters = static_cast<size_t>(p->batch * num_n) * 4 * sizeof(int32_t);
         if (p->split > 1)
             partials = static_cast<size_t>(p->batch) * p->split * num_n * p->nu * 128 * sizeof(float);
@@ -365,15 +369,19 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         opt.tile_n != 256)
         return fail(HGEMM_ERR_INVALID_ARG, "tile_n must be 0, 128, 192, 224 or 256");
     if (opt.split_k < 0) return fail(HGEMM_ERR_INVALID_ARG, "split_k must be >= 0");
-    if (opt.skinny_tile_n != 0 && opt.skinny_tile_n != 128 && opt.skinny_tile_n != 256 &&
-        opt.skinny_tile_n != 512)
-        return fail(HGEMM_ERR_INVALID_ARG, "skinny_tile_n must be 0, 128, 256 or 512");
+    if (opt.skinny_tile_n != 0 && opt.skinny_tile_n != 128 && opt.skinny_tile_n != 192 &&
+        opt.skinny_tile_n != 256 && opt.skinny_tile_n != 384 && opt.skinny_tile_n != 512)
+        return fail(HGEMM_ERR_INVALID_ARG, "skinny_tile_n must be 0, 128, 192, 256, 384 or 512");
     if (opt.cta_pair < 0 || opt.cta_pair > 2)
         return fail(HGEMM_ERR_INVALID_ARG, "cta_pair must be 0, 1 or 2");
     if (opt.pair_k_blocks < 0 || opt.pair_k_blocks > 2)
         return fail(HGEMM_ERR_INVALID_ARG, "pair_k_blocks must be 0, 1 or 2");
     if (opt.tail_mode < 0 || opt.tail_mode > 3)
         return fail(HGEMM_ERR_INVALID_ARG, "tail_mode must be 0, 1, 2 or 3");
+    if (opt.skinny_stream_k < 0 || opt.skinny_stream_k > 2)
+        return fail(HGEMM_ERR_INVALID_ARG, "skinny_stream_k must be 0, 1 or 2");
+    if (opt.skinny_prefetch < -1 || opt.skinny_prefetch > 64)
+        return fail(HGEMM_ERR_INVALID_ARG, "skinny_prefetch must be in [-1, 64]");
     if (opt.cta_pair == 1 && opt.tile_n != 0 && opt.tile_n != 256 && opt.tile_n != 224)
         return fail(HGEMM_ERR_INVALID_ARG, "CTA-pair tiles are 256 x 256 or 256 x 224 (tile_n 0, 256 or 224)");
     if (opt.force_path == HGEMM_PATH_SKINNY && M > 32)
@@ -400,7 +408,7 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
     p->din = din; p->dout = dout; p->opt = opt;
     p->device = dev; p->num_sms = sms;
     p->timeout_ns = opt.timeout_ns ? opt.timeout_ns : kDefaultTimeoutNs;
-    p->bn = 0; p->nu = 0; p->nt = 1; p->split = 1; p->kb_per = 0; p->grid = 0;
+    p->bn = 0; p->nu = 0; p->nb = 2; p->split = 1; p->kb_per = 0; p->grid = 0;
     p->pair = false;
 
     if (M == 0 || N == 0) {
@@ -489,15 +497,32 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         }
     } else if (p->path == HGEMM_PATH_SKINNY) {
         p->nu = M <= 16 ? 16 : 32;
-        p->nt = opt.skinny_tile_n ? opt.skinny_tile_n / 128 : hg::pick_skinny_nt(N);
-        const int64_t work = batch * ceil_div(N, 128 * p->nt);
-        int split = opt.split_k ? opt.split_k : choose_split(work, num_kb, sms);
-        if (split > num_kb) split = num_kb;
-        if (split < 1) split = 1;
-        p->kb_per = static_cast<int>(ceil_div(num_kb, split));
-        p->split = static_cast<int>(ceil_div(num_kb, p->kb_per));  // no empty split
-        const int64_t units = work * p->split;
-        p->grid = static_cast<int>(units < sms ? units : sms);
+        p->nb = opt.skinny_tile_n ? opt.skinny_tile_n / 64 : hg::pick_skinny_nb(N, batch, sms);
+        const int64_t work = batch * ceil_div(N, 64 * p->nb);
+        const int64_t steps = work * num_kb;
+        // Deal mode (stream-K, on request only): every SM streams an equal
+        // share of the (tile, K block) steps.  On 8 x 28672 x 4096 it ran
+        // 45-54 us against 38.5 us for 112 unsplit 256-column units: the
+        // unsplit units read each row of B together (112 x 512 contiguous
+        // bytes) while dealt ranges read unrelated rows at once.
+        const bool deal = opt.skinny_stream_k == 2;
+        if (deal && steps < (int64_t(1) << 30)) {
+            p->skinny_deal = true;
+            p->grid = static_cast<int>(steps < sms ? steps : sms);
+            const int64_t q = steps / p->grid;
+            // a tile's num_kb steps meet at most (num_kb - 1) / q + 2 ranges
+            const int64_t segs = (num_kb - 1) / q + 2;
+            p->split = static_cast<int>(segs < p->grid ? segs : p->grid);
+            p->kb_per = 0;
+        } else {
+            int split = opt.split_k ? opt.split_k : choose_split(work, num_kb, sms);
+            if (split > num_kb) split = num_kb;
+            if (split < 1) split = 1;
+            p->kb_per = static_cast<int>(ceil_div(num_kb, split));
+            p->split = static_cast<int>(ceil_div(num_kb, p->kb_per));  // no empty split
+            const int64_t units = work * p->split;
+            p->grid = static_cast<int>(units < sms ? units : sms);
+        }
     }
     st = alloc_workspace(p);
     if (st != HGEMM_OK) {
@@ -553,7 +578,10 @@ hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *
         st = encode_3d(&p->tmA, A, dt, 2, p->K, p->M, p->batch, lda, sA, 64,
                        static_cast<uint32_t>(p->nu));
         if (st != HGEMM_OK) return st;
-        st = encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64);
+        // streamed once: 128-byte L2 fills (256-byte promotion measured 1.3 %
+        // slower on 8 x 28672 x 4096)
+        st = encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
         if (st != HGEMM_OK) return st;
         std::memset(&p->tmC, 0, sizeof(p->tmC));
     }
@@ -646,11 +674,15 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     sp.N = static_cast<int32_t>(p->N);
     sp.K = static_cast<int32_t>(p->K);
     sp.batch = static_cast<int32_t>(p->batch);
-    sp.num_tiles = static_cast<int32_t>(ceil_div(p->N, 128 * p->nt));
+    sp.num_tiles = static_cast<int32_t>(ceil_div(p->N, 64 * p->nb));
     sp.num_kb = static_cast<int32_t>(ceil_div(p->K, 64));
     sp.split = p->split;
     sp.kb_per_split = p->kb_per;
     sp.units = sp.batch * sp.split * sp.num_tiles;
+    sp.deal = p->skinny_deal ? 1 : 0;
+    // default none: on 8 x 28672 x 4096, 4 or 8 stages measured the same as
+    // none (38.4-38.7 us back to back), 16 and more slower
+    sp.prefetch = p->opt.skinny_prefetch > 0 ? p->opt.skinny_prefetch : 0;
     sp.idesc = hg::idesc_f16(bf, 1, 0, 128, static_cast<uint32_t>(p->nu));
     sp.C = C;
     sp.ldc = p->ldc;
@@ -659,7 +691,7 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     sp.counters = reinterpret_cast<int32_t *>(p->ws + p->off_counters);
     sp.err = err;
     sp.timeout_ns = p->timeout_ns;
-    e = hg::launch_skinny(p->nu, p->nt, out_type(p->dout), p->tmA, p->tmB, sp, p->grid, s);
+    e = hg::launch_skinny(p->nu, p->nb, out_type(p->dout), p->tmA, p->tmB, sp, p->grid, s);
     return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "skinny kernel launch");
 }
 
@@ -787,8 +819,8 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
         r.tma_store = plan->ldc_tma ? 1 : 0;
     } else if (plan->path == HGEMM_PATH_SKINNY) {
         r.tile_m = plan->nu;
-        r.tile_n = 128 * plan->nt;
-        r.stages = hg::skinny_stages(plan->nu, plan->nt);
+        r.tile_n = 64 * plan->nb;
+        r.stages = hg::skinny_stages(plan->nu, plan->nb);
         r.split_k = plan->split;
     }
     r.grid = plan->grid;
@@ -799,7 +831,10 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     if (plan->path == HGEMM_PATH_ZERO_FILL) r.kernels_per_run = 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
     r.tail_split = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->tail_split : 1;
-    r.stream_k = plan->path == HGEMM_PATH_TILED && plan->pair && plan->stream_k ? 1 : 0;
+    r.stream_k = (plan->path == HGEMM_PATH_TILED && plan->pair && plan->stream_k) ||
+                         (plan->path == HGEMM_PATH_SKINNY && plan->skinny_deal)
+                     ? 1
+                     : 0;
     r.wide_boxes = plan->path == HGEMM_PATH_TILED && plan->pair && plan->bn == 256 &&
                            plan->K % 64 == 0 && plan->N % 64 == 0 && (plan->wide || !plan->maps_ok)
                        ? 1
@@ -892,13 +927,18 @@ int pick_split(int64_t work_tiles, int num_kb, int num_sms) {
     return choose_split(work_tiles, num_kb, num_sms);
 }
 
-int pick_skinny_nt(int64_t N) {
-    // 256 columns per work unit: 512 contiguous bytes per K row of B (see
-    // gemm_skinny.cu).  Measured on 8 x 28672 x 4096: 256-column units
-    // unsplit 39.4 us, 128-column units unsplit 49.4 us (224 units = 1.5
-    // waves), 512-column units 49.5 us (only 56 CTAs busy).  Narrow products
-    // keep 128 columns so that more units exist.
-    return N >= 4096 ? 2 : 1;
+int pick_skinny_nb(int64_t N, int64_t batch, int num_sms) {
+    // Columns per work unit: each K row of B is read in runs of 128 x nb
+    // contiguous bytes, and the units of one wave read the same rows.
+    // Measured on 8 x 28672 x 4096 (back to back, best of 5): 256-column
+    // units (112 CTAs) 37.8-38.5 us; 192-column units (150 CTAs, the grid
+    // cuBLAS uses) 40.2 us; 384 with split 2 44.4 us; 128-column units
+    // unsplit 49.4 us (224 units = 1.5 waves); 512-column units 49.5 us
+    // (only 56 CTAs busy).  Narrow products keep 128 columns so that more
+    // units exist, and split K to fill the SMs.
+    (void)batch;
+    (void)num_sms;
+    return N >= 4096 ? 4 : 2;
 }
 
 hgemm_status_t set_error_detail(hgemm_status_t s, const char *msg) { return fail(s, "%s", msg); }

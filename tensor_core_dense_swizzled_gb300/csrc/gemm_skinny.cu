@@ -12,9 +12,13 @@
 //     TMA zero fill) is the MMA's N.  B^T is read MN-major straight from the
 //     row-major K x N B (64-column blocks); A^T is read K-major from the
 //     row-major M x K A.
-//   * a work unit covers NT x 128 consecutive columns of C (NT MMAs per
-//     16-deep K step), so every K row of B is read in runs of NT x 256
-//     contiguous bytes;
+//   * a work unit covers NB x 64 consecutive columns of C (NT = ceil(NB / 2)
+//     MMAs of 128 columns per 16-deep K step), so every K row of B is read in
+//     runs of NB x 128 contiguous bytes.  With NB odd the last MMA's upper 64
+//     rows read whatever follows the stage in shared memory and are never
+//     stored: the tensor core is idle on this path anyway, and 192-column
+//     units put 150 CTAs on 8 x 28672 (as cuBLAS does on GB300, grid 150
+//     of 192 x 8 tiles) where 256-column units leave 40 SMs idle;
 //   * split K into `split` ranges so that batch * split * ceil(N / (128 NT))
 //     work units fill every SM with a balanced number of units; each
 //     persistent CTA runs a deep ring of stages (about 200 KB in flight).
@@ -43,11 +47,12 @@ constexpr uint32_t pow2_at_least(uint32_t x) {
     return p;
 }
 
-template <int NU, int NT>
+template <int NU, int NB>
 struct SkinnyCfg {
     static_assert(NU == 16 || NU == 32, "padded M");
-    static_assert(NT == 1 || NT == 2 || NT == 4, "128-column sub-tiles per unit");
-    static constexpr int W_BLOCKS = 2 * NT;          // 64-column blocks of B per stage
+    static_assert(NB == 2 || NB == 3 || NB == 4 || NB == 6 || NB == 8, "64-column blocks per unit");
+    static constexpr int NT = (NB + 1) / 2;          // 128-column MMAs per K step
+    static constexpr int W_BLOCKS = NB;              // 64-column blocks of B per stage
     static constexpr uint32_t W_BLOCK = BK * 128;    // 64 k x 64 n
     static constexpr uint32_t W_BYTES = W_BLOCKS * W_BLOCK;
     static constexpr uint32_t X_BYTES = NU * BK * 2;  // A tile: NU rows x 64 k
@@ -73,11 +78,70 @@ __device__ __forceinline__ void unit_coords(const SkinnyParams &p, int u, int &b
     nt = r - s * p.num_tiles;
 }
 
-template <int NU, int NT, int OUT>
+// One piece of a CTA's work: K blocks [kb0, kb1) of column tile nt of batch
+// b.  The tile's K range is cut into nseg pieces; this is piece seg (pieces
+// are numbered in K order, and partials are summed in that order).
+struct SkPiece {
+    int b, nt, kb0, kb1, seg, nseg;
+};
+
+// The sequence of pieces a CTA runs (the producer, the MMA issuer and the
+// epilogue walk the same sequence).  Split mode: units blockIdx.x,
+// + gridDim.x, ...; unit (b, s, nt) is K split s of tile nt.  Deal mode
+// (p.deal): the steps are dealt in equal contiguous ranges, step order
+// (batch, tile, K block) with the K block fastest.
+struct SkinnySched {
+    int u, s, s_end, q, r;
+    __device__ __forceinline__ explicit SkinnySched(const SkinnyParams &p) {
+        u = blockIdx.x;
+        s = s_end = q = r = 0;
+        if (p.deal) {
+            const int total = p.batch * p.num_tiles * p.num_kb;
+            const int c = blockIdx.x, g = gridDim.x;
+            q = total / g;  // >= 1: the grid is at most the number of steps
+            r = total % g;
+            s = c * q + min(c, r);
+            s_end = s + q + (c < r ? 1 : 0);
+        }
+    }
+    // CTA whose range holds step `step` (ranges of q + 1 steps, then of q).
+    __device__ __forceinline__ int owner(int step) const {
+        const int big = r * (q + 1);
+        return step < big ? step / (q + 1) : r + (step - big) / q;
+    }
+    __device__ __forceinline__ bool next(const SkinnyParams &p, SkPiece &w) {
+        if (p.deal) {
+            if (s >= s_end) return false;
+            const int g = s / p.num_kb;
+            w.kb0 = s - g * p.num_kb;
+            w.kb1 = min(p.num_kb, w.kb0 + (s_end - s));
+            s += w.kb1 - w.kb0;
+            w.b = g / p.num_tiles;
+            w.nt = g - w.b * p.num_tiles;
+            const int first = owner(g * p.num_kb);
+            w.seg = owner(g * p.num_kb + w.kb0) - first;
+            w.nseg = owner(g * p.num_kb + p.num_kb - 1) - first + 1;
+            return true;
+        }
+        if (u >= p.units) return false;
+        int sidx;
+        unit_coords(p, u, w.b, sidx, w.nt);
+        w.kb0 = sidx * p.kb_per_split;
+        w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
+        w.seg = sidx;
+        w.nseg = p.split;
+        u += gridDim.x;
+        return true;
+    }
+};
+
+template <int NU, int NB, int OUT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     hgemm_skinny_kernel(const __grid_constant__ CUtensorMap tmX,
                         const __grid_constant__ CUtensorMap tmW, const SkinnyParams p) {
-    using Cfg = SkinnyCfg<NU, NT>;
+    using Cfg = SkinnyCfg<NU, NB>;
+    constexpr int NT = Cfg::NT;
+    constexpr int UW = NB * 64;  // columns of C per work unit
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -127,19 +191,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            // Nothing this kernel reads may be read before the previous kernel
-            // of the stream has completed (dependent launches).
+            // Ask L2 for this CTA's first p.prefetch stages of B while the
+            // previous kernel of the stream may still run (a dependent launch
+            // starts on SMs the previous kernel has left): the ramp of this
+            // kernel then overlaps the previous one's last CTAs, when DRAM is
+            // under-used.  L2 is where the GPU's memory is coherent, so data
+            // the previous kernel still writes is not read stale: nothing
+            // reaches shared memory before griddep_wait.
+            {
+                SkinnySched pre(p);
+                SkPiece w;
+                int n = 0;
+                while (n < p.prefetch && pre.next(p, w)) {
+                    for (int kb = w.kb0; kb < w.kb1 && n < p.prefetch; ++kb, ++n)
+                        for (int j = 0; j < Cfg::W_BLOCKS; ++j)
+                            tma_prefetch_3d(&tmW, w.nt * UW + j * 64, kb * BK, w.b);
+                }
+            }
+            // Nothing this kernel reads may reach shared memory before the
+            // previous kernel of the stream has completed (dependent launches).
             griddep_wait();
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
-                int b, s, nt;
-                unit_coords(p, u, b, s, nt);
-                const int kb0 = s * p.kb_per_split;
-                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-                for (int kb = kb0; kb < kb1; ++kb) {
+            SkinnySched sched(p);
+            SkPiece w;
+            while (ok && sched.next(p, w)) {
+                const int b = w.b, nt = w.nt;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(empty(stage), phase ^ 1u, wc,
                                       timeout_code(ROLE_PRODUCER, stage))) {
                         ok = false;
@@ -149,7 +229,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < Cfg::W_BLOCKS; ++j)
                         tma_load_3d(sW + stage * Cfg::W_BYTES + j * Cfg::W_BLOCK, &tmW, full(stage),
-                                    nt * (NT * TN) + j * 64, kb * BK, b);
+                                    nt * UW + j * 64, kb * BK, b);
                     tma_load_3d(sX + stage * Cfg::X_BYTES, &tmX, full(stage), kb * BK, 0, b);
                     ++issued;
                     if (++stage == Cfg::STAGES) {
@@ -176,11 +256,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x, ++local) {
-                int b, s, nt;
-                unit_coords(p, u, b, s, nt);
-                const int kb0 = s * p.kb_per_split;
-                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+            SkinnySched sched(p);
+            SkPiece w;
+            for (; ok && sched.next(p, w); ++local) {
+                const int kb0 = w.kb0, kb1 = w.kb1;
                 const int buf = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
                 if (!wait_bounded(tempty(buf), tph ^ 1u, wc, timeout_code(ROLE_MMA, 0x100 + buf))) {
@@ -203,6 +282,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < NT; ++j) {
                             // MMA A = columns j*128 .. j*128+127 of the B tile, MN-major
+                            // (with NB odd, the last one's upper 64 columns are
+                            // the shared memory after the stage: never stored)
                             const uint64_t ad = sdesc_sw128(
                                 w0 + 2 * j * Cfg::W_BLOCK + k * 16 * 128, Cfg::W_BLOCK, 1024);
                             umma_f16(d0 + j * NU, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
@@ -224,10 +305,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------ epilogue + fixup
         const int q = warp & 3;
         int local = 0;
-        const int num_n128 = (p.N + TN - 1) / TN;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++local) {
-            int b, s, nt;
-            unit_coords(p, u, b, s, nt);
+        const int num_sub = p.num_tiles * NT;  // 128-column sub-tiles: NT per unit
+        SkinnySched sched(p);
+        SkPiece w;
+        for (; sched.next(p, w); ++local) {
+            const int b = w.b, nt = w.nt;
             const int buf = local & 1;
             const uint32_t tph = (local >> 1) & 1;
             if (!wait_bounded_warp(tfull(buf), tph, wc, timeout_code(ROLE_EPILOGUE, buf))) break;
@@ -251,11 +333,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t cbase = static_cast<int64_t>(b) * p.strideC;
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-                const int n128 = nt * NT + j;
-                if (n128 >= num_n128) break;  // sub-tile entirely past N (warp-uniform)
-                const int n = n128 * TN + nl;
-                if (p.split == 1) {
-                    if (n < p.N) {
+                const int col0 = nt * UW + j * TN;  // first column of sub-tile j
+                if (col0 >= p.N) break;             // sub-tile entirely past N (warp-uniform)
+                const int sub = nt * NT + j;
+                const int n = col0 + nl;
+                // the column is in this unit and in C (with NB odd, the last
+                // sub-tile holds 64 columns of the unit)
+                const bool in = (j * TN + nl < UW) && n < p.N;
+                if (w.nseg == 1) {
+                    if (in) {
 #pragma unroll
                         for (int m = 0; m < NU; ++m)
                             if (m < p.M)
@@ -264,29 +350,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     continue;
                 }
-                const int64_t ctr = (static_cast<int64_t>(b) * num_n128 + n128) * EPI_WARPS + q;
+                const int64_t ctr = (static_cast<int64_t>(b) * num_sub + sub) * EPI_WARPS + q;
                 float *part = p.partials +
-                              ((static_cast<int64_t>(b) * p.split + s) * num_n128 + n128) *
+                              ((static_cast<int64_t>(b) * p.split + w.seg) * num_sub + sub) *
                                   (static_cast<int64_t>(NU) * TN);
 #pragma unroll
                 for (int m = 0; m < NU; ++m) __stcg(part + m * TN + nl, __uint_as_float(v[j][m]));
                 __threadfence();
                 __syncwarp();
                 int last = 0;
-                if (lane == 0) last = (atomicAdd(p.counters + ctr, 1) == p.split - 1) ? 1 : 0;
+                if (lane == 0) last = (atomicAdd(p.counters + ctr, 1) == w.nseg - 1) ? 1 : 0;
                 last = __shfl_sync(0xFFFFFFFFu, last, 0);
                 if (last) {
                     __threadfence();
-                    const int64_t stride_split = static_cast<int64_t>(num_n128) * NU * TN;
+                    const int64_t stride_split = static_cast<int64_t>(num_sub) * NU * TN;
                     const float *p0 = p.partials +
-                                      (static_cast<int64_t>(b) * p.split * num_n128 + n128) * (NU * TN);
-                    if (n < p.N) {
-                        for (int m = 0; m < p.M && m < NU; ++m) {
-                            float acc = 0.f;
-                            for (int ss = 0; ss < p.split; ++ss)
-                                acc += __ldcg(p0 + ss * stride_split + m * TN + nl);
-                            store_one<OUT>(p.C, cbase + static_cast<int64_t>(m) * p.ldc + n, acc);
+                                      (static_cast<int64_t>(b) * p.split * num_sub + sub) * (NU * TN);
+                    if (in) {
+                        // Sum in split order 0, 1, ... (deterministic).  The NU
+                        // rows of one split are independent loads issued
+                        // together, so the fixup costs one L2 round trip per
+                        // split (row by row it was NU x split dependent round
+                        // trips, which outlasted the next unit's main loop).
+                        float acc[NU];
+#pragma unroll
+                        for (int m = 0; m < NU; ++m) acc[m] = 0.f;
+                        for (int ss = 0; ss < w.nseg; ++ss) {
+                            const float *ps = p0 + ss * stride_split + nl;
+                            float t[NU];
+#pragma unroll
+                            for (int m = 0; m < NU; ++m)
+                                t[m] = (m < p.M) ? __ldcg(ps + m * TN) : 0.f;
+#pragma unroll
+                            for (int m = 0; m < NU; ++m) acc[m] += t[m];
                         }
+#pragma unroll
+                        for (int m = 0; m < NU; ++m)
+                            if (m < p.M)
+                                store_one<OUT>(p.C, cbase + static_cast<int64_t>(m) * p.ldc + n, acc[m]);
                     }
                     if (lane == 0) p.counters[ctr] = 0;  // ready for the next run
                 }
@@ -303,53 +404,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int NU, int NT, int OUT>
+template <int NU, int NB, int OUT>
 cudaError_t launch_impl(const CUtensorMap &tmX, const CUtensorMap &tmW, const SkinnyParams &p,
                         int grid, cudaStream_t stream) {
-    auto kern = hgemm_skinny_kernel<NU, NT, OUT>;
+    auto kern = hgemm_skinny_kernel<NU, NB, OUT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SkinnyCfg<NU, NT>::SMEM_TOTAL);
+                                         SkinnyCfg<NU, NB>::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    return launch_dependent(kern, grid, NUM_THREADS, SkinnyCfg<NU, NT>::SMEM_TOTAL, stream, tmX,
+    return launch_dependent(kern, grid, NUM_THREADS, SkinnyCfg<NU, NB>::SMEM_TOTAL, stream, tmX,
                             tmW, p);
 }
 
-template <int NU, int NT>
+template <int NU, int NB>
 cudaError_t launch_out(int out, const CUtensorMap &tmX, const CUtensorMap &tmW,
                        const SkinnyParams &p, int grid, cudaStream_t s) {
     switch (out) {
-        case OUT_F16: return launch_impl<NU, NT, OUT_F16>(tmX, tmW, p, grid, s);
-        case OUT_BF16: return launch_impl<NU, NT, OUT_BF16>(tmX, tmW, p, grid, s);
-        case OUT_F32: return launch_impl<NU, NT, OUT_F32>(tmX, tmW, p, grid, s);
+        case OUT_F16: return launch_impl<NU, NB, OUT_F16>(tmX, tmW, p, grid, s);
+        case OUT_BF16: return launch_impl<NU, NB, OUT_BF16>(tmX, tmW, p, grid, s);
+        case OUT_F32: return launch_impl<NU, NB, OUT_F32>(tmX, tmW, p, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 template <int NU>
-cudaError_t launch_nt(int nt, int out, const CUtensorMap &tmX, const CUtensorMap &tmW,
+cudaError_t launch_nb(int nb, int out, const CUtensorMap &tmX, const CUtensorMap &tmW,
                       const SkinnyParams &p, int grid, cudaStream_t s) {
-    switch (nt) {
-        case 1: return launch_out<NU, 1>(out, tmX, tmW, p, grid, s);
+    switch (nb) {
         case 2: return launch_out<NU, 2>(out, tmX, tmW, p, grid, s);
+        case 3: return launch_out<NU, 3>(out, tmX, tmW, p, grid, s);
         case 4: return launch_out<NU, 4>(out, tmX, tmW, p, grid, s);
+        case 6: return launch_out<NU, 6>(out, tmX, tmW, p, grid, s);
+        case 8: return launch_out<NU, 8>(out, tmX, tmW, p, grid, s);
         default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int NU>
+int stages_nb(int nb) {
+    switch (nb) {
+        case 2: return SkinnyCfg<NU, 2>::STAGES;
+        case 3: return SkinnyCfg<NU, 3>::STAGES;
+        case 4: return SkinnyCfg<NU, 4>::STAGES;
+        case 6: return SkinnyCfg<NU, 6>::STAGES;
+        case 8: return SkinnyCfg<NU, 8>::STAGES;
+        default: return 0;
     }
 }
 
 }  // namespace
 
-int skinny_stages(int nu, int nt) {
-    if (nu == 16)
-        return nt == 1 ? SkinnyCfg<16, 1>::STAGES
-                       : (nt == 2 ? SkinnyCfg<16, 2>::STAGES : SkinnyCfg<16, 4>::STAGES);
-    return nt == 1 ? SkinnyCfg<32, 1>::STAGES
-                   : (nt == 2 ? SkinnyCfg<32, 2>::STAGES : SkinnyCfg<32, 4>::STAGES);
-}
+int skinny_stages(int nu, int nb) { return nu == 16 ? stages_nb<16>(nb) : stages_nb<32>(nb); }
 
-cudaError_t launch_skinny(int nu, int nt, int out, const CUtensorMap &tmX, const CUtensorMap &tmW,
+cudaError_t launch_skinny(int nu, int nb, int out, const CUtensorMap &tmX, const CUtensorMap &tmW,
                           const SkinnyParams &p, int grid, cudaStream_t stream) {
-    if (nu == 16) return launch_nt<16>(nt, out, tmX, tmW, p, grid, stream);
-    if (nu == 32) return launch_nt<32>(nt, out, tmX, tmW, p, grid, stream);
+    if (nu == 16) return launch_nb<16>(nb, out, tmX, tmW, p, grid, stream);
+    if (nu == 32) return launch_nb<32>(nb, out, tmX, tmW, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

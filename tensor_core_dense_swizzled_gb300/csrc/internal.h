@@ -17,8 +17,8 @@ hgemm_status_t encode_map_3d(CUtensorMap *map, const void *base, int bf16, int64
 // The skinny path's split-K choice (units per wave >= 90% when possible).
 int pick_split(int64_t work_tiles, int num_kb, int num_sms);
 
-// The skinny path's default number of 128-column sub-tiles per work unit.
-int pick_skinny_nt(int64_t N);
+// The skinny path's default number of 64-column blocks per work unit.
+int pick_skinny_nb(int64_t N, int64_t batch, int num_sms);
 
 // Records `msg` as the calling thread's hgemm_last_error_detail() and returns s.
 hgemm_status_t set_error_detail(hgemm_status_t s, const char *msg);

@@ -50,12 +50,12 @@ struct TiledParams {
     int32_t stream_k;
 };
 
-// Skinny kernel: C^T = B^T . A^T, NT x 128 output columns of C per work
-// unit, split-K.  Partials and counters are indexed by 128-column sub-tile
-// (num_n128 = ceil(N / 128)).
+// Skinny kernel: C^T = B^T . A^T, NB x 64 output columns of C per work
+// unit (NT = ceil(NB / 2) sub-tiles of 128 columns), split-K.  Partials and
+// counters are indexed by sub-tile (num_tiles x NT of them).
 struct SkinnyParams {
     int32_t M, N, K, batch;
-    int32_t num_tiles;    // NT x 128-wide column tiles: ceil(N / (128 NT))
+    int32_t num_tiles;    // NB x 64-wide column tiles (work units along N): ceil(N / (64 NB))
     int32_t num_kb;       // 64-wide K blocks in total
     int32_t split;        // K splits
     int32_t kb_per_split; // K blocks per split (last split may have fewer)
@@ -63,24 +63,32 @@ struct SkinnyParams {
     uint32_t idesc;
     void *C;
     int64_t ldc, strideC;
-    float *partials;      // [batch][split][num_n128][NU][128] fp32 (split > 1)
-    int32_t *counters;    // [batch][num_n128][4] arrival counters (one per epilogue warp), zero between runs
+    float *partials;      // [batch][split][num_tiles x NT][NU][128] fp32 (split > 1)
+    int32_t *counters;    // [batch][num_tiles x NT][4] arrival counters (one per epilogue warp), zero between runs
     int32_t *err;
     uint64_t timeout_ns;
+    // 1: stream-K dealing -- the batch x num_tiles x num_kb (tile, K block)
+    // steps are dealt to the CTAs as equal contiguous ranges, so every SM
+    // streams the same number of bytes; a tile cut into several pieces is
+    // summed by the last piece to arrive.  `split` is then the most pieces a
+    // tile can be cut into (the partials' stride) and kb_per_split unused.
+    int32_t deal;
+    // Stages of B each CTA asks L2 for before waiting on the previous kernel.
+    int32_t prefetch;
 };
 
 // Shared memory the tiled kernel needs for a given BN (bytes, incl. alignment slack).
 int tiled_smem_bytes(int bn);
 int tiled_stages(int bn);
-int skinny_stages(int nu, int nt);
+int skinny_stages(int nu, int nb);
 
 // Launchers return cudaSuccess or the launch error.  `out` is an OutType.
 cudaError_t launch_tiled(int bn, int out, bool tma_store, const CUtensorMap &tmA,
                          const CUtensorMap &tmB, const CUtensorMap &tmC, const TiledParams &p,
                          int grid, cudaStream_t stream);
 
-// nu = padded M (16 or 32); nt = 128-column sub-tiles per work unit (1, 2, 4).
-cudaError_t launch_skinny(int nu, int nt, int out, const CUtensorMap &tmA, const CUtensorMap &tmB,
+// nu = padded M (16 or 32); nb = 64-column blocks per work unit (2, 3, 4, 6, 8).
+cudaError_t launch_skinny(int nu, int nb, int out, const CUtensorMap &tmA, const CUtensorMap &tmB,
                           const SkinnyParams &p, int grid, cudaStream_t stream);
 
 // CTA-pair kernel (cta_group::2): 256 x pn tiles, TiledParams with num_m

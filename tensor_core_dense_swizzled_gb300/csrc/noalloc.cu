@@ -124,11 +124,12 @@ extern "C" hgemm_status_t hgemm_skinny_noalloc(const void *A, const void *B, voi
                                 "dimensions a multiple of 8 elements (it cannot make aligned copies)");
 
     // scratch layout: [error word][counters: num_n x 4][partials: split x num_n x NU x 128 fp32]
-    // (num_n = 128-column sub-tiles; a work unit covers nt of them)
+    // (num_n = 128-column sub-tiles; a work unit of nb 64-column blocks covers
+    // ceil(nb / 2) of them)
     const int nu = M <= 16 ? 16 : 32;
-    const int nt = hg::pick_skinny_nt(N);
-    const int64_t num_n = ceil_div(N, 128);
-    const int64_t num_tiles = ceil_div(N, 128 * nt);
+    const int nb = hg::pick_skinny_nb(N, 1, sms);
+    const int64_t num_tiles = ceil_div(N, 64 * nb);
+    const int64_t num_n = num_tiles * ((nb + 1) / 2);
     const int num_kb = static_cast<int>(ceil_div(K, 64));
     const int64_t counter_bytes = round256(num_n * 4 * static_cast<int64_t>(sizeof(int32_t)));
     int split = hg::pick_split(num_tiles, num_kb, sms);
@@ -179,7 +180,7 @@ extern "C" hgemm_status_t hgemm_skinny_noalloc(const void *A, const void *B, voi
     sp.partials = reinterpret_cast<float *>(scratch + kErrBytes + counter_bytes);
     sp.timeout_ns = kTimeoutNs;
     const int grid = static_cast<int>(sp.units < sms ? sp.units : sms);
-    e = hg::launch_skinny(nu, nt, out, tmX, tmW, sp, grid, s);
+    e = hg::launch_skinny(nu, nb, out, tmX, tmW, sp, grid, s);
     if (e != cudaSuccess) return set_error_detail(HGEMM_ERR_CUDA, cudaGetErrorString(e));
     return HGEMM_OK;
 }

@@ -77,6 +77,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// Brings the box at (x, y, z) of a tiled map into L2 without writing shared
+// memory or signalling a barrier (parts outside the tensor are ignored).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int32_t x, int32_t y,
+                                                int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // Tiled 3-D store from shared memory; rows/columns outside the tensor are clipped.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src, int32_t x,
                                              int32_t y, int32_t z) {

@@ -58,6 +58,8 @@ class Options(ctypes.Structure):
         ("no_tail_split", ctypes.c_int),
         ("pair_k_blocks", ctypes.c_int),
         ("tail_mode", ctypes.c_int),
+        ("skinny_stream_k", ctypes.c_int),
+        ("skinny_prefetch", ctypes.c_int),
     ]
 
 

@@ -500,15 +500,36 @@ def test_skinny_split_k(dev, split):
     check(got, Cref, Den, "bf16")
 
 
-@pytest.mark.parametrize("cols", [128, 256, 512])
+@pytest.mark.parametrize("cols", [128, 192, 256, 384, 512])
 @pytest.mark.parametrize("M,N,K,split", [(8, 1000, 640, 3), (1, 5000, 1024, 4), (32, 700, 256, 1),
-                                         (17, 4096, 512, 2)])
+                                         (17, 4096, 512, 2), (8, 28672, 256, 1)])
 def test_skinny_unit_widths(dev, cols, M, N, K, split):
-    """Work units of 128, 256 or 512 columns (ragged last unit included)."""
+    """Work units of 128 to 512 columns (ragged last unit included).  192 and
+    384 columns are an odd number of 64-column blocks: the last MMA of a unit
+    is half used, its other 64 rows are never stored."""
     got, Cref, Den, info = run_case(dev, M, N, K, "bf16", "bf16", seed=M + N + cols, scale_b=0.02,
                                     options=H.Options(skinny_tile_n=cols, split_k=split), runs=2)
     assert info["path"] == H.HGEMM_PATH_SKINNY and info["tile_n"] == cols
     check(got, Cref, Den, "bf16")
+
+
+@pytest.mark.parametrize("cols", [128, 192, 256, 512])
+@pytest.mark.parametrize("M,N,K,batch", [(8, 1000, 640, 1), (1, 5000, 1024, 1), (32, 700, 256, 1),
+                                         (17, 4096, 512, 1), (8, 3000, 4096, 1), (4, 900, 320, 3),
+                                         (8, 200, 64, 1)])
+@pytest.mark.parametrize("dout", ["bf16", "f32"])
+def test_skinny_stream_k(dev, cols, M, N, K, batch, dout):
+    """Deal mode: the (tile, K block) steps are dealt to the SMs in equal
+    contiguous ranges, so column tiles are cut into pieces on consecutive
+    CTAs (up to `split_k` of them) and the last piece to arrive sums them in
+    K order.  Covers batches (a range crossing batch entries), a single K
+    block (no tile is cut), ragged N and three runs that must agree bit for
+    bit."""
+    got, Cref, Den, info = run_case(dev, M, N, K, "bf16", dout, batch=batch, seed=M + N + K + cols,
+                                    scale_b=0.02, runs=3,
+                                    options=H.Options(skinny_tile_n=cols, skinny_stream_k=2))
+    assert info["path"] == H.HGEMM_PATH_SKINNY and info["stream_k"] == 1 and info["tile_n"] == cols
+    check(got, Cref, Den, dout)
 
 
 def test_skinny_batched_and_misaligned(dev):
