@@ -96,6 +96,8 @@ typedef struct {
                                  steps are dealt to the SMs in equal contiguous ranges */
     int skinny_prefetch;      /* skinny path: stages of B each CTA asks L2 for before it waits on
                                  the previous kernel of the stream; 0 or -1 none */
+    int group_m;              /* tiled path: m-tiles per raster group (tiles run m-fastest within a
+                                 group of group_m tile rows); 0 automatic (16) */
 } hgemm_options_t;
 
 /* Read-only description of what a plan will launch. */

@@ -380,6 +380,8 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         return fail(HGEMM_ERR_INVALID_ARG, "tail_mode must be 0, 1, 2 or 3");
     if (opt.skinny_stream_k < 0 || opt.skinny_stream_k > 2)
         return fail(HGEMM_ERR_INVALID_ARG, "skinny_stream_k must be 0, 1 or 2");
+    if (opt.group_m < 0 || opt.group_m > 4096)
+        return fail(HGEMM_ERR_INVALID_ARG, "group_m must be in [0, 4096]");
     if (opt.skinny_prefetch < -1 || opt.skinny_prefetch > 64)
         return fail(HGEMM_ERR_INVALID_ARG, "skinny_prefetch must be in [-1, 64]");
     if (opt.cta_pair == 1 && opt.tile_n != 0 && opt.tile_n != 256 && opt.tile_n != 224)
@@ -645,7 +647,7 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.num_n = static_cast<int32_t>(ceil_div(p->N, p->bn));
         tp.num_kb = static_cast<int32_t>(ceil_div(p->K, 64));
         tp.tiles = tp.batch * tp.num_m * tp.num_n;
-        tp.group_m = 16;
+        tp.group_m = p->opt.group_m ? p->opt.group_m : 16;
         tp.idesc = hg::idesc_f16(bf, 0, 1, p->pair ? 256 : 128, static_cast<uint32_t>(p->bn));
         tp.C = C;
         tp.ldc = p->ldc;

@@ -60,6 +60,7 @@ class Options(ctypes.Structure):
         ("tail_mode", ctypes.c_int),
         ("skinny_stream_k", ctypes.c_int),
         ("skinny_prefetch", ctypes.c_int),
+        ("group_m", ctypes.c_int),
     ]
 
 
