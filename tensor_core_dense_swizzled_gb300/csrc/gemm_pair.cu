@@ -357,6 +357,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * Cfg::TMEM_STRIDE;
+                const uint64_t adesc0 = sdesc_sw128(sA, 16, 1024);
+                const uint64_t bdesc0 = sdesc_sw128(sB, Cfg::B_COLS, 1024);
                 for (int ks = ks0; ks < ks1; ++ks) {
                     if (!wait_bounded(full(stage), phase, wc, timeout_code(ROLE_MMA, stage))) {
                         ok = false;
@@ -364,17 +366,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     tc_fence_after();
                     const int nsub = min(KS, p.num_kb - ks * KS);
+                    // Descriptors: those of stage 0 plus the byte offset / 16 in
+                    // the start-address field (shared-memory offsets stay below
+                    // 256 KB, so the add cannot carry out of the field).  One
+                    // thread issues every MMA; rebuilding each descriptor cost
+                    // it more than the MMA's own issue.
+                    const uint64_t a_st = adesc0 + ((stage * Cfg::A_BYTES) >> 4);
+                    const uint64_t b_st = bdesc0 + ((stage * Cfg::B_BYTES) >> 4);
+                    const uint32_t acc0 = ks > ks0 ? 1u : 0u;
 #pragma unroll
                     for (int s = 0; s < KS; ++s) {
                         if (s >= nsub) break;
-                        const uint32_t a0 = sA + stage * Cfg::A_BYTES + s * Cfg::A_SUB;
-                        const uint32_t b0 = sB + stage * Cfg::B_BYTES + s * Cfg::B_BLOCK;
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
-                            const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
-                            const uint64_t bd = sdesc_sw128(b0 + k * 16 * 128, Cfg::B_COLS, 1024);
-                            umma_f16_pair(d_tmem, ad, bd, p.idesc,
-                                          (ks > ks0 || s > 0 || k > 0) ? 1u : 0u);
+                            const uint64_t ad = a_st + ((s * Cfg::A_SUB + k * 32) >> 4);
+                            const uint64_t bd = b_st + ((s * Cfg::B_BLOCK + k * 16 * 128) >> 4);
+                            umma_f16_pair(d_tmem, ad, bd, p.idesc, (s > 0 || k > 0) ? 1u : acc0);
                         }
                     }
                     umma_commit_pair(empty(stage), 0x3);
