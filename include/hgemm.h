@@ -87,11 +87,13 @@ typedef struct {
                                  tiles stays whole (no stream-K, no K halves) */
     int pair_k_blocks;        /* CTA pairs: 0 automatic (2), or 1 / 2 64-wide K blocks per pipeline
                                  stage (tile_k of the plan info is 64 x this) */
-    int tail_mode;            /* CTA pairs, the last partial wave of tiles: 0 automatic; 1 whole
-                                 tiles; 2 K halves of each tail tile run by two pairs at once
-                                 (needs 2 x tail tiles <= pairs); 3 stream-K (needs tiles >=
-                                 pairs).  Automatic takes 3, else 2, else 1, the first whose
-                                 condition holds; a forced 3 or 2 falls back the same way. */
+    int tail_mode;            /* CTA pairs, the tiles that do not fill a wave: 0 automatic; 1 whole
+                                 tiles; 2 K halves of each such tile, run by two pairs in the
+                                 first wave (needs 2 x tail tiles <= pairs); 3 stream-K over the
+                                 last waves (needs tiles >= pairs); 4 their K steps dealt to all
+                                 pairs in the first wave (needs tail steps >= pairs, at most 4
+                                 pieces per tile).  A forced mode whose condition fails falls
+                                 back to 2, then 3, then 1. */
     int skinny_stream_k;      /* skinny path: 0 automatic (off), 1 off, 2 on: the (tile, K block)
                                  steps are dealt to the SMs in equal contiguous ranges */
     int skinny_prefetch;      /* skinny path: stages of B each CTA asks L2 for before it waits on
@@ -115,9 +117,9 @@ typedef struct {
     int tail_split;       /* CTA pairs: 2 when the last partial wave's tiles run as two K halves */
     int wide_boxes;       /* CTA pairs: 1 when each pipeline stage of A and of B is one TMA copy
                              (4-D views; 256-wide tiles, K and N multiples of 64) */
-    int stream_k;         /* 1 when K steps are dealt in equal contiguous ranges: CTA pairs
-                             (tail_mode 3) or the skinny path (skinny_stream_k); on the skinny
-                             path split_k is then the most pieces a column tile is cut into */
+    int stream_k;         /* K steps dealt in equal contiguous ranges: CTA pairs 1 (tail_mode 3)
+                             or 2 (tail_mode 4), the skinny path 1 (skinny_stream_k; split_k is
+                             then the most pieces a column tile is cut into) */
 } hgemm_plan_info_t;
 
 /* Creates a plan for C_b = A_b . B_b, b < batch.

@@ -140,7 +140,8 @@ struct hgemm_plan_s {
     int tail_split = 1;
     int pair_ks = 2;  // pair path: 64-wide K blocks per pipeline stage
     bool wide = false;  // pair path: A/B maps are the 4-D one-copy-per-stage views
-    bool stream_k = false;  // pair path: stream-K schedule (see plan_create)
+    int stream_k = 0;  // pair path: 1 stream-K of the last waves, 2 first-wave dealing (see plan_create)
+    int max_seg = 0;   // stream_k == 2: most pieces a dealt tile is cut into
     // skinny path
     int nu, nb, split, kb_per;  // padded M, 64-column blocks per unit, K splits
     bool skinny_deal = false;   // stream-K dealing (split = most pieces per tile)
@@ -265,7 +266,14 @@ hgemm_status_t alloc_workspace(hgemm_plan_s *p) {
         if (p->split > 1)
             partials = static_cast<size_t>(p->batch) * p->split * num_n * p->nu * 128 * sizeof(float);
     }
-    if (p->path == HGEMM_PATH_TILED && p->pair && p->stream_k) {
+    if (p->path == HGEMM_PATH_TILED && p->pair && p->stream_k == 2) {
+        // per dealt tile: counters [tile][CTA][warp]; partials
+        // [tile][max_seg][CTA][warp][bn / 32 chunks of 32 x 32 fp32]
+        counters = static_cast<size_t>(p->full_tiles * 2 * 4) * sizeof(int32_t);
+        partials = static_cast<size_t>(p->full_tiles * p->max_seg * 2 * 4 * (p->bn / 32) * 1024) *
+                   sizeof(float);
+    }
+    if (p->path == HGEMM_PATH_TILED && p->pair && p->stream_k == 1) {
         // per pair (the cut at the start of its range): 2 CTAs x 4 epilogue
         // warps, each with one flag and bn / 32 chunks of 32 x 32 fp32
         const int64_t slots = p->grid / 2;
@@ -376,8 +384,8 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         return fail(HGEMM_ERR_INVALID_ARG, "cta_pair must be 0, 1 or 2");
     if (opt.pair_k_blocks < 0 || opt.pair_k_blocks > 2)
         return fail(HGEMM_ERR_INVALID_ARG, "pair_k_blocks must be 0, 1 or 2");
-    if (opt.tail_mode < 0 || opt.tail_mode > 3)
-        return fail(HGEMM_ERR_INVALID_ARG, "tail_mode must be 0, 1, 2 or 3");
+    if (opt.tail_mode < 0 || opt.tail_mode > 4)
+        return fail(HGEMM_ERR_INVALID_ARG, "tail_mode must be 0, 1, 2, 3 or 4");
     if (opt.skinny_stream_k < 0 || opt.skinny_stream_k > 2)
         return fail(HGEMM_ERR_INVALID_ARG, "skinny_stream_k must be 0, 1 or 2");
     if (opt.group_m < 0 || opt.group_m > 4096)
@@ -483,10 +491,22 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
                 const int64_t num_steps = ceil_div(ceil_div(K, 64), p->pair_ks);
                 const bool can_sk = T > 0 && ptiles >= max_pairs;
                 const bool can_halves = T > 0 && 2 * T <= max_pairs && num_steps >= 2;
+                // first-wave dealing: the T * num_steps steps cover every pair
+                // and cut no tile into more than MAX_SEG (4) pieces
+                const int64_t dealt = T * num_steps;
+                const int64_t dq = dealt / max_pairs;
+                const int64_t segs = dq > 0 ? (num_steps - 1) / dq + 2 : 0;
+                const bool can_deal = T > 0 && dq >= 1 && segs <= 4;
                 int mode = opt.no_tail_split ? 1 : opt.tail_mode;
                 if (mode == 0) mode = can_halves ? 2 : 3;
-                if (mode == 3 && can_sk) {
-                    p->stream_k = true;
+                if (mode == 4 && !can_deal) mode = can_halves ? 2 : 3;
+                if (mode == 4) {
+                    p->stream_k = 2;
+                    p->full_tiles = T;  // tiles 0 .. T-1 are dealt
+                    p->max_seg = static_cast<int>(segs < max_pairs ? segs : max_pairs);
+                    p->units = max_pairs;  // every pair takes part
+                } else if (mode == 3 && can_sk) {
+                    p->stream_k = 1;
                     // all waves but the last one and a bit run whole tiles
                     p->full_tiles = (ptiles / max_pairs - 1) * max_pairs;
                 } else if (mode >= 2 && can_halves) {
@@ -658,7 +678,8 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.tail_split = p->pair ? p->tail_split : 1;
         tp.units = static_cast<int32_t>(p->pair ? p->units : tp.tiles);
         tp.wide_boxes = p->wide ? 1 : 0;
-        tp.stream_k = p->stream_k ? 1 : 0;
+        tp.stream_k = p->stream_k;
+        tp.max_seg = p->max_seg;
         tp.partials = reinterpret_cast<float *>(p->ws + p->off_partials);
         tp.tail_sync = reinterpret_cast<int32_t *>(p->ws + p->off_counters);
         if (p->pair)
@@ -833,10 +854,9 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     if (plan->path == HGEMM_PATH_ZERO_FILL) r.kernels_per_run = 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
     r.tail_split = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->tail_split : 1;
-    r.stream_k = (plan->path == HGEMM_PATH_TILED && plan->pair && plan->stream_k) ||
-                         (plan->path == HGEMM_PATH_SKINNY && plan->skinny_deal)
-                     ? 1
-                     : 0;
+    r.stream_k = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->stream_k
+                 : plan->path == HGEMM_PATH_SKINNY && plan->skinny_deal ? 1
+                                                                       : 0;
     r.wide_boxes = plan->path == HGEMM_PATH_TILED && plan->pair && plan->bn == 256 &&
                            plan->K % 64 == 0 && plan->N % 64 == 0 && (plan->wide || !plan->maps_ok)
                        ? 1

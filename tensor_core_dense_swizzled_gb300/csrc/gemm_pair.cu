@@ -91,11 +91,17 @@ enum PieceRole : int {
     PIECE_CLOSE = 2,   // stream-K: the first K steps of a tile whose remaining
                        //   steps the next pair ran first; add its partial, store C
     PIECE_SPILL = 3,   // stream-K: the last K steps of a tile; publish the partial
+    PIECE_PART = 4,    // first-wave dealing: piece seg of nseg of a tile; publish the
+                       //   partial, the last piece to arrive sums them all and stores C
 };
 struct Piece {
     int t, ks0, ks1, role;
-    int slot;  // PIECE_HALF0/1: index of the split tile among the split tiles
+    int slot;       // PIECE_HALF0/1: index of the split tile among the split tiles
+    int seg, nseg;  // PIECE_PART
 };
+
+// Most pieces a tile dealt in the first wave may be cut into.
+constexpr int MAX_SEG = 4;
 
 // The sequence of pieces a pair runs; the producer, the MMA issuer and the
 // epilogue of both CTAs walk the same sequence.
@@ -110,6 +116,12 @@ struct Piece {
 // through global memory; a release/acquire hand-over between SMs took about
 // 4.5 us on GB300, which the first wave hides behind the next whole tile
 // (with the halves last it was exposed at the end of the kernel).
+// First-wave dealing (p.stream_k == 2): the K steps of tiles 0 ..
+// full_tiles - 1 (the tiles that do not fill a wave) are dealt to all pairs
+// as contiguous, equal ranges (to one step) and run FIRST; then whole tiles
+// full_tiles + pair, + npairs, ...  Every pair gets the same work.  A dealt
+// tile cut into pieces on consecutive pairs is combined by its last piece
+// to arrive (PIECE_PART: no waiting), while the next whole tiles run.
 // Stream-K mode (p.stream_k == 1): whole tiles below p.full_tiles first,
 // then the K steps of the last S = tiles -
 // full_tiles tiles (pairs <= S < 2 pairs) are dealt to the pairs as
@@ -123,19 +135,52 @@ struct Piece {
 // slower than whole tiles, from L2 misses.)
 struct PairSched {
     int u;
-    int s, s_end;
+    int s, s_end, q, r;
     __device__ __forceinline__ PairSched(const TiledParams &p, int num_ks, int pair, int npairs) {
         u = pair;
-        s = s_end = 0;
+        s = s_end = q = r = 0;
         if (p.stream_k) {
-            const int total = (p.tiles - p.full_tiles) * num_ks;
-            const int q = total / npairs, r = total % npairs;
+            // mode 1: the last tiles - full_tiles tiles; mode 2: tiles
+            // 0 .. full_tiles - 1, dealt before the whole tiles
+            const int total = (p.stream_k == 2 ? p.full_tiles : p.tiles - p.full_tiles) * num_ks;
+            q = total / npairs;
+            r = total % npairs;
             s = pair * q + min(pair, r);
             s_end = s + q + (pair < r ? 1 : 0);
+            if (p.stream_k == 2) u = p.full_tiles + pair;
         }
     }
+    // Pair whose dealt range holds step `step` (ranges of q + 1 steps, then of q).
+    __device__ __forceinline__ int owner(int step) const {
+        const int big = r * (q + 1);
+        return step < big ? step / (q + 1) : r + (step - big) / q;
+    }
     __device__ __forceinline__ bool next(const TiledParams &p, int num_ks, int npairs, Piece &w) {
-        if (p.stream_k && u >= p.full_tiles) {
+        if (p.stream_k == 2) {
+            if (s < s_end) {
+                w.t = s / num_ks;
+                w.ks0 = s - w.t * num_ks;
+                w.ks1 = min(num_ks, w.ks0 + (s_end - s));
+                s += w.ks1 - w.ks0;
+                if (w.ks0 == 0 && w.ks1 == num_ks) {
+                    w.role = PIECE_WHOLE;
+                } else {
+                    w.role = PIECE_PART;
+                    const int first = owner(w.t * num_ks);
+                    w.seg = owner(w.t * num_ks + w.ks0) - first;
+                    w.nseg = owner(w.t * num_ks + num_ks - 1) - first + 1;
+                }
+                return true;
+            }
+            if (u >= p.tiles) return false;
+            w.t = u;
+            w.ks0 = 0;
+            w.ks1 = num_ks;
+            w.role = PIECE_WHOLE;
+            u += npairs;
+            return true;
+        }
+        if (p.stream_k == 1 && u >= p.full_tiles) {
             if (s >= s_end) return false;
             const int r = s / num_ks;
             w.t = p.full_tiles + r;
@@ -429,6 +474,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (w.role == PIECE_WHOLE) {
                 drain_accumulator<OUT, TMA_STORE, PN>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
                                                       release);
+                continue;
+            }
+            if (w.role == PIECE_PART) {
+                // First-wave dealing: every piece publishes its fp32 partial
+                // (layout [tile][seg][CTA][warp][NCH chunks]) and counts itself
+                // on the (tile, CTA, warp) counter with an acquire-release
+                // atomic; the piece that arrives last sums the nseg partials in
+                // segment order and stores C.  Nothing waits for anything.
+                const int cidx = (w.t * 2 + static_cast<int>(rank)) * EPI_WARPS + q;
+                int32_t *ctr = p.tail_sync + cidx;
+                const int64_t seg_stride = static_cast<int64_t>(2 * EPI_WARPS) * NCH * 1024;
+                const float *parts =
+                    p.partials + ((static_cast<int64_t>(w.t) * p.max_seg * 2 + rank) * EPI_WARPS + q) *
+                                     (NCH * 1024);
+                spill_accumulator(tbase, const_cast<float *>(parts) + w.seg * seg_stride, 0, NCH);
+                tc_fence_before();
+                __syncwarp();
+                release();  // TMEM read: the MMA may move on
+                __syncwarp();  // every lane's stores before lane 0's release (cumulative)
+                int last = 0;
+                if (lane == 0) {
+                    int old;
+                    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                                 : "=r"(old)
+                                 : "l"(ctr)
+                                 : "memory");
+                    last = old == w.nseg - 1 ? 1 : 0;
+                }
+                last = __shfl_sync(0xFFFFFFFFu, last, 0);
+                __syncwarp();  // lane 0's acquire before every lane's loads
+                if (last) {
+                    drain_partials<OUT, TMA_STORE, PN, MAX_SEG>(parts, seg_stride, w.nseg, stg, stg_f,
+                                                                sbuf, row0, col0, b, epi);
+                    if (lane == 0) *ctr = 0;  // ready for the next run
+                }
                 continue;
             }
             if (w.role >= PIECE_CLOSE) {

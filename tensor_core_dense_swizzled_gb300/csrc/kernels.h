@@ -42,12 +42,17 @@ struct TiledParams {
     // Pair kernel only: 1 when the A and B maps are the 4-D views that load a
     // whole stage of each operand with one copy (see launch_pair).
     int32_t wide_boxes;
-    // Pair kernel only: 1 = stream-K schedule (tiles >= pairs): tiles below
+    // Pair kernel only: 2 = first-wave dealing (see max_seg); 1 = stream-K
+    // schedule (tiles >= pairs): tiles below
     // full_tiles run whole, the K steps of the rest (pairs <= rest < 2 pairs)
     // are dealt to the pairs in equal contiguous ranges; cut tiles meet
     // through partials / tail_sync slots indexed by pair ([pair][rank][warp]:
     // PN / 32 chunks of 32 x 32 fp32, one flag).
     int32_t stream_k;
+    // Pair kernel, stream_k == 2 (first-wave dealing of tiles 0 .. full_tiles
+    // - 1): partials [tile][max_seg][rank][warp][PN / 32 chunks][32 x 32]
+    // fp32, tail_sync = counters [tile][rank][warp] (zero between runs).
+    int32_t max_seg;
 };
 
 // Skinny kernel: C^T = B^T . A^T, NB x 64 output columns of C per work

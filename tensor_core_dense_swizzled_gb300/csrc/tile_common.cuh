@@ -82,10 +82,16 @@ cudaError_t launch_dependent(Kernel kern, int grid, int threads, int smem, cudaS
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Epilogue staging: each epilogue warp owns EPI_STG_BUFS pieces of
-// EPI_STG_BYTES (32 rows x 128 bytes) of shared memory.
+// Epilogue staging: each epilogue warp owns EPI_STG_BUFS x EPI_STG_BYTES of
+// shared memory, used as pieces of 32 rows x 32 columns: two of 4 KB for fp32
+// output, four of 2 KB for fp16/bf16 (more TMA stores in flight: the drain
+// of a tile waits on stores still reading their pieces).
 constexpr int EPI_STG_BYTES = 4096;
 constexpr int EPI_STG_BUFS = 2;
+template <int OUT>
+struct EpiPiece {
+    static constexpr int BYTES = OUT == OUT_F32 ? 4096 : 2048;
+};
 
 struct EpiArgs {
     const CUtensorMap *tmC;  // TMA-store path
@@ -94,21 +100,76 @@ struct EpiArgs {
     int32_t M, N;
 };
 
+// Converts 32 fp32 columns (chunk c of a warp's 32 rows, lane = row) and
+// stores them into C: TMA_STORE through the warp's swizzled staging pieces
+// (fp32 rows of 128 bytes: chunk j of row r at j ^ (r & 7); fp16/bf16 rows of
+// 64 bytes: chunk j at j ^ ((r >> 1) & 3), the 64-byte-row swizzle of
+// "tensor-cores-cutlass-and-cute" section 三.5) and one TMA store by lane 0
+// -- the C map clips rows >= M and columns >= N (it is only used when
+// N * sizeof(out) is a multiple of 16 bytes); otherwise the 32 x 32 piece is
+// transposed through shared memory (element (r, c) at r*32 + (c ^ r):
+// conflict-free both ways) and lane l writes column l of every row with
+// predicated, coalesced stores.
+template <int OUT, bool TMA_STORE>
+__device__ __forceinline__ void store_chunk(const uint32_t (&v)[32], int c, uint32_t stg,
+                                            float *stg_f, int &sbuf, int row0, int col0, int b,
+                                            const EpiArgs &e) {
+    const int lane = threadIdx.x & 31;
+    if constexpr (TMA_STORE) {
+        constexpr int PIECE = EpiPiece<OUT>::BYTES;
+        constexpr int NPIECE = EPI_STG_BUFS * EPI_STG_BYTES / PIECE;
+        if (lane == 0) bulk_wait_read<NPIECE - 1>();
+        __syncwarp();
+        const uint32_t piece = stg + sbuf * PIECE;
+        if constexpr (OUT == OUT_F32) {
+            const uint32_t row_addr = piece + lane * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1],
+                             v[4 * j + 2], v[4 * j + 3]);
+        } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack2<OUT>(v[2 * i], v[2 * i + 1]);
+            const uint32_t row_addr = piece + lane * 64;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), pk[4 * j], pk[4 * j + 1],
+                             pk[4 * j + 2], pk[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(e.tmC, piece, col0 + c * 32, row0, b);
+            bulk_commit();
+        }
+        sbuf = (sbuf + 1 == NPIECE) ? 0 : sbuf + 1;
+    } else {
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) stg_f[lane * 32 + (j ^ lane)] = __uint_as_float(v[j]);
+        __syncwarp();
+        const int col = col0 + c * 32 + lane;
+        if (col < e.N) {
+            const int64_t base = static_cast<int64_t>(b) * e.strideC;
+#pragma unroll 4
+            for (int r = 0; r < 32; ++r) {
+                const int row = row0 + r;
+                if (row >= e.M) break;
+                store_one<OUT>(e.C, base + static_cast<int64_t>(row) * e.ldc + col,
+                               stg_f[r * 32 + (lane ^ r)]);
+            }
+        }
+    }
+}
+
 // One epilogue warp drains its 32 TMEM lanes (output rows row0..row0+31) x
 // NCOLS fp32 columns of one accumulator, starting at TMEM address `tbase`,
 // into C columns col0.. of batch b.  `release()` runs once the last column
 // is in registers, so the MMA issuer can reuse the accumulator while the
 // stores drain.
 //
-// TMA_STORE: 32-column pieces go through the warp's swizzled staging pieces
-// (fp32 rows of 128 bytes: chunk j of row r at j ^ (r & 7); fp16/bf16 rows of
-// 64 bytes: chunk j at j ^ ((r >> 1) & 3), the 64-byte-row swizzle of
-// "tensor-cores-cutlass-and-cute" section 三.5), one thread TMA-stores each
-// piece; the C map clips rows >= M and columns >= N (it is only used when
-// N * sizeof(out) is a multiple of 16 bytes).
-// Otherwise each 32 x 32 piece is transposed through shared memory (element
-// (r, c) at r*32 + (c ^ r): conflict-free both ways) and lane l writes column
-// l of every row with predicated, coalesced stores.
+// Each 32-column chunk is stored by store_chunk.
 //
 // ADD: `addend` holds another fp32 partial of the same 32 rows in the layout
 // spill_accumulator writes; it is added to the accumulator (own + addend)
@@ -165,50 +226,52 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, 
                 v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a.w);
             }
         }
-        if constexpr (TMA_STORE) {
-            if (lane == 0) bulk_wait_read<EPI_STG_BUFS - 1>();
-            __syncwarp();
-            const uint32_t piece = stg + sbuf * EPI_STG_BYTES;
-            if constexpr (OUT == OUT_F32) {
-                const uint32_t row_addr = piece + lane * 128;
+        store_chunk<OUT, TMA_STORE>(v, c, stg, stg_f, sbuf, row0, col0, b, e);
+    }
+}
+
+// Sums nseg fp32 partials of one warp's 32 rows x NCOLS columns, stored in
+// the spill_accumulator layout at parts + s * seg_stride (s = 0 .. nseg-1),
+// in the order s = 0, 1, ... (so the result does not depend on which piece
+// arrived last), and stores the sum into C like drain_accumulator.  All
+// loads of a chunk are issued before any is used: one L2 round trip per
+// chunk.  nseg <= MAXSEG.
+template <int OUT, bool TMA_STORE, int NCOLS, int MAXSEG>
+__device__ __forceinline__ void drain_partials(const float *parts, int64_t seg_stride, int nseg,
+                                               uint32_t stg, float *stg_f, int &sbuf, int row0,
+                                               int col0, int b, const EpiArgs &e) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int c = 0; c < NCOLS / 32; ++c) {
+        float4 t[MAXSEG][8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1],
-                                 v[4 * j + 2], v[4 * j + 3]);
-            } else {
-                uint32_t pk[16];
+        for (int s = 0; s < MAXSEG; ++s) {
+            if (s < nseg) {
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(parts + s * seg_stride + c * 1024) + lane;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = pack2<OUT>(v[2 * i], v[2 * i + 1]);
-                const uint32_t row_addr = piece + lane * 64;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), pk[4 * j], pk[4 * j + 1],
-                                 pk[4 * j + 2], pk[4 * j + 3]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_3d(e.tmC, piece, col0 + c * 32, row0, b);
-                bulk_commit();
-            }
-            sbuf ^= 1;
-        } else {
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) stg_f[lane * 32 + (j ^ lane)] = __uint_as_float(v[j]);
-            __syncwarp();
-            const int col = col0 + c * 32 + lane;
-            if (col < e.N) {
-                const int64_t base = static_cast<int64_t>(b) * e.strideC;
-#pragma unroll 4
-                for (int r = 0; r < 32; ++r) {
-                    const int row = row0 + r;
-                    if (row >= e.M) break;
-                    store_one<OUT>(e.C, base + static_cast<int64_t>(row) * e.ldc + col,
-                                   stg_f[r * 32 + (lane ^ r)]);
-                }
+                for (int j = 0; j < 8; ++j) t[s][j] = __ldcg(src + j * 32);
             }
         }
+        uint32_t v[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float4 a = t[0][j];
+#pragma unroll
+            for (int s = 1; s < MAXSEG; ++s) {
+                if (s < nseg) {
+                    a.x += t[s][j].x;
+                    a.y += t[s][j].y;
+                    a.z += t[s][j].z;
+                    a.w += t[s][j].w;
+                }
+            }
+            v[4 * j] = __float_as_uint(a.x);
+            v[4 * j + 1] = __float_as_uint(a.y);
+            v[4 * j + 2] = __float_as_uint(a.z);
+            v[4 * j + 3] = __float_as_uint(a.w);
+        }
+        store_chunk<OUT, TMA_STORE>(v, c, stg, stg_f, sbuf, row0, col0, b, e);
     }
 }
 

@@ -225,6 +225,26 @@ def test_cta_pair_stream_k(dev, shape, dout, ks):
     check(got, Cref, Den, dout)
 
 
+@pytest.mark.parametrize("shape", [(1536, 2560, 512, 1), (1536, 2048, 320, 1), (2048, 2048, 256, 1),
+                                   (1500, 2000, 700, 1), (768, 2048, 512, 2)])
+@pytest.mark.parametrize("dout", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("ks", [1, 2])
+def test_cta_pair_first_wave_dealing(dev, shape, dout, ks):
+    """tail_mode 4: the K steps of the tiles that do not fill a wave (here
+    all 48 to 64 tiles) are dealt to all pairs first; a tile cut into up to
+    four pieces on consecutive pairs is summed, in piece order, by the piece
+    that arrives last.  K = 320 and 700 leave a last stage of one K block;
+    N = 2000 is not a multiple of 64 (box-by-box loads); the batched case
+    deals across batch entries.  Three runs must agree bit for bit (the
+    counters reset, the sum order is fixed)."""
+    M, N, K, batch = shape
+    got, Cref, Den, info = run_case(dev, M, N, K, "bf16", dout, batch=batch, seed=M + N + K + 13,
+                                    options=H.Options(cta_pair=1, pair_k_blocks=ks, tail_mode=4),
+                                    runs=3)
+    assert info["tile_m"] == 256 and info["stream_k"] == 2
+    check(got, Cref, Den, dout)
+
+
 @pytest.mark.parametrize("shape", [(512, 1024, 512), (300, 520, 200), (1024, 768, 96), (640, 1000, 333),
                                    (512, 768, 130), (256, 512, 192), (2560, 2048, 256), (4096, 4096, 128)])
 @pytest.mark.parametrize("dout", ["f32", "bf16", "f16"])
