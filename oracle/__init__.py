@@ -185,3 +185,73 @@ def _check_extent(X: np.ndarray, rows: int, cols: int, ld: int, batch: int, stri
     last = (batch - 1) * stride + (rows - 1) * ld + cols - 1
     if last >= X.size:
         raise ValueError("operand buffer too small for its shape")
+
+
+# ---------------------------------------------------------------- fused epilogue
+
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+
+# Largest slope of GELU(x) = x * Phi(x): its derivative Phi(x) + x * phi(x)
+# has derivative phi(x) * (2 - x^2), so it peaks at x = sqrt(2) at
+# Phi(sqrt 2) + sqrt(2) * phi(sqrt 2) = 1.1289...  An error e in GELU's
+# argument moves its value by at most this times e.
+GELU_MAX_SLOPE = (0.5 * (1.0 + __import__("math").erf(1.0))
+                  + np.sqrt(2.0) * np.exp(-1.0) / np.sqrt(2.0 * np.pi))
+
+
+def _phi_cdf(x: np.ndarray) -> np.ndarray:
+    """Standard normal CDF, 0.5 * (1 + erf(x / sqrt 2)), in fp64."""
+    try:
+        from scipy.special import erf  # library routine for erf
+        return 0.5 * (1.0 + erf(x / np.sqrt(2.0)))
+    except ImportError:  # pragma: no cover - scipy is on both machines
+        import math
+        return 0.5 * (1.0 + np.vectorize(math.erf)(x / np.sqrt(2.0)))
+
+
+def activation(x: np.ndarray, act: int) -> np.ndarray:
+    """ReLU max(x, 0) or GELU x * Phi(x) (the erf form of the Gaussian error
+    linear unit: cuBLASLt's BIAS / RELU / GELU epilogues that
+    "tensor-cores-cutlass-and-cute" lists in its comparison with cuBLAS)."""
+    x = np.asarray(x, dtype=np.float64)
+    if act == ACT_NONE:
+        return x
+    if act == ACT_RELU:
+        return np.maximum(x, 0.0)
+    if act == ACT_GELU:
+        return x * _phi_cdf(x)
+    raise ValueError("unknown activation")
+
+
+def epilogue(Cref: np.ndarray, Den: np.ndarray, *, alpha: float = 1.0, beta: float = 0.0,
+             C_prev: np.ndarray | None = None, bias: np.ndarray | None = None,
+             row_scale: np.ndarray | None = None, col_scale: np.ndarray | None = None,
+             act: int = ACT_NONE):
+    """The fused epilogue in fp64 on the oracle's product (shape (batch,) M x N):
+
+        D[i][j] = act(alpha * rs[i] * cs[j] * Cref[i][j] + beta * C_prev[i][j] + bias[j])
+
+    (rs, cs, bias default to 1, 1, 0; the vectors are shared by every batch
+    entry).  Returns (D, DenD), DenD the acceptance denominator: the bound on
+    |D - D_gpu| that the product's own bound Den carries through the affine
+    part, plus the magnitudes of the added terms (each rounded once in fp32),
+    times GELU's largest slope when GELU is applied."""
+    Cref = np.asarray(Cref, dtype=np.float64)
+    Den = np.asarray(Den, dtype=np.float64)
+    M, N = Cref.shape[-2], Cref.shape[-1]
+    rs = np.ones(M) if row_scale is None else np.asarray(row_scale, dtype=np.float64)
+    cs = np.ones(N) if col_scale is None else np.asarray(col_scale, dtype=np.float64)
+    scale = alpha * rs[:, None] * cs[None, :]
+    t = scale * Cref
+    den = np.abs(scale) * Den
+    if beta != 0.0:
+        Cp = np.asarray(C_prev, dtype=np.float64)
+        t = t + beta * Cp
+        den = den + np.abs(beta * Cp)
+    if bias is not None:
+        bv = np.asarray(bias, dtype=np.float64)[None, :]
+        t = t + bv
+        den = den + np.abs(bv)
+    if act == ACT_GELU:
+        den = den * GELU_MAX_SLOPE
+    return activation(t, act), den
