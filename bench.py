@@ -60,6 +60,10 @@ def parse():
     ap.add_argument("--workload", default="square4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--epilogue", choices=["none", "bias_gelu", "bias_gelu_tanh", "beta_bias_relu"],
+                    default="none",
+                    help="fused epilogue on every step (hgemm_run_ex): bias + GELU (erf or tanh "
+                         "form), or beta = 1 (reads C) + bias + ReLU")
     ap.add_argument("--probe-seconds", type=float, default=1.0,
                     help="untimed load after the timed region so the clock sampler sees the GPU busy")
     return ap.parse_args()
@@ -328,9 +332,25 @@ def run_ours(args, w, world, rank, local, pg):
     info = H.hgemm_plan_get_info(plans[0])
     stream = torch.cuda.current_stream(dev)
 
+    epi = None
+    if args.epilogue != "none":
+        import types
+        gen = torch.Generator().manual_seed(w.seed + 99)
+        bias_dev = torch.randn(w.N, generator=gen).to(dev)
+        epi = types.SimpleNamespace(
+            alpha=1.0, beta=1.0 if args.epilogue == "beta_bias_relu" else 0.0, bias=bias_dev,
+            row_scale=None, col_scale=None,
+            activation={"bias_gelu": H.HGEMM_ACT_GELU, "bias_gelu_tanh": H.HGEMM_ACT_GELU_TANH,
+                        "beta_bias_relu": H.HGEMM_ACT_RELU}[args.epilogue])
+        for a_, b_, c_ in sets:
+            c_.zero_()  # beta = 1 reads C: start from defined values
+
     def step(i):
         a, b, c = sets[i % nsets]
-        H.hgemm_run(plans[i % nsets], a, b, c, stream)
+        if epi is None:
+            H.hgemm_run(plans[i % nsets], a, b, c, stream)
+        else:
+            H.hgemm_run_ex(plans[i % nsets], a, b, c, epi, stream)
 
     for i in range(args.warmup):
         step(i)
@@ -431,7 +451,7 @@ def run_ours(args, w, world, rank, local, pg):
             "l2": f"{nsets} rotating input/output sets ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)",
             "path": {2: "tiled", 3: "skinny", 1: "zero_fill", 0: "empty"}[info["path"]],
             "tile": [info["tile_m"], info["tile_n"], info["tile_k"]], "stages": info["stages"],
-            "split_k": info["split_k"], "grid": info["grid"]}),
+            "split_k": info["split_k"], "grid": info["grid"], "epilogue": args.epilogue}),
         "pct_nominal_tensor_peak": 100.0 * value / world / NOMINAL_TC_TFLOPS,
         "pct_nominal_hbm": 100.0 * (min_bytes * args.steps / (region_ms * 1e-3) / 1e9) / NOMINAL_HBM_GBS,
         "roofline": roof,

@@ -152,6 +152,39 @@ hgemm_status_t hgemm_plan_create_ex(hgemm_plan_t *plan, int64_t M, int64_t N, in
  * INVALID_ARG for a null pointer when the plan has work to do. */
 hgemm_status_t hgemm_run(hgemm_plan_t plan, const void *A, const void *B, void *C, void *stream);
 
+/* Fused epilogue: the kernels write, for every element of C,
+ *
+ *     D[i][j] = act(alpha * rs[i] * cs[j] * (A.B)[i][j] + beta * C[i][j] + bias[j])
+ *
+ * (C on the right is the value C held before the call), rounded once to the
+ * output type.  The terms follow the bias / ReLU / GELU epilogues the pages
+ * list among cuBLASLt's features ("tensor-cores-cutlass-and-cute", its
+ * comparison with cuBLAS); scale, add, then activate.  All arithmetic is
+ * fp32.  Vectors are device fp32 arrays shared by every batch entry; NULL
+ * means rs = 1, cs = 1, bias = 0.  beta == 0 leaves C unread (it may hold
+ * anything, NaN included). */
+typedef enum {
+    HGEMM_ACT_NONE = 0,
+    HGEMM_ACT_RELU = 1, /* max(x, 0) */
+    HGEMM_ACT_GELU = 2, /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)) */
+    HGEMM_ACT_GELU_TANH = 3 /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), the tanh form
+                               (tanh from the hardware approximation) */
+} hgemm_activation_t;
+
+typedef struct {
+    float alpha;            /* scales the product */
+    float beta;             /* scales C's previous value; 0: C is not read */
+    const float *bias;      /* N values added per column, or NULL */
+    const float *row_scale; /* M values scaling row i of the product, or NULL */
+    const float *col_scale; /* N values scaling column j of the product, or NULL */
+    int activation;         /* hgemm_activation_t, applied last */
+} hgemm_epilogue_t;
+
+/* hgemm_run with a fused epilogue (NULL: plain product, as hgemm_run).
+ * INVALID_ARG for an unknown activation or non-finite alpha / beta. */
+hgemm_status_t hgemm_run_ex(hgemm_plan_t plan, const void *A, const void *B, void *C, void *stream,
+                            const hgemm_epilogue_t *epilogue);
+
 /* End-to-end variant for operands in HOST memory (pinned memory is fastest):
  * copies A and B to plan-owned device buffers on `stream`, runs the product,
  * copies the M x N block(s) of C back into the host buffer (elements outside

@@ -189,7 +189,7 @@ def _check_extent(X: np.ndarray, rows: int, cols: int, ld: int, batch: int, stri
 
 # ---------------------------------------------------------------- fused epilogue
 
-ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_GELU_TANH = 0, 1, 2, 3
 
 # Largest slope of GELU(x) = x * Phi(x): its derivative Phi(x) + x * phi(x)
 # has derivative phi(x) * (2 - x^2), so it peaks at x = sqrt(2) at
@@ -210,9 +210,10 @@ def _phi_cdf(x: np.ndarray) -> np.ndarray:
 
 
 def activation(x: np.ndarray, act: int) -> np.ndarray:
-    """ReLU max(x, 0) or GELU x * Phi(x) (the erf form of the Gaussian error
+    """ReLU max(x, 0), GELU x * Phi(x) (the erf form of the Gaussian error
     linear unit: cuBLASLt's BIAS / RELU / GELU epilogues that
-    "tensor-cores-cutlass-and-cute" lists in its comparison with cuBLAS)."""
+    "tensor-cores-cutlass-and-cute" lists in its comparison with cuBLAS), or
+    its tanh form."""
     x = np.asarray(x, dtype=np.float64)
     if act == ACT_NONE:
         return x
@@ -220,6 +221,9 @@ def activation(x: np.ndarray, act: int) -> np.ndarray:
         return np.maximum(x, 0.0)
     if act == ACT_GELU:
         return x * _phi_cdf(x)
+    if act == ACT_GELU_TANH:
+        # the tanh form of GELU: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+        return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.044715 * x ** 3)))
     raise ValueError("unknown activation")
 
 
@@ -252,6 +256,6 @@ def epilogue(Cref: np.ndarray, Den: np.ndarray, *, alpha: float = 1.0, beta: flo
         bv = np.asarray(bias, dtype=np.float64)[None, :]
         t = t + bv
         den = den + np.abs(bv)
-    if act == ACT_GELU:
+    if act in (ACT_GELU, ACT_GELU_TANH):
         den = den * GELU_MAX_SLOPE
     return activation(t, act), den

@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -612,7 +613,8 @@ hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *
     return HGEMM_OK;
 }
 
-hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, cudaStream_t s) {
+hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, cudaStream_t s,
+                        const hg::EpiParams &ep = hg::EpiParams{1.f, 0.f, nullptr, nullptr, nullptr, 0, 0}) {
     if (p->path == HGEMM_PATH_EMPTY) return HGEMM_OK;
     if (!C) return fail(HGEMM_ERR_INVALID_ARG, "C is NULL");
     const int ob = out_bytes(p->dout);
@@ -623,6 +625,11 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         return fail(HGEMM_ERR_INVALID_ARG, "plan was created on device %d but device %d is current", p->device, cur);
     cudaError_t e;
     if (p->path == HGEMM_PATH_ZERO_FILL) {
+        if (ep.on) {
+            e = hg::launch_epilogue_fill(C, p->ldc, p->sC, p->M, p->N, p->batch, out_type(p->dout),
+                                         ep, p->num_sms, s);
+            return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "epilogue launch");
+        }
         e = hg::launch_zero_fill(C, p->ldc, p->sC, p->M, p->N, p->batch, ob, p->num_sms, s);
         return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "zero-fill launch");
     }
@@ -670,6 +677,7 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.group_m = p->opt.group_m ? p->opt.group_m : 16;
         tp.idesc = hg::idesc_f16(bf, 0, 1, p->pair ? 256 : 128, static_cast<uint32_t>(p->bn));
         tp.C = C;
+        tp.ep = ep;
         tp.ldc = p->ldc;
         tp.strideC = p->sC;
         tp.err = err;
@@ -708,6 +716,7 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     sp.prefetch = p->opt.skinny_prefetch > 0 ? p->opt.skinny_prefetch : 0;
     sp.idesc = hg::idesc_f16(bf, 1, 0, 128, static_cast<uint32_t>(p->nu));
     sp.C = C;
+    sp.ep = ep;
     sp.ldc = p->ldc;
     sp.strideC = p->sC;
     sp.partials = reinterpret_cast<float *>(p->ws + p->off_partials);
@@ -749,6 +758,26 @@ hgemm_status_t hgemm_plan_create_ex(hgemm_plan_t *plan, int64_t M, int64_t N, in
 hgemm_status_t hgemm_run(hgemm_plan_t plan, const void *A, const void *B, void *C, void *stream) {
     if (!plan) return fail(HGEMM_ERR_INVALID_ARG, "plan is NULL");
     return plan_run(plan, A, B, C, static_cast<cudaStream_t>(stream));
+}
+
+hgemm_status_t hgemm_run_ex(hgemm_plan_t plan, const void *A, const void *B, void *C, void *stream,
+                            const hgemm_epilogue_t *epilogue) {
+    if (!plan) return fail(HGEMM_ERR_INVALID_ARG, "plan is NULL");
+    hg::EpiParams ep{1.f, 0.f, nullptr, nullptr, nullptr, 0, 0};
+    if (epilogue) {
+        if (epilogue->activation < HGEMM_ACT_NONE || epilogue->activation > HGEMM_ACT_GELU_TANH)
+            return fail(HGEMM_ERR_INVALID_ARG, "unknown activation %d", epilogue->activation);
+        if (!std::isfinite(epilogue->alpha) || !std::isfinite(epilogue->beta))
+            return fail(HGEMM_ERR_INVALID_ARG, "alpha and beta must be finite");
+        ep.alpha = epilogue->alpha;
+        ep.beta = epilogue->beta;
+        ep.bias = epilogue->bias;
+        ep.row_scale = epilogue->row_scale;
+        ep.col_scale = epilogue->col_scale;
+        ep.act = epilogue->activation;
+        ep.on = 1;
+    }
+    return plan_run(plan, A, B, C, static_cast<cudaStream_t>(stream), ep);
 }
 
 hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void *B_host, void *C_host,

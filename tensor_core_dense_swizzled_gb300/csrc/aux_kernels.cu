@@ -105,6 +105,25 @@ __global__ void zero_fill_kernel(char *C, int64_t ldc, int64_t strideC, int64_t 
     }
 }
 
+// K = 0 with a fused epilogue: the product is an empty sum, so
+// D = act(beta * C_prev + bias) (scales multiply zero).
+template <int OUT>
+__global__ void epilogue_fill_kernel(void *C, int64_t ldc, int64_t strideC, int64_t rows,
+                                     int64_t cols, int64_t batch, EpiParams ep) {
+    const int64_t total = batch * rows * cols;
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t j = idx % cols;
+        const int64_t rb = idx / cols;
+        const int64_t i = rb % rows;
+        const int64_t b = rb / rows;
+        const int64_t e = b * strideC + i * ldc + j;
+        const float bias = ep.bias ? __ldg(ep.bias + j) : 0.f;
+        const float prev = ep.beta != 0.f ? load_one<OUT>(C, e) : 0.f;
+        store_one<OUT>(C, e, epi_value(ep, 0.f, 1.f, 1.f, bias, prev));
+    }
+}
+
 __global__ void watchdog_selftest_kernel(int32_t *err, uint64_t timeout_ns) {
     __shared__ __align__(8) uint64_t bar;
     __shared__ int32_t abort_flag;
@@ -155,6 +174,21 @@ cudaError_t launch_zero_fill(void *C, int64_t ldc, int64_t strideC, int64_t rows
     if (total == 0) return cudaSuccess;
     zero_fill_kernel<<<grid_for(total, 256, num_sms), 256, 0, stream>>>(
         static_cast<char *>(C), ldc, strideC, rows, cols, batch, elem_bytes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_epilogue_fill(void *C, int64_t ldc, int64_t strideC, int64_t rows,
+                                 int64_t cols, int64_t batch, int out, const EpiParams &ep,
+                                 int num_sms, cudaStream_t stream) {
+    const int64_t total = batch * rows * cols;
+    if (total == 0) return cudaSuccess;
+    const int grid = grid_for(total, 256, num_sms);
+    switch (out) {
+        case OUT_F16: epilogue_fill_kernel<OUT_F16><<<grid, 256, 0, stream>>>(C, ldc, strideC, rows, cols, batch, ep); break;
+        case OUT_BF16: epilogue_fill_kernel<OUT_BF16><<<grid, 256, 0, stream>>>(C, ldc, strideC, rows, cols, batch, ep); break;
+        case OUT_F32: epilogue_fill_kernel<OUT_F32><<<grid, 256, 0, stream>>>(C, ldc, strideC, rows, cols, batch, ep); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

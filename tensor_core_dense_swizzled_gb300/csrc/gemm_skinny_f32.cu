@@ -1,0 +1,11 @@
+// gemm_skinny_f32.cu -- the skinny-path kernels with f32 output.
+#include "gemm_skinny.cuh"
+
+namespace hg {
+
+cudaError_t launch_skinny_f32(int nu, int nb, const CUtensorMap &tmX, const CUtensorMap &tmW,
+                              const SkinnyParams &p, int grid, cudaStream_t s) {
+    return launch_skinny_typed<OUT_F32>(nu, nb, tmX, tmW, p, grid, s);
+}
+
+}  // namespace hg

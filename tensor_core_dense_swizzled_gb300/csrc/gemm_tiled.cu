@@ -85,7 +85,7 @@ __device__ __forceinline__ void tile_coords(const TiledParams &p, int t, int &b,
     grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);
 }
 
-template <int BN, int OUT, bool TMA_STORE>
+template <int BN, int OUT, bool TMA_STORE, bool EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     hgemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int ew = warp - 2;  // staging slot
         const uint32_t stg = sC + ew * STG_BUFS * STG_BYTES;
         float *stg_f = reinterpret_cast<float *>(smem + Cfg::SMEM_C + ew * STG_BUFS * STG_BYTES);
-        const EpiArgs epi{&tmC, p.C, p.ldc, p.strideC, p.M, p.N};
+        const EpiArgs epi{&tmC, p.C, p.ldc, p.strideC, p.M, p.N, p.ep};
         int sbuf = 0;
         int local = 0;
         for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::TMEM_STRIDE;
             const int row0 = mt * BM + q * 32;
             const int col0 = nt * BN;
-            drain_accumulator<OUT, TMA_STORE, BN>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
+            drain_accumulator<OUT, TMA_STORE, BN, false, EPI>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
                                                   [&] {
                                                       if (lane == 0) mbar_arrive(tempty(buf));
                                                   });
@@ -264,10 +264,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int BN, int OUT, bool TS>
+template <int BN, int OUT, bool TS, bool EPI>
 cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const TiledParams &p, int grid, cudaStream_t stream) {
-    auto kern = hgemm_tiled_kernel<BN, OUT, TS>;
+    auto kern = hgemm_tiled_kernel<BN, OUT, TS, EPI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TiledCfg<BN>::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
@@ -278,8 +278,12 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
 template <int BN, int OUT>
 cudaError_t launch_ts(bool ts, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap &tmC, const TiledParams &p, int grid, cudaStream_t s) {
-    return ts ? launch_impl<BN, OUT, true>(tmA, tmB, tmC, p, grid, s)
-              : launch_impl<BN, OUT, false>(tmA, tmB, tmC, p, grid, s);
+    // p.ep.on: the fused-epilogue variant
+    if (p.ep.on)
+        return ts ? launch_impl<BN, OUT, true, true>(tmA, tmB, tmC, p, grid, s)
+                  : launch_impl<BN, OUT, false, true>(tmA, tmB, tmC, p, grid, s);
+    return ts ? launch_impl<BN, OUT, true, false>(tmA, tmB, tmC, p, grid, s)
+              : launch_impl<BN, OUT, false, false>(tmA, tmB, tmC, p, grid, s);
 }
 
 template <int BN>

@@ -21,6 +21,16 @@ constexpr uint32_t idesc_f16(uint32_t ab_bf16, uint32_t a_mn, uint32_t b_mn,
            ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// Fused epilogue of the final values of C (see hgemm_epilogue_t):
+// D = act(alpha * rs[i] * cs[j] * acc + beta * C_prev + bias[j]).  `on` = 0:
+// D = acc (nothing else is read).
+struct EpiParams {
+    float alpha, beta;
+    const float *bias, *row_scale, *col_scale;
+    int32_t act;  // 0 none, 1 ReLU, 2 GELU
+    int32_t on;
+};
+
 // Persistent tiled kernel: 128 x BN output tiles, BK = 64, TMEM accumulators.
 struct TiledParams {
     int32_t M, N, K, batch;
@@ -53,6 +63,7 @@ struct TiledParams {
     // - 1): partials [tile][max_seg][rank][warp][PN / 32 chunks][32 x 32]
     // fp32, tail_sync = counters [tile][rank][warp] (zero between runs).
     int32_t max_seg;
+    EpiParams ep;
 };
 
 // Skinny kernel: C^T = B^T . A^T, NB x 64 output columns of C per work
@@ -80,6 +91,7 @@ struct SkinnyParams {
     int32_t deal;
     // Stages of B each CTA asks L2 for before waiting on the previous kernel.
     int32_t prefetch;
+    EpiParams ep;
 };
 
 // Shared memory the tiled kernel needs for a given BN (bytes, incl. alignment slack).
@@ -131,6 +143,12 @@ cudaError_t launch_repack16(const Repack16Job *jobs, int njobs, int num_sms, cud
 // Writes zeros into a batch of rows x cols blocks of `elem_bytes`-byte elements.
 cudaError_t launch_zero_fill(void *C, int64_t ldc, int64_t strideC, int64_t rows, int64_t cols,
                              int64_t batch, int elem_bytes, int num_sms, cudaStream_t stream);
+
+// K = 0 with a fused epilogue: D = act(beta * C_prev + bias) over the
+// batch of rows x cols blocks of C.  `out` is an OutType.
+cudaError_t launch_epilogue_fill(void *C, int64_t ldc, int64_t strideC, int64_t rows,
+                                 int64_t cols, int64_t batch, int out, const EpiParams &ep,
+                                 int num_sms, cudaStream_t stream);
 
 // One-warp kernel waiting on an mbarrier nothing signals (watchdog self-test).
 cudaError_t launch_watchdog_selftest(int32_t *err, uint64_t timeout_ns, cudaStream_t stream);

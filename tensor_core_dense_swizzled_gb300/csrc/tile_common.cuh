@@ -95,10 +95,127 @@ struct EpiPiece {
 
 struct EpiArgs {
     const CUtensorMap *tmC;  // TMA-store path
-    void *C;                 // predicated-store path
+    void *C;                 // predicated-store path; C's previous values (beta != 0)
     int64_t ldc, strideC;
     int32_t M, N;
+    EpiParams ep;
 };
+
+// tanh via the hardware approximation (MUFU, relative error about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Activation of the fused epilogue: 1 ReLU; 2 GELU in the erf form
+// x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)); 3 GELU in the tanh form
+// 0.5 x (1 + tanh(sqrt(2 / pi) (x + 0.044715 x^3))).
+__device__ __forceinline__ float epi_act(float x, int act) {
+    if (act == 1) return fmaxf(x, 0.f);
+    if (act == 2) return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+    if (act == 3) {
+        const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+        return 0.5f * x * (1.f + tanh_approx(u));
+    }
+    return x;
+}
+
+// D = act(alpha * rs * cs * acc + beta * c_prev + bias), fp32.
+__device__ __forceinline__ float epi_value(const EpiParams &ep, float acc, float rs, float cs,
+                                           float bias, float c_prev) {
+    float t = ep.alpha * rs * cs * acc;
+    if (ep.beta != 0.f) t = fmaf(ep.beta, c_prev, t);
+    return epi_act(t + bias, ep.act);
+}
+
+template <int OUT>
+__device__ __forceinline__ float load_one(const void *C, int64_t idx) {
+    if constexpr (OUT == OUT_F32) {
+        return static_cast<const float *>(C)[idx];
+    } else if constexpr (OUT == OUT_BF16) {
+        return __bfloat162float(static_cast<const __nv_bfloat16 *>(C)[idx]);
+    } else {
+        return __half2float(static_cast<const __half *>(C)[idx]);
+    }
+}
+
+// Unpacks two 16-bit values of the output type to floats.
+template <int OUT>
+__device__ __forceinline__ void unpack2(uint32_t w, float &lo, float &hi) {
+    if constexpr (OUT == OUT_BF16) {
+        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162 *>(&w);
+        lo = __low2float(h);
+        hi = __high2float(h);
+    } else {
+        __half2 h = *reinterpret_cast<__half2 *>(&w);
+        lo = __low2float(h);
+        hi = __high2float(h);
+    }
+}
+
+// Applies the fused epilogue to one lane's 32 values of row `row`, columns
+// col .. col+31 (lane = row; the TMA-store path: rows of C are 16-byte
+// multiples and so is N * sizeof(out), so C's previous values are read as
+// 16-byte vectors that never cross column N).  The column vectors are read
+// once per chunk, element l by lane l, and handed to every lane by shuffles.
+template <int OUT>
+__device__ __forceinline__ void epi_row(uint32_t (&v)[32], int row, int col, int b,
+                                        const EpiArgs &e) {
+    const EpiParams &ep = e.ep;
+    const int lane = threadIdx.x & 31;
+    const bool row_in = row < e.M;
+    const float rs = (ep.row_scale && row_in) ? __ldg(ep.row_scale + row) : 1.f;
+    const bool lin = col + lane < e.N;
+    const float cs_l = (ep.col_scale && lin) ? __ldg(ep.col_scale + col + lane) : 1.f;
+    const float bias_l = (ep.bias && lin) ? __ldg(ep.bias + col + lane) : 0.f;
+    const float arow = ep.alpha * rs;
+    if (ep.beta != 0.f) {
+        // C's previous values: every load of the chunk issued before any is
+        // used (one memory round trip per chunk)
+        const int64_t off = static_cast<int64_t>(b) * e.strideC + static_cast<int64_t>(row) * e.ldc + col;
+        uint4 raw[OUT == OUT_F32 ? 8 : 4];
+        constexpr int NV = OUT == OUT_F32 ? 8 : 4;  // 16-byte vectors per 32 columns
+        constexpr int EPV = 32 / NV;                // elements per vector
+#pragma unroll
+        for (int q = 0; q < NV; ++q) {
+            raw[q] = make_uint4(0u, 0u, 0u, 0u);
+            if (row_in && col + EPV * q < e.N)
+                raw[q] = *(reinterpret_cast<const uint4 *>(static_cast<const char *>(e.C) +
+                                                           off * (OUT == OUT_F32 ? 4 : 2)) + q);
+        }
+#pragma unroll
+        for (int q = 0; q < NV; ++q) {
+            float prev[EPV];
+            if constexpr (OUT == OUT_F32) {
+                prev[0] = __uint_as_float(raw[q].x);
+                prev[1] = __uint_as_float(raw[q].y);
+                prev[2] = __uint_as_float(raw[q].z);
+                prev[3] = __uint_as_float(raw[q].w);
+            } else {
+                unpack2<OUT>(raw[q].x, prev[0], prev[1]);
+                unpack2<OUT>(raw[q].y, prev[2], prev[3]);
+                unpack2<OUT>(raw[q].z, prev[4], prev[5]);
+                unpack2<OUT>(raw[q].w, prev[6], prev[7]);
+            }
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) {
+                const int jj = EPV * q + j;
+                const float cs = __shfl_sync(0xFFFFFFFFu, cs_l, jj);
+                const float bias = __shfl_sync(0xFFFFFFFFu, bias_l, jj);
+                const float t = fmaf(ep.beta, prev[j], arow * cs * __uint_as_float(v[jj]));
+                v[jj] = __float_as_uint(epi_act(t + bias, ep.act));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const float cs = __shfl_sync(0xFFFFFFFFu, cs_l, jj);
+            const float bias = __shfl_sync(0xFFFFFFFFu, bias_l, jj);
+            v[jj] = __float_as_uint(epi_act(arow * cs * __uint_as_float(v[jj]) + bias, ep.act));
+        }
+    }
+}
 
 // Converts 32 fp32 columns (chunk c of a warp's 32 rows, lane = row) and
 // stores them into C: TMA_STORE through the warp's swizzled staging pieces
@@ -110,12 +227,15 @@ struct EpiArgs {
 // transposed through shared memory (element (r, c) at r*32 + (c ^ r):
 // conflict-free both ways) and lane l writes column l of every row with
 // predicated, coalesced stores.
-template <int OUT, bool TMA_STORE>
-__device__ __forceinline__ void store_chunk(const uint32_t (&v)[32], int c, uint32_t stg,
+// EPI: the fused epilogue (e.ep) is applied first; a separate kernel variant
+// so that plain products carry none of its code or registers.
+template <int OUT, bool TMA_STORE, bool EPI>
+__device__ __forceinline__ void store_chunk(uint32_t (&v)[32], int c, uint32_t stg,
                                             float *stg_f, int &sbuf, int row0, int col0, int b,
                                             const EpiArgs &e) {
     const int lane = threadIdx.x & 31;
     if constexpr (TMA_STORE) {
+        if constexpr (EPI) epi_row<OUT>(v, row0 + lane, col0 + c * 32, b, e);
         constexpr int PIECE = EpiPiece<OUT>::BYTES;
         constexpr int NPIECE = EPI_STG_BUFS * EPI_STG_BYTES / PIECE;
         if (lane == 0) bulk_wait_read<NPIECE - 1>();
@@ -152,12 +272,28 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&v)[32], int c, uint
         const int col = col0 + c * 32 + lane;
         if (col < e.N) {
             const int64_t base = static_cast<int64_t>(b) * e.strideC;
+            if constexpr (EPI) {
+                const EpiParams &ep = e.ep;
+                const float cs = ep.col_scale ? __ldg(ep.col_scale + col) : 1.f;
+                const float bias = ep.bias ? __ldg(ep.bias + col) : 0.f;
 #pragma unroll 4
-            for (int r = 0; r < 32; ++r) {
-                const int row = row0 + r;
-                if (row >= e.M) break;
-                store_one<OUT>(e.C, base + static_cast<int64_t>(row) * e.ldc + col,
-                               stg_f[r * 32 + (lane ^ r)]);
+                for (int r = 0; r < 32; ++r) {
+                    const int row = row0 + r;
+                    if (row >= e.M) break;
+                    const int64_t idx = base + static_cast<int64_t>(row) * e.ldc + col;
+                    const float rs = ep.row_scale ? __ldg(ep.row_scale + row) : 1.f;
+                    const float prev = ep.beta != 0.f ? load_one<OUT>(e.C, idx) : 0.f;
+                    store_one<OUT>(e.C, idx,
+                                   epi_value(ep, stg_f[r * 32 + (lane ^ r)], rs, cs, bias, prev));
+                }
+            } else {
+#pragma unroll 4
+                for (int r = 0; r < 32; ++r) {
+                    const int row = row0 + r;
+                    if (row >= e.M) break;
+                    store_one<OUT>(e.C, base + static_cast<int64_t>(row) * e.ldc + col,
+                                   stg_f[r * 32 + (lane ^ r)]);
+                }
             }
         }
     }
@@ -174,7 +310,7 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&v)[32], int c, uint
 // ADD: `addend` holds another fp32 partial of the same 32 rows in the layout
 // spill_accumulator writes; it is added to the accumulator (own + addend)
 // before the conversion.
-template <int OUT, bool TMA_STORE, int NCOLS, bool ADD = false, typename Release>
+template <int OUT, bool TMA_STORE, int NCOLS, bool ADD = false, bool EPI = false, typename Release>
 __device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, float *stg_f,
                                                   int &sbuf, int row0, int col0, int b,
                                                   const EpiArgs &e, Release release,
@@ -226,52 +362,57 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, 
                 v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a.w);
             }
         }
-        store_chunk<OUT, TMA_STORE>(v, c, stg, stg_f, sbuf, row0, col0, b, e);
+        store_chunk<OUT, TMA_STORE, EPI>(v, c, stg, stg_f, sbuf, row0, col0, b, e);
     }
 }
 
 // Sums nseg fp32 partials of one warp's 32 rows x NCOLS columns, stored in
 // the spill_accumulator layout at parts + s * seg_stride (s = 0 .. nseg-1),
 // in the order s = 0, 1, ... (so the result does not depend on which piece
-// arrived last), and stores the sum into C like drain_accumulator.  All
-// loads of a chunk are issued before any is used: one L2 round trip per
-// chunk.  nseg <= MAXSEG.
-template <int OUT, bool TMA_STORE, int NCOLS, int MAXSEG>
+// arrived last), and stores the sum into C like drain_accumulator.  Each
+// chunk is summed in two passes of 16 columns; all segments' loads of a pass
+// are issued before any is used (two L2 round trips per chunk, 64 registers
+// of loads in flight).  nseg <= MAXSEG.
+template <int OUT, bool TMA_STORE, int NCOLS, int MAXSEG, bool EPI = false>
 __device__ __forceinline__ void drain_partials(const float *parts, int64_t seg_stride, int nseg,
                                                uint32_t stg, float *stg_f, int &sbuf, int row0,
                                                int col0, int b, const EpiArgs &e) {
     const int lane = threadIdx.x & 31;
 #pragma unroll 1
     for (int c = 0; c < NCOLS / 32; ++c) {
-        float4 t[MAXSEG][8];
-#pragma unroll
-        for (int s = 0; s < MAXSEG; ++s) {
-            if (s < nseg) {
-                const float4 *src =
-                    reinterpret_cast<const float4 *>(parts + s * seg_stride + c * 1024) + lane;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) t[s][j] = __ldcg(src + j * 32);
-            }
-        }
         uint32_t v[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float4 a = t[0][j];
+        for (int h = 0; h < 2; ++h) {
+            float4 t[MAXSEG][4];
 #pragma unroll
-            for (int s = 1; s < MAXSEG; ++s) {
+            for (int s = 0; s < MAXSEG; ++s) {
                 if (s < nseg) {
-                    a.x += t[s][j].x;
-                    a.y += t[s][j].y;
-                    a.z += t[s][j].z;
-                    a.w += t[s][j].w;
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(parts + s * seg_stride + c * 1024) + lane;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) t[s][j] = __ldcg(src + (4 * h + j) * 32);
                 }
             }
-            v[4 * j] = __float_as_uint(a.x);
-            v[4 * j + 1] = __float_as_uint(a.y);
-            v[4 * j + 2] = __float_as_uint(a.z);
-            v[4 * j + 3] = __float_as_uint(a.w);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float4 a = t[0][j];
+#pragma unroll
+                for (int s = 1; s < MAXSEG; ++s) {
+                    if (s < nseg) {
+                        a.x += t[s][j].x;
+                        a.y += t[s][j].y;
+                        a.z += t[s][j].z;
+                        a.w += t[s][j].w;
+                    }
+                }
+                const int q = 4 * (4 * h + j);
+                v[q] = __float_as_uint(a.x);
+                v[q + 1] = __float_as_uint(a.y);
+                v[q + 2] = __float_as_uint(a.z);
+                v[q + 3] = __float_as_uint(a.w);
+            }
         }
-        store_chunk<OUT, TMA_STORE>(v, c, stg, stg_f, sbuf, row0, col0, b, e);
+        store_chunk<OUT, TMA_STORE, EPI>(v, c, stg, stg_f, sbuf, row0, col0, b, e);
     }
 }
 

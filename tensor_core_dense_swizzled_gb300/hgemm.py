@@ -17,7 +17,8 @@ __all__ = [
     "HGEMM_PATH_TILED", "HGEMM_PATH_SKINNY", "HgemmError", "Options", "PlanInfo", "lib_path",
     "load", "hgemm_plan_create", "hgemm_plan_create_ex", "hgemm_run", "hgemm_run_host",
     "hgemm_check", "hgemm_plan_destroy", "hgemm_plan_get_info", "hgemm", "hgemm_cache_clear",
-    "hgemm_watchdog_selftest", "hgemm_skinny_noalloc", "hgemm_status_string",
+    "hgemm_watchdog_selftest", "hgemm_skinny_noalloc", "hgemm_status_string", "Epilogue",
+    "hgemm_run_ex", "HGEMM_ACT_NONE", "HGEMM_ACT_RELU", "HGEMM_ACT_GELU", "HGEMM_ACT_GELU_TANH",
     "hgemm_last_error_detail", "hgemm_version",
     "STATUS",
 ]
@@ -64,6 +65,22 @@ class Options(ctypes.Structure):
     ]
 
 
+HGEMM_ACT_NONE, HGEMM_ACT_RELU, HGEMM_ACT_GELU, HGEMM_ACT_GELU_TANH = 0, 1, 2, 3
+
+
+class Epilogue(ctypes.Structure):
+    """hgemm_epilogue_t: D = act(alpha * rs[i] * cs[j] * (A.B) + beta * C + bias[j]).
+    Pointers are device addresses (ints) or None."""
+    _fields_ = [
+        ("alpha", ctypes.c_float),
+        ("beta", ctypes.c_float),
+        ("bias", ctypes.c_void_p),
+        ("row_scale", ctypes.c_void_p),
+        ("col_scale", ctypes.c_void_p),
+        ("activation", ctypes.c_int),
+    ]
+
+
 class PlanInfo(ctypes.Structure):
     _fields_ = [
         ("path", ctypes.c_int),
@@ -105,6 +122,7 @@ def load():
         lib.hgemm_plan_create_ex.argtypes = lib.hgemm_plan_create.argtypes + [ctypes.POINTER(Options)]
         lib.hgemm_run.argtypes = [p, p, p, p, p]
         lib.hgemm_run_host.argtypes = [p, p, p, p, p]
+        lib.hgemm_run_ex.argtypes = [p, p, p, p, p, ctypes.POINTER(Epilogue)]
         lib.hgemm_check.argtypes = [p, p]
         lib.hgemm_plan_destroy.argtypes = [p]
         lib.hgemm_plan_get_info.argtypes = [p, ctypes.POINTER(PlanInfo)]
@@ -115,6 +133,7 @@ def load():
         lib.hgemm_skinny_noalloc.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int,
                                              ctypes.c_int, p]
         for name in ("hgemm_plan_create", "hgemm_plan_create_ex", "hgemm_run", "hgemm_run_host",
+                     "hgemm_run_ex",
                      "hgemm_check", "hgemm_plan_destroy", "hgemm_plan_get_info", "hgemm",
                      "hgemm_cache_clear", "hgemm_watchdog_selftest", "hgemm_skinny_noalloc"):
             getattr(lib, name).restype = st
@@ -177,6 +196,21 @@ def hgemm_plan_create_ex(M, N, K, lda, ldb, ldc, batch, strideA, strideB, stride
 
 def hgemm_run(plan: int, A, B, C, stream=None):
     _check(load().hgemm_run(plan, _ptr(A), _ptr(B), _ptr(C), _stream(stream)), "hgemm_run")
+
+
+def hgemm_run_ex(plan: int, A, B, C, epilogue=None, stream=None):
+    """hgemm_run with a fused epilogue (an Epilogue, or None).  Vector
+    arguments of the Epilogue may be given as tensors: they are converted to
+    device addresses here (the caller keeps the tensors alive)."""
+    ep = None
+    if epilogue is not None:
+        ep = Epilogue(float(getattr(epilogue, "alpha", 1.0)), float(getattr(epilogue, "beta", 0.0)),
+                      _ptr(epilogue.bias) if getattr(epilogue, "bias", None) is not None else None,
+                      _ptr(epilogue.row_scale) if getattr(epilogue, "row_scale", None) is not None else None,
+                      _ptr(epilogue.col_scale) if getattr(epilogue, "col_scale", None) is not None else None,
+                      int(getattr(epilogue, "activation", 0)))
+    _check(load().hgemm_run_ex(plan, _ptr(A), _ptr(B), _ptr(C), _stream(stream),
+                               ctypes.byref(ep) if ep is not None else None), "hgemm_run_ex")
 
 
 def hgemm_run_host(plan: int, A_host, B_host, C_host, stream=None):

@@ -46,6 +46,22 @@ def test_gelu_identities(oracle_mod):
     assert d.max() >= oracle_mod.GELU_MAX_SLOPE - 1e-3
 
 
+def test_gelu_tanh_form(oracle_mod):
+    """The tanh form is odd-symmetric like the erf form (g(x) - g(-x) = x),
+    zero at zero, tends to ReLU, stays within 1e-3 of the erf form, and its
+    slope stays under the bound the acceptance measure uses."""
+    x = np.linspace(-8.0, 8.0, 3201)
+    g = oracle_mod.activation(x, oracle_mod.ACT_GELU_TANH)
+    ge = oracle_mod.activation(x, oracle_mod.ACT_GELU)
+    assert oracle_mod.activation(np.array([0.0]), oracle_mod.ACT_GELU_TANH)[0] == 0.0
+    assert np.max(np.abs(g - g[::-1] - x)) < 1e-12
+    assert np.max(np.abs(g - ge)) < 1e-3
+    assert np.max(np.abs(g - ge)) > 1e-5  # a different function, not the erf form again
+    assert abs(oracle_mod.activation(np.array([20.0]), 3)[0] - 20.0) < 1e-12
+    d = np.diff(g) / np.diff(x)
+    assert d.max() <= oracle_mod.GELU_MAX_SLOPE + 2e-3
+
+
 def test_relu(oracle_mod):
     x = np.array([-3.0, -0.0, 0.0, 1e-30, 2.5])
     assert list(oracle_mod.activation(x, oracle_mod.ACT_RELU)) == [0.0, 0.0, 0.0, 1e-30, 2.5]
