@@ -102,6 +102,22 @@ def gemm(A: np.ndarray, B: np.ndarray, dtype_in: int, M: int, N: int, K: int,
     return Cref, Den
 
 
+def gemm_bt(A: np.ndarray, Bs: np.ndarray, dtype_in: int, M: int, N: int, K: int,
+            lda: int, ldb: int, batch: int = 1, strideA: int = 0, strideB: int = 0):
+    """C = A . Bs^T with ``Bs`` stored N x K (element (j, k) of batch b at
+    b*strideB + j*ldb + k): the product with B[k][j] = Bs[j][k].  The stored
+    matrix is transposed into a dense K x N copy (data movement only) and the
+    product is :func:`gemm`'s."""
+    Bs = _u16(Bs)
+    _check_extent(Bs, N, K, ldb, batch, strideB)
+    Bt = np.empty((batch, K, N), dtype=np.uint16)
+    for b in range(batch):
+        if N and K:
+            rows = np.lib.stride_tricks.as_strided(Bs[b * strideB:], shape=(N, K), strides=(ldb * 2, 2))
+            Bt[b] = rows.T
+    return gemm(A, Bt.reshape(-1), dtype_in, M, N, K, lda, N, batch, strideA, K * N)
+
+
 def gemm_entries(A: np.ndarray, B: np.ndarray, dtype_in: int, K: int, lda: int, ldb: int,
                  eb, ei, ej, strideA: int = 0, strideB: int = 0):
     """The same definition for the entries ``(eb[e], ei[e], ej[e])`` only."""

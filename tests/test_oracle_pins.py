@@ -357,3 +357,36 @@ def test_normalized_error_semantics(oracle_mod):
     assert oracle_mod.normalized_error(C, Cref, Den) == float("inf")
     C = np.array([[[float("nan"), 0.0, -2.0]]])
     assert oracle_mod.normalized_error(C, Cref, Den) == float("inf")
+
+
+# ---------------------------------------------------------------- transposed B
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_worked_example_with_b_stored_transposed(oracle_mod, dtype):
+    """B given as its N x K transpose (B^T[j][k] = j) with a padded leading
+    dimension still gives the worked example's D = 16 i j."""
+    _, table = load_worked_example()
+    A, B = worked_example_operands(dtype)
+    Bkn = lib_decode(B, dtype).reshape(16, 8)
+    ldb = 20
+    Bs = np.zeros(8 * ldb, dtype=np.float64)
+    for j in range(8):
+        Bs[j * ldb:j * ldb + 16] = Bkn[:, j]
+    Cref, Den = oracle_mod.gemm_bt(A, encode_exact(Bs, dtype), dtype, 16, 8, 16, 16, ldb)
+    assert np.array_equal(Cref[0], table)
+
+
+def test_transposed_b_batched_against_fsum(oracle_mod):
+    """Batched C = A . Bs^T against math.fsum of the products read straight
+    from the stored N x K layout."""
+    rng = np.random.default_rng(11)
+    M, N, K, batch, ldb, sB = 3, 5, 7, 2, 9, 50
+    A = encode_exact(rng.integers(-4, 5, size=batch * M * K).astype(np.float64), 0)
+    Bs = encode_exact(rng.integers(-4, 5, size=(batch - 1) * sB + N * ldb).astype(np.float64), 0)
+    Cref, _ = oracle_mod.gemm_bt(A, Bs, 0, M, N, K, K, ldb, batch, M * K, sB)
+    a, bs = lib_decode(A, 0), lib_decode(Bs, 0)
+    for b in range(batch):
+        for i in range(M):
+            for j in range(N):
+                want = math.fsum(a[b * M * K + i * K + k] * bs[b * sB + j * ldb + k] for k in range(K))
+                assert Cref[b, i, j] == want
