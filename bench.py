@@ -231,8 +231,13 @@ def oracle_rows_time(w, A_bits, B_bits, rows: int, threads: int) -> float:
     import oracle
     din = 0 if w.dtype_in == "f16" else 1
     t0 = time.perf_counter()
-    oracle.gemm(A_bits[: max(1, rows * w.lda)], B_bits[: (w.K - 1) * w.ldb + w.N] if w.batch == 1 else B_bits,
-                din, rows, w.N, w.K, w.lda, w.ldb, 1, 0, 0, threads=threads)
+    if w.trans_b:  # the transposition is part of the oracle's work
+        oracle.gemm_bt(A_bits[: max(1, rows * w.lda)], B_bits[: w.N * w.ldb], din, rows, w.N, w.K,
+                       w.lda, w.ldb, 1, 0, 0)
+    else:
+        oracle.gemm(A_bits[: max(1, rows * w.lda)],
+                    B_bits[: (w.K - 1) * w.ldb + w.N] if w.batch == 1 else B_bits,
+                    din, rows, w.N, w.K, w.lda, w.ldb, 1, 0, 0, threads=threads)
     return time.perf_counter() - t0
 
 
@@ -298,7 +303,7 @@ def run_reference(args, w, rank, world):
 def config_of(w, world, extra=None):
     c = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "dtype_in": w.dtype_in,
          "dtype_out": w.dtype_out, "seed": w.seed, "parallelism": "replicas" if world > 1 else "single",
-         "layout": "A MxK, B KxN, C MxN row-major"}
+         "layout": ("A MxK, B NxK (C = A.B^T)" if w.trans_b else "A MxK, B KxN") + ", C MxN row-major"}
     if extra:
         c.update(extra)
     return c
@@ -327,8 +332,9 @@ def run_ours(args, w, world, rank, local, pg):
     sets, plans = [], []
     for _ in range(nsets):
         sets.append((A.to(dev), B.to(dev), torch.empty(shape_c, dtype=TD[w.dtype_out], device=dev)))
-        plans.append(H.hgemm_plan_create(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, w.batch, w.strideA,
-                                         w.strideB, w.strideC, DT[w.dtype_in], DT[w.dtype_out]))
+        plans.append(H.hgemm_plan_create_ex(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, w.batch, w.strideA,
+                                            w.strideB, w.strideC, DT[w.dtype_in], DT[w.dtype_out],
+                                            H.Options(trans_b=int(w.trans_b))))
     info = H.hgemm_plan_get_info(plans[0])
     stream = torch.cuda.current_stream(dev)
 

@@ -100,6 +100,10 @@ typedef struct {
                                  the previous kernel of the stream; 0 or -1 none */
     int group_m;              /* tiled path: m-tiles per raster group (tiles run m-fastest within a
                                  group of group_m tile rows); 0 automatic (16) */
+    int trans_b;              /* 0: B is K x N row-major (element (k, j) at B + k*ldb + j); 1: B is
+                                 stored N x K row-major (element (k, j) at B + j*ldb + k, ldb >= K),
+                                 i.e. C = A . B_stored^T -- a linear layer's weight, or attention's
+                                 S = Q K^T with K stored [seq][dim] */
 } hgemm_options_t;
 
 /* Read-only description of what a plan will launch. */
@@ -117,6 +121,7 @@ typedef struct {
     int tail_split;       /* CTA pairs: 2 when the last partial wave's tiles run as two K halves */
     int wide_boxes;       /* CTA pairs: 1 when each pipeline stage of A and of B is one TMA copy
                              (4-D views; 256-wide tiles, K and N multiples of 64) */
+    int trans_b;          /* the plan's B layout (hgemm_options_t.trans_b) */
     int stream_k;         /* K steps dealt in equal contiguous ranges: CTA pairs 1 (tail_mode 3)
                              or 2 (tail_mode 4), the skinny path 1 (skinny_stream_k; split_k is
                              then the most pieces a column tile is cut into) */

@@ -174,7 +174,7 @@ int64_t span_elems(int64_t rows, int64_t cols, int64_t ld, int64_t batch, int64_
 }
 
 hgemm_status_t validate(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                        int64_t batch, int64_t sA, int64_t sB, int64_t sC, hgemm_dtype_t din,
+                        int64_t batch, int64_t sA, int64_t sB, int64_t sC, bool trans_b, hgemm_dtype_t din,
                         hgemm_dtype_t dout) {
     if (din != HGEMM_F16 && din != HGEMM_BF16)
         return fail(HGEMM_ERR_INVALID_ARG, "dtype_in must be HGEMM_F16 or HGEMM_BF16 (got %d)",
@@ -190,8 +190,11 @@ hgemm_status_t validate(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
         return fail(HGEMM_ERR_UNSUPPORTED, "sizes above 2^31-1 are not supported");
     if (M > 0 && K > 0 && lda < K)
         return fail(HGEMM_ERR_INVALID_ARG, "lda (%lld) < K (%lld)", static_cast<long long>(lda), static_cast<long long>(K));
-    if (K > 0 && N > 0 && ldb < N)
+    if (K > 0 && N > 0 && !trans_b && ldb < N)
         return fail(HGEMM_ERR_INVALID_ARG, "ldb (%lld) < N (%lld)", static_cast<long long>(ldb), static_cast<long long>(N));
+    if (K > 0 && N > 0 && trans_b && ldb < K)
+        return fail(HGEMM_ERR_INVALID_ARG, "ldb (%lld) < K (%lld) with trans_b (B stored N x K)",
+                    static_cast<long long>(ldb), static_cast<long long>(K));
     if (M > 0 && N > 0 && ldc < N)
         return fail(HGEMM_ERR_INVALID_ARG, "ldc (%lld) < N (%lld)", static_cast<long long>(ldc), static_cast<long long>(N));
     if (batch > 1 && (sA < 0 || sB < 0 || sC < 0))
@@ -297,8 +300,9 @@ hgemm_status_t alloc_workspace(hgemm_plan_s *p) {
         // (by the leading dimension now, or by a misaligned pointer later)
         p->lda_p = round_up(p->K, 8);
         p->sA_p = p->M * p->lda_p;
-        p->ldb_p = round_up(p->N, 8);
-        p->sB_p = p->K * p->ldb_p;
+        // B stored K x N, or N x K with trans_b: rows x cols of the stored matrix
+        p->ldb_p = round_up(p->opt.trans_b ? p->K : p->N, 8);
+        p->sB_p = (p->opt.trans_b ? p->N : p->K) * p->ldb_p;
         p->apack_bytes = static_cast<size_t>(p->batch * p->sA_p * 2);
         p->bpack_bytes = static_cast<size_t>(p->batch * p->sB_p * 2);
     }
@@ -368,7 +372,10 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
                            const hgemm_options_t *options) {
     if (!out) return fail(HGEMM_ERR_INVALID_ARG, "plan pointer is NULL");
     *out = nullptr;
-    hgemm_status_t st = validate(M, N, K, lda, ldb, ldc, batch, sA, sB, sC, din, dout);
+    if (options && (options->trans_b < 0 || options->trans_b > 1))
+        return fail(HGEMM_ERR_INVALID_ARG, "trans_b must be 0 or 1");
+    hgemm_status_t st = validate(M, N, K, lda, ldb, ldc, batch, sA, sB, sC,
+                                 options && options->trans_b, din, dout);
     if (st != HGEMM_OK) return st;
     hgemm_options_t opt{};
     if (options) opt = *options;
@@ -572,17 +579,25 @@ hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *
         // Pair tiles 256 wide with K and N multiples of 64: the 4-D views
         // (one copy per operand per stage); otherwise, or if the driver
         // rejects them, the 3-D maps.
+        // B stored N x K (trans_b) is staged K-major like A: its 4-D view
+        // splits K the same way (128 rows of B per CTA), and needs only K to
+        // be a multiple of 64.
+        const bool tb = p->opt.trans_b != 0;
         p->wide = false;
-        if (p->pair && p->bn == 256 && p->K % 64 == 0 && p->N % 64 == 0) {
+        if (p->pair && p->bn == 256 && p->K % 64 == 0 && (tb || p->N % 64 == 0)) {
             p->wide = encode_split_4d(&p->tmA, A, dt, p->K, p->M, p->batch, lda, sA, 128,
                                       static_cast<uint32_t>(p->pair_ks)) == HGEMM_OK &&
-                      encode_split_4d(&p->tmB, B, dt, p->N, p->K, p->batch, ldb, sB,
-                                      static_cast<uint32_t>(64 * p->pair_ks), 2) == HGEMM_OK;
+                      (tb ? encode_split_4d(&p->tmB, B, dt, p->K, p->N, p->batch, ldb, sB, 128,
+                                            static_cast<uint32_t>(p->pair_ks))
+                          : encode_split_4d(&p->tmB, B, dt, p->N, p->K, p->batch, ldb, sB,
+                                            static_cast<uint32_t>(64 * p->pair_ks), 2)) == HGEMM_OK;
         }
         if (!p->wide) {
             st = encode_3d(&p->tmA, A, dt, 2, p->K, p->M, p->batch, lda, sA, 64, 128);
             if (st != HGEMM_OK) return st;
-            st = encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64);
+            // 64 x 64 boxes of B either way: (n, k) MN-major, (k, n) K-major
+            st = tb ? encode_3d(&p->tmB, B, dt, 2, p->K, p->N, p->batch, ldb, sB, 64, 64)
+                    : encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64);
             if (st != HGEMM_OK) return st;
         }
         if (tma_store) {
@@ -603,8 +618,11 @@ hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *
         if (st != HGEMM_OK) return st;
         // streamed once: 128-byte L2 fills (256-byte promotion measured 1.3 %
         // slower on 8 x 28672 x 4096)
-        st = encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64,
-                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+        st = p->opt.trans_b
+                 ? encode_3d(&p->tmB, B, dt, 2, p->K, p->N, p->batch, ldb, sB, 64, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)
+                 : encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
         if (st != HGEMM_OK) return st;
         std::memset(&p->tmC, 0, sizeof(p->tmC));
     }
@@ -652,7 +670,8 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     }
     if (pack_b) {
         jobs[njobs++] = hg::Repack16Job{B, p->ldb, p->sB, p->ws + p->off_bpack, p->ldb_p,
-                                        p->sB_p, p->K, p->N, p->batch};
+                                        p->sB_p, p->opt.trans_b ? p->N : p->K,
+                                        p->opt.trans_b ? p->K : p->N, p->batch};
         Be = p->ws + p->off_bpack;
     }
     if (njobs > 0) {  // both copies in one launch
@@ -675,7 +694,10 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.num_kb = static_cast<int32_t>(ceil_div(p->K, 64));
         tp.tiles = tp.batch * tp.num_m * tp.num_n;
         tp.group_m = p->opt.group_m ? p->opt.group_m : 16;
-        tp.idesc = hg::idesc_f16(bf, 0, 1, p->pair ? 256 : 128, static_cast<uint32_t>(p->bn));
+        // B MN-major (stored K x N, N contiguous) or K-major (trans_b: N x K)
+        tp.idesc = hg::idesc_f16(bf, 0, p->opt.trans_b ? 0 : 1, p->pair ? 256 : 128,
+                                 static_cast<uint32_t>(p->bn));
+        tp.b_kmajor = p->opt.trans_b ? 1 : 0;
         tp.C = C;
         tp.ep = ep;
         tp.ldc = p->ldc;
@@ -714,7 +736,10 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     // default none: on 8 x 28672 x 4096, 4 or 8 stages measured the same as
     // none (38.4-38.7 us back to back), 16 and more slower
     sp.prefetch = p->opt.skinny_prefetch > 0 ? p->opt.skinny_prefetch : 0;
-    sp.idesc = hg::idesc_f16(bf, 1, 0, 128, static_cast<uint32_t>(p->nu));
+    // the MMA's A operand is B^T: MN-major from a K x N B, K-major from an
+    // N x K B (trans_b)
+    sp.idesc = hg::idesc_f16(bf, p->opt.trans_b ? 0 : 1, 0, 128, static_cast<uint32_t>(p->nu));
+    sp.b_kmajor = p->opt.trans_b ? 1 : 0;
     sp.C = C;
     sp.ep = ep;
     sp.ldc = p->ldc;
@@ -790,7 +815,9 @@ hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void 
         return fail(HGEMM_ERR_INVALID_ARG, "host pointer is NULL");
     const int ob = out_bytes(p->dout);
     const size_t a_bytes = static_cast<size_t>(span_elems(p->M, p->K, p->lda, p->batch, p->sA)) * 2;
-    const size_t b_bytes = static_cast<size_t>(span_elems(p->K, p->N, p->ldb, p->batch, p->sB)) * 2;
+    const size_t b_bytes =
+        static_cast<size_t>(p->opt.trans_b ? span_elems(p->N, p->K, p->ldb, p->batch, p->sB)
+                                           : span_elems(p->K, p->N, p->ldb, p->batch, p->sB)) * 2;
     const size_t c_bytes = static_cast<size_t>(span_elems(p->M, p->N, p->ldc, p->batch, p->sC)) * ob;
     cudaError_t e;
     auto grow = [&](char **buf, size_t *have, size_t want) -> cudaError_t {
@@ -883,11 +910,13 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     if (plan->path == HGEMM_PATH_ZERO_FILL) r.kernels_per_run = 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
     r.tail_split = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->tail_split : 1;
+    r.trans_b = plan->opt.trans_b;
     r.stream_k = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->stream_k
                  : plan->path == HGEMM_PATH_SKINNY && plan->skinny_deal ? 1
                                                                        : 0;
     r.wide_boxes = plan->path == HGEMM_PATH_TILED && plan->pair && plan->bn == 256 &&
-                           plan->K % 64 == 0 && plan->N % 64 == 0 && (plan->wide || !plan->maps_ok)
+                           plan->K % 64 == 0 && (plan->opt.trans_b || plan->N % 64 == 0) &&
+                           (plan->wide || !plan->maps_ok)
                        ? 1
                        : 0;
     *info = r;

@@ -342,7 +342,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // block (zero-filled), so the bytes are the stage's.
                         if (rank == 0) mbar_arrive_expect_tx(full(stage), 2u * Cfg::STAGE_BYTES);
                         tma_load_4d_pair(dA, &tmA, fb, 0, m0, ks * KS, b);
-                        tma_load_4d_pair(dB, &tmB, fb, 0, ks * KS * BK, n0 / 64, b);
+                        if (p.b_kmajor)  // B stored N x K: the same view as A's
+                            tma_load_4d_pair(dB, &tmB, fb, 0, n0, ks * KS, b);
+                        else
+                            tma_load_4d_pair(dB, &tmB, fb, 0, ks * KS * BK, n0 / 64, b);
                     } else {
                         // K blocks of this step that exist (the last step of an
                         // odd count has one); the leader arms for both CTAs' bytes.
@@ -354,10 +357,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             if (s >= nsub) break;
                             const int kb = ks * KS + s;
                             tma_load_3d_pair(dA + s * Cfg::A_SUB, &tmA, fb, kb * BK, m0, b);
+                            if (p.b_kmajor) {
+                                // K-major: 64-row blocks j of K block s stacked, so
+                                // the CTA's 128 rows of B are contiguous
 #pragma unroll
-                            for (int j = 0; j < Cfg::B_BLOCKS; ++j)
-                                tma_load_3d_pair(dB + j * Cfg::B_COLS + s * Cfg::B_BLOCK, &tmB, fb,
-                                                 n0 + j * 64, kb * BK, b);
+                                for (int j = 0; j < Cfg::B_BLOCKS; ++j)
+                                    tma_load_3d_pair(dB + s * Cfg::B_SUB + j * Cfg::B_BLOCK, &tmB, fb,
+                                                     kb * BK, n0 + j * 64, b);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < Cfg::B_BLOCKS; ++j)
+                                    tma_load_3d_pair(dB + j * Cfg::B_COLS + s * Cfg::B_BLOCK, &tmB,
+                                                     fb, n0 + j * 64, kb * BK, b);
+                            }
                         }
                     }
                     ++issued;
@@ -406,7 +418,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * Cfg::TMEM_STRIDE;
                 const uint64_t adesc0 = sdesc_sw128(sA, 16, 1024);
-                const uint64_t bdesc0 = sdesc_sw128(sB, Cfg::B_COLS, 1024);
+                // B MN-major: 64-column blocks B_COLS apart, 2 KB per 16 K rows;
+                // K-major (stored N x K): rows of 128 bytes, 32 bytes per 16 K
+                const bool bk = p.b_kmajor != 0;
+                const uint64_t bdesc0 =
+                    bk ? sdesc_sw128(sB, 16, 1024) : sdesc_sw128(sB, Cfg::B_COLS, 1024);
                 for (int ks = ks0; ks < ks1; ++ks) {
                     if (!wait_bounded(full(stage), phase, wc, timeout_code(ROLE_MMA, stage))) {
                         ok = false;
@@ -428,7 +444,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
                             const uint64_t ad = a_st + ((s * Cfg::A_SUB + k * 32) >> 4);
-                            const uint64_t bd = b_st + ((s * Cfg::B_BLOCK + k * 16 * 128) >> 4);
+                            const uint64_t bd =
+                                b_st + (bk ? ((s * Cfg::B_SUB + k * 32) >> 4)
+                                           : ((s * Cfg::B_BLOCK + k * 16 * 128) >> 4));
                             umma_f16_pair(d_tmem, ad, bd, p.idesc, (s > 0 || k > 0) ? 1u : acc0);
                         }
                     }

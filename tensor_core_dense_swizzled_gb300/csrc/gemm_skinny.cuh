@@ -223,7 +223,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 while (n < p.prefetch && pre.next(p, w)) {
                     for (int kb = w.kb0; kb < w.kb1 && n < p.prefetch; ++kb, ++n)
                         for (int j = 0; j < Cfg::W_BLOCKS; ++j)
-                            tma_prefetch_3d(&tmW, w.nt * UW + j * 64, kb * BK, w.b);
+                            if (p.b_kmajor)
+                                tma_prefetch_3d(&tmW, kb * BK, w.nt * UW + j * 64, w.b);
+                            else
+                                tma_prefetch_3d(&tmW, w.nt * UW + j * 64, kb * BK, w.b);
                 }
             }
             // Nothing this kernel reads may reach shared memory before the
@@ -245,9 +248,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     mbar_arrive_expect_tx(full(stage), Cfg::TX_BYTES);
 #pragma unroll
-                    for (int j = 0; j < Cfg::W_BLOCKS; ++j)
-                        tma_load_3d(sW + stage * Cfg::W_BYTES + j * Cfg::W_BLOCK, &tmW, full(stage),
-                                    nt * UW + j * 64, kb * BK, b);
+                    for (int j = 0; j < Cfg::W_BLOCKS; ++j) {
+                        // 64 x 64 blocks of B: (n, k) MN-major, or (k, n) when B is
+                        // stored N x K (blocks stack into rows = columns of C)
+                        if (p.b_kmajor)
+                            tma_load_3d(sW + stage * Cfg::W_BYTES + j * Cfg::W_BLOCK, &tmW,
+                                        full(stage), kb * BK, nt * UW + j * 64, b);
+                        else
+                            tma_load_3d(sW + stage * Cfg::W_BYTES + j * Cfg::W_BLOCK, &tmW,
+                                        full(stage), nt * UW + j * 64, kb * BK, b);
+                    }
                     tma_load_3d(sX + stage * Cfg::X_BYTES, &tmX, full(stage), kb * BK, 0, b);
                     ++issued;
                     if (++stage == Cfg::STAGES) {
@@ -302,8 +312,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             // MMA A = columns j*128 .. j*128+127 of the B tile, MN-major
                             // (with NB odd, the last one's upper 64 columns are
                             // the shared memory after the stage: never stored)
-                            const uint64_t ad = sdesc_sw128(
-                                w0 + 2 * j * Cfg::W_BLOCK + k * 16 * 128, Cfg::W_BLOCK, 1024);
+                            const uint64_t ad =
+                                p.b_kmajor
+                                    ? sdesc_sw128(w0 + 2 * j * Cfg::W_BLOCK + k * 32, 16, 1024)
+                                    : sdesc_sw128(w0 + 2 * j * Cfg::W_BLOCK + k * 16 * 128,
+                                                  Cfg::W_BLOCK, 1024);
                             umma_f16(d0 + j * NU, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         }
                     }

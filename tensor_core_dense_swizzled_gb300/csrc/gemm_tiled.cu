@@ -160,10 +160,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     mbar_arrive_expect_tx(full(stage), Cfg::TX_BYTES);
                     tma_load_3d(sA + stage * Cfg::A_BYTES, &tmA, full(stage), kb * BK, mt * BM, b);
+                    // 64 x 64 blocks of B: (n, k) MN-major, or (k, n) K-major
+                    // when B is stored N x K (the blocks stack into BN rows)
 #pragma unroll
-                    for (int j = 0; j < Cfg::B_BLOCKS; ++j)
-                        tma_load_3d(sB + stage * Cfg::B_BYTES + j * Cfg::B_BLOCK, &tmB, full(stage),
-                                    nt * BN + j * 64, kb * BK, b);
+                    for (int j = 0; j < Cfg::B_BLOCKS; ++j) {
+                        if (p.b_kmajor)
+                            tma_load_3d(sB + stage * Cfg::B_BYTES + j * Cfg::B_BLOCK, &tmB,
+                                        full(stage), kb * BK, nt * BN + j * 64, b);
+                        else
+                            tma_load_3d(sB + stage * Cfg::B_BYTES + j * Cfg::B_BLOCK, &tmB,
+                                        full(stage), nt * BN + j * 64, kb * BK, b);
+                    }
                     ++issued;
                     if (++stage == Cfg::STAGES) {
                         stage = 0;
@@ -211,7 +218,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(b0 + k * 16 * 128, Cfg::B_BLOCK, 1024);
+                        const uint64_t bd = p.b_kmajor
+                                                ? sdesc_sw128(b0 + k * 32, 16, 1024)
+                                                : sdesc_sw128(b0 + k * 16 * 128, Cfg::B_BLOCK, 1024);
                         umma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     umma_commit(empty(stage));

@@ -64,6 +64,9 @@ struct TiledParams {
     // fp32, tail_sync = counters [tile][rank][warp] (zero between runs).
     int32_t max_seg;
     EpiParams ep;
+    // 1: B is stored N x K (K contiguous) and staged K-major; 0: K x N,
+    // staged MN-major.
+    int32_t b_kmajor;
 };
 
 // Skinny kernel: C^T = B^T . A^T, NB x 64 output columns of C per work
@@ -92,6 +95,9 @@ struct SkinnyParams {
     // Stages of B each CTA asks L2 for before waiting on the previous kernel.
     int32_t prefetch;
     EpiParams ep;
+    // 1: B is stored N x K (K contiguous): the MMA's A operand (B^T) is
+    // staged K-major, rows = columns of C; 0: K x N, staged MN-major.
+    int32_t b_kmajor;
 };
 
 // Shared memory the tiled kernel needs for a given BN (bytes, incl. alignment slack).

@@ -62,6 +62,7 @@ class Options(ctypes.Structure):
         ("skinny_stream_k", ctypes.c_int),
         ("skinny_prefetch", ctypes.c_int),
         ("group_m", ctypes.c_int),
+        ("trans_b", ctypes.c_int),
     ]
 
 
@@ -97,6 +98,7 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes", ctypes.c_int64),
         ("tail_split", ctypes.c_int),
         ("wide_boxes", ctypes.c_int),
+        ("trans_b", ctypes.c_int),
         ("stream_k", ctypes.c_int),
     ]
 

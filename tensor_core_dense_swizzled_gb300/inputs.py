@@ -53,6 +53,7 @@ class Workload:
     scale_a: float
     scale_b: float
     seed: int
+    trans_b: bool = False  # B stored N x K (C = A . B_stored^T), same values as the K x N draw
 
     @property
     def lda(self) -> int:
@@ -60,7 +61,7 @@ class Workload:
 
     @property
     def ldb(self) -> int:
-        return self.N
+        return self.K if self.trans_b else self.N
 
     @property
     def ldc(self) -> int:
@@ -72,7 +73,7 @@ class Workload:
 
     @property
     def strideB(self) -> int:
-        return self.K * self.N if self.batch > 1 else 0
+        return self.K * self.N if self.batch > 1 else 0  # K x N or N x K: the same size
 
     @property
     def strideC(self) -> int:
@@ -90,6 +91,14 @@ WORKLOADS = {
         Workload("ragged4095", 4095, 4095, 4095, 1, "f16", "f32", "uniform", "uniform", 1.0, 1.0, 3),
         Workload("ragged4095_h", 4095, 4095, 4095, 1, "f16", "f16", "uniform", "uniform", 1.0, 1.0, 3),
         Workload("skinny", 8, 28672, 4096, 1, "bf16", "bf16", "normal", "normal", 1.0, 0.02, 4),
+        # the same products with B stored N x K: a linear layer's [out][in]
+        # weight, attention's K stored [seq][dim], and the square product
+        Workload("skinny_tn", 8, 28672, 4096, 1, "bf16", "bf16", "normal", "normal", 1.0, 0.02, 4,
+                 trans_b=True),
+        Workload("batched_qk_tn", 1024, 1024, 128, 64, "bf16", "f32", "normal", "normal",
+                 1.0 / math.sqrt(128.0), 1.0 / math.sqrt(128.0), 3, trans_b=True),
+        Workload("square4096_tn", 4096, 4096, 4096, 1, "bf16", "bf16", "normal", "normal", 1.0, 1.0, 1,
+                 trans_b=True),
     ]
 }
 
@@ -107,12 +116,15 @@ def _draw(gen: torch.Generator, shape, dist: str, scale: float) -> torch.Tensor:
 def make_inputs(w: Workload):
     """Returns CPU tensors ``(A, B)`` in the workload's input dtype, shaped
     ``(batch, M, K)`` / ``(batch, K, N)`` when ``batch > 1`` and ``(M, K)`` /
-    ``(K, N)`` otherwise; both contiguous row-major."""
+    ``(K, N)`` otherwise (B ``(..., N, K)`` for ``trans_b`` workloads); all
+    contiguous row-major."""
     gen = torch.Generator().manual_seed(w.seed)
     sa = (w.batch, w.M, w.K) if w.batch > 1 else (w.M, w.K)
     sb = (w.batch, w.K, w.N) if w.batch > 1 else (w.K, w.N)
     A = _draw(gen, sa, w.dist_a, w.scale_a).to(_TD[w.dtype_in])
     B = _draw(gen, sb, w.dist_b, w.scale_b).to(_TD[w.dtype_in])
+    if w.trans_b:  # stored N x K, the same values
+        B = B.transpose(-1, -2).contiguous()
     return A, B
 
 
