@@ -34,7 +34,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F16, BF16 = 0, 1
+F16, BF16, E4M3, E5M2 = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -64,6 +64,10 @@ def _load():
             lib.oracle_decode_f16.restype = ctypes.c_double
             lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
             lib.oracle_decode_bf16.restype = ctypes.c_double
+            lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint16]
+            lib.oracle_decode_e4m3.restype = ctypes.c_double
+            lib.oracle_decode_e5m2.argtypes = [ctypes.c_uint16]
+            lib.oracle_decode_e5m2.restype = ctypes.c_double
             lib.oracle_decode_array.argtypes = [p, ctypes.c_int, i64, p]
             lib.oracle_decode_array.restype = None
             _lib = lib
@@ -144,9 +148,16 @@ def gemm_entries(A: np.ndarray, B: np.ndarray, dtype_in: int, K: int, lda: int, 
     return Cref, Den
 
 
+def widen8(b: np.ndarray) -> np.ndarray:
+    """8-bit patterns (E4M3 / E5M2) as the 16-bit pattern arrays the oracle
+    reads (the byte in the low half)."""
+    return np.ascontiguousarray(np.asarray(b, dtype=np.uint8).astype(np.uint16))
+
+
 def decode(bits: np.ndarray, dtype: int) -> np.ndarray:
-    """Reads raw fp16 (dtype 0) or bf16 (dtype 1) patterns with the oracle's
-    own decoder; returns fp64 of the same shape."""
+    """Reads raw fp16 (dtype 0), bf16 (1), E4M3 (2) or E5M2 (3) patterns
+    (16-bit arrays; 8-bit patterns widened) with the oracle's own decoders;
+    returns fp64 of the same shape."""
     lib = _load()
     bits = _u16(bits)
     out = np.empty(bits.shape, dtype=np.float64)
@@ -156,7 +167,8 @@ def decode(bits: np.ndarray, dtype: int) -> np.ndarray:
 
 def decode_one(h: int, dtype: int) -> float:
     lib = _load()
-    return lib.oracle_decode_f16(h) if dtype == F16 else lib.oracle_decode_bf16(h)
+    return [lib.oracle_decode_f16, lib.oracle_decode_bf16, lib.oracle_decode_e4m3,
+            lib.oracle_decode_e5m2][dtype](h)
 
 
 def normalized_error(C: np.ndarray, Cref: np.ndarray, Den: np.ndarray) -> float:

@@ -23,7 +23,10 @@
  *
  * Element (i,k) of A_b lives at A[b*strideA + i*lda + k]; (k,j) of B_b at
  * B[b*strideB + k*ldb + j].  Inputs are raw 16-bit patterns; `dtype_in` says
- * how to read them: 0 = IEEE binary16 (fp16), 1 = bfloat16.
+ * how to read them: 0 = IEEE binary16 (fp16), 1 = bfloat16, 2 = E4M3 and
+ * 3 = E5M2 (8-bit patterns in the low byte: the 8-bit inputs of the
+ * tensor-core path, "tensor-cores-cutlass-and-cute" section 二.1, its table
+ * of input types: FP8 e4m3 with twice the K per instruction).
  *
  * Parity pins (tests/test_oracle_pins.py): the single-warp worked example of
  * the "post_1787550000" mma.sync layout experiment (section 6.1: A[i][k] = i,
@@ -75,8 +78,53 @@ double oracle_decode_bf16(uint16_t h) {
     return sign ? -v : v;
 }
 
+/* 8-bit floating point, E4M3 (the "fn" variant): 1 sign bit, 4 exponent
+ * bits (bias 7), 3 fraction bits.  Exponent 0 holds zero and the subnormals
+ * (frac * 2^-9); there are no infinities, and only S.1111.111 is NaN, so the
+ * largest value is 1.75 * 2^8 = 448.  Patterns above 0xff are not E4M3. */
+double oracle_decode_e4m3(uint16_t h) {
+    if (h > 0xff) return NAN;
+    int sign = (h >> 7) & 1;
+    int e = (h >> 3) & 0xf;
+    int f = h & 0x7;
+    double v;
+    if (e == 0xf && f == 0x7)
+        return NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);
+    else
+        v = ldexp(1.0 + f / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* 8-bit floating point, E5M2: 1 sign bit, 5 exponent bits (bias 15), 2
+ * fraction bits, laid out like binary16's upper byte: exponent 0 holds zero
+ * and the subnormals (frac * 2^-16), exponent 31 infinities (frac 0) and
+ * NaNs; the largest finite value is 1.75 * 2^15 = 57344. */
+double oracle_decode_e5m2(uint16_t h) {
+    if (h > 0xff) return NAN;
+    int sign = (h >> 7) & 1;
+    int e = (h >> 2) & 0x1f;
+    int f = h & 0x3;
+    double v;
+    if (e == 0x1f)
+        v = f ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)f, -16);
+    else
+        v = ldexp(1.0 + f / 4.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* dtype_in: 0 fp16, 1 bf16, 2 E4M3, 3 E5M2 (8-bit patterns stored in the
+ * low byte of each 16-bit element). */
 static double decode(uint16_t h, int dtype_in) {
-    return dtype_in == 0 ? oracle_decode_f16(h) : oracle_decode_bf16(h);
+    switch (dtype_in) {
+        case 0: return oracle_decode_f16(h);
+        case 1: return oracle_decode_bf16(h);
+        case 2: return oracle_decode_e4m3(h);
+        default: return oracle_decode_e5m2(h);
+    }
 }
 
 /* ---- full product ------------------------------------------------------ */
@@ -126,7 +174,7 @@ int oracle_gemm(const uint16_t *A, const uint16_t *B, int dtype_in,
                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                 int64_t batch, int64_t strideA, int64_t strideB,
                 double *Cref, double *Den, int threads) {
-    if (M < 0 || N < 0 || K < 0 || batch < 1 || (dtype_in != 0 && dtype_in != 1))
+    if (M < 0 || N < 0 || K < 0 || batch < 1 || (dtype_in < 0 || dtype_in > 3))
         return -1;
     if (threads < 1) threads = 1;
     double *table = make_table(dtype_in);
@@ -170,7 +218,7 @@ int oracle_gemm_entries(const uint16_t *A, const uint16_t *B, int dtype_in,
                         int64_t strideA, int64_t strideB, int64_t n,
                         const int64_t *eb, const int64_t *ei, const int64_t *ej,
                         double *Cref, double *Den) {
-    if (K < 0 || n < 0 || (dtype_in != 0 && dtype_in != 1)) return -1;
+    if (K < 0 || n < 0 || (dtype_in < 0 || dtype_in > 3)) return -1;
     for (int64_t e = 0; e < n; ++e) {
         const uint16_t *arow = A + eb[e] * strideA + ei[e] * lda;
         const uint16_t *bcol = B + eb[e] * strideB + ej[e];

@@ -390,3 +390,61 @@ def test_transposed_b_batched_against_fsum(oracle_mod):
             for j in range(N):
                 want = math.fsum(a[b * M * K + i * K + k] * bs[b * sB + j * ldb + k] for k in range(K))
                 assert Cref[b, i, j] == want
+
+
+# ---------------------------------------------------------------- 8-bit inputs
+
+FP8_TORCH = {2: "float8_e4m3fn", 3: "float8_e5m2"}
+
+
+@pytest.mark.parametrize("dtype", [2, 3])
+def test_fp8_decoder_all_patterns(oracle_mod, dtype):
+    """The oracle's E4M3 / E5M2 decoders against PyTorch's float8 dtypes
+    (an independent library decoder) on all 256 patterns; NaNs agree."""
+    import torch
+    b = np.arange(256, dtype=np.uint8)
+    lib = torch.from_numpy(b).view(getattr(torch, FP8_TORCH[dtype])).float().double().numpy()
+    got = oracle_mod.decode(oracle_mod.widen8(b), dtype)
+    assert np.array_equal(np.isnan(got), np.isnan(lib))
+    ok = ~np.isnan(lib)
+    assert np.array_equal(got[ok], lib[ok])
+
+
+def test_fp8_special_values(oracle_mod):
+    """Extremes of the two formats: E4M3 has no infinity, max 448, smallest
+    subnormal 2^-9; E5M2 max 57344, infinity at 0x7c, smallest subnormal
+    2^-16."""
+    d = oracle_mod.decode_one
+    assert d(0x7E, 2) == 448.0 and d(0xFE, 2) == -448.0 and math.isnan(d(0x7F, 2))
+    assert d(0x01, 2) == 2.0 ** -9 and d(0x08, 2) == 2.0 ** -6 and d(0x38, 2) == 1.0
+    assert d(0x7B, 3) == 57344.0 and d(0x7C, 3) == math.inf and math.isnan(d(0x7D, 3))
+    assert d(0x01, 3) == 2.0 ** -16 and d(0x3C, 3) == 1.0 and d(0xFC, 3) == -math.inf
+    assert math.isnan(d(0x100, 2))  # not an 8-bit pattern
+
+
+def test_worked_example_e4m3(oracle_mod):
+    """The worked example (integers 0..15 are exact in E4M3) read as 8-bit
+    inputs: D = 16 i j exactly."""
+    import torch
+    _, table = load_worked_example()
+    A = torch.tensor([[float(i)] * 16 for i in range(16)]).to(torch.float8_e4m3fn)
+    B = torch.tensor([[float(j) for j in range(8)] for _ in range(16)]).to(torch.float8_e4m3fn)
+    a8 = A.view(torch.uint8).numpy().reshape(-1)
+    b8 = B.view(torch.uint8).numpy().reshape(-1)
+    Cref, Den = oracle_mod.gemm(oracle_mod.widen8(a8), oracle_mod.widen8(b8), 2, 16, 8, 16, 16, 8)
+    assert np.array_equal(Cref[0], table) and np.array_equal(Den[0], table)
+
+
+def test_fp8_product_against_fsum(oracle_mod):
+    """A small E5M2 x E5M2 product against math.fsum of library-decoded values."""
+    import torch
+    g = torch.Generator().manual_seed(5)
+    M, N, K = 4, 6, 9
+    A = (torch.randn(M, K, generator=g) * 3).to(torch.float8_e5m2)
+    B = (torch.randn(K, N, generator=g) * 3).to(torch.float8_e5m2)
+    Cref, _ = oracle_mod.gemm(oracle_mod.widen8(A.view(torch.uint8).numpy().reshape(-1)),
+                              oracle_mod.widen8(B.view(torch.uint8).numpy().reshape(-1)), 3, M, N, K, K, N)
+    a, b = A.float().double().numpy(), B.float().double().numpy()
+    for i in range(M):
+        for j in range(N):
+            assert Cref[0, i, j] == math.fsum(a[i, k] * b[k, j] for k in range(K))
