@@ -46,6 +46,9 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense fp16/bf16 tensor peak (or % HBM BW)"
 NOMINAL_TC_TFLOPS = 2250.0   # dense fp16/bf16 per GPU, nominal
+NOMINAL_F8_RATIO = 2.0       # dense fp8 / dense bf16 tensor rate, nominal (4.5 / 2.25 PFLOP/s)
+F8_TYPES = ("e4m3", "e5m2")
+ORACLE_IN = {"f16": 0, "bf16": 1, "e4m3": 2, "e5m2": 3}  # the oracle's input-type codes
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 2**20
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
@@ -213,15 +216,25 @@ def flops_of(w):
     return 2 * w.M * w.N * w.K * w.batch
 
 
+def in_bytes_of(w) -> int:
+    return 1 if w.dtype_in in F8_TYPES else 2
+
+
+def tensor_ratio(w) -> float:
+    """Tensor-core rate of the workload's input type relative to bf16."""
+    return NOMINAL_F8_RATIO if w.dtype_in in F8_TYPES else 1.0
+
+
 def min_bytes_of(w):
     ob = 4 if w.dtype_out == "f32" else 2
-    return w.batch * (w.M * w.K * 2 + w.K * w.N * 2 + w.M * w.N * ob), ob
+    ib = in_bytes_of(w)
+    return w.batch * (w.M * w.K * ib + w.K * w.N * ib + w.M * w.N * ob), ob
 
 
 def roofline_bound(w) -> str:
     fl = flops_of(w)
     by, _ = min_bytes_of(w)
-    ridge = NOMINAL_TC_TFLOPS * 1e12 / (NOMINAL_HBM_GBS * 1e9)
+    ridge = NOMINAL_TC_TFLOPS * tensor_ratio(w) * 1e12 / (NOMINAL_HBM_GBS * 1e9)
     return "tensor" if fl / by > ridge else "hbm"
 
 
@@ -229,7 +242,7 @@ def roofline_bound(w) -> str:
 
 def oracle_rows_time(w, A_bits, B_bits, rows: int, threads: int) -> float:
     import oracle
-    din = 0 if w.dtype_in == "f16" else 1
+    din = ORACLE_IN[w.dtype_in]
     t0 = time.perf_counter()
     if w.trans_b:  # the transposition is part of the oracle's work
         oracle.gemm_bt(A_bits[: max(1, rows * w.lda)], B_bits[: w.N * w.ldb], din, rows, w.N, w.K,
@@ -247,6 +260,10 @@ def cpu_inputs(w):
 
     from tensor_core_dense_swizzled_gb300 import inputs
     A, B = inputs.make_inputs(w)
+    if w.dtype_in in F8_TYPES:  # 8-bit patterns widened to the oracle's 16-bit arrays
+        ab = A.contiguous().view(torch.uint8).numpy().astype(np.uint16).reshape(-1)
+        bb = B.contiguous().view(torch.uint8).numpy().astype(np.uint16).reshape(-1)
+        return ab, bb
     ab = A.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
     bb = B.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
     return ab, bb
@@ -321,12 +338,14 @@ def run_ours(args, w, world, rank, local, pg):
     __graft_entry__.build()
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    DT = {"f16": H.HGEMM_F16, "bf16": H.HGEMM_BF16, "f32": H.HGEMM_F32}
+    DT = {"f16": H.HGEMM_F16, "bf16": H.HGEMM_BF16, "f32": H.HGEMM_F32, "e4m3": H.HGEMM_E4M3,
+          "e5m2": H.HGEMM_E5M2}
     TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
     A, B = inputs.make_inputs(w)
     flops = flops_of(w)
     min_bytes, ob = min_bytes_of(w)
-    set_bytes = A.numel() * 2 + B.numel() * 2 + w.batch * w.M * w.N * ob
+    ib = in_bytes_of(w)
+    set_bytes = A.numel() * ib + B.numel() * ib + w.batch * w.M * w.N * ob
     nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes))
     shape_c = (w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N)
     sets, plans = [], []
@@ -411,9 +430,12 @@ def run_ours(args, w, world, rank, local, pg):
     sustained = region_ms > 1000.0
     if bound == "tensor":
         achieved = flops / (avg_launch_ms * 1e-3) / 1e12
-        peak = peaks["bf16_sustained"] if sustained else peaks["bf16"]
+        # an 8-bit contraction: the measured bf16 peak x the nominal fp8 / bf16 ratio
+        peak = (peaks["bf16_sustained"] if sustained else peaks["bf16"]) * tensor_ratio(w)
         unit = "TFLOP/s"
         peak_kind = ("sustained" if sustained else "burst") + f" bf16, {peaks['source']}"
+        if tensor_ratio(w) != 1.0:
+            peak_kind += f", x {tensor_ratio(w):g} (nominal fp8 / bf16 rate)"
     else:
         achieved = min_bytes / (avg_launch_ms * 1e-3) / 1e9
         peak = peaks["hbm"]
@@ -438,7 +460,7 @@ def run_ours(args, w, world, rank, local, pg):
         dt = time.perf_counter() - t0
         dt = max_over_ranks(pg, dt, dev)
         e2e = {"value": flops * args.e2e_steps * world / dt / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": A.numel() * 2 + B.numel() * 2,
+               "h2d_bytes_per_step": A.numel() * ib + B.numel() * ib,
                "d2h_bytes_per_step": w.batch * w.M * w.N * ob, "steps": args.e2e_steps}
 
     cpu = None
@@ -458,7 +480,7 @@ def run_ours(args, w, world, rank, local, pg):
             "path": {2: "tiled", 3: "skinny", 1: "zero_fill", 0: "empty"}[info["path"]],
             "tile": [info["tile_m"], info["tile_n"], info["tile_k"]], "stages": info["stages"],
             "split_k": info["split_k"], "grid": info["grid"], "epilogue": args.epilogue}),
-        "pct_nominal_tensor_peak": 100.0 * value / world / NOMINAL_TC_TFLOPS,
+        "pct_nominal_tensor_peak": 100.0 * value / world / (NOMINAL_TC_TFLOPS * tensor_ratio(w)),
         "pct_nominal_hbm": 100.0 * (min_bytes * args.steps / (region_ms * 1e-3) / 1e9) / NOMINAL_HBM_GBS,
         "roofline": roof,
         "cpu_baseline": cpu,

@@ -46,7 +46,11 @@ extern "C" {
 typedef enum {
     HGEMM_F16 = 0,  /* IEEE binary16 */
     HGEMM_BF16 = 1, /* bfloat16 */
-    HGEMM_F32 = 2   /* IEEE binary32 (output only) */
+    HGEMM_F32 = 2,  /* IEEE binary32 (output only) */
+    HGEMM_E4M3 = 3, /* 8-bit float, 1-4-3 bits, bias 7, no infinities, S.1111.111 is NaN
+                       (input only) */
+    HGEMM_E5M2 = 4  /* 8-bit float, 1-5-2 bits, bias 15, IEEE-style infinities and NaNs
+                       (input only) */
 } hgemm_dtype_t;
 
 typedef enum {
@@ -134,8 +138,24 @@ typedef struct {
  *                    has rows to read or write).
  *   batch >= 1; strideA/B/C (elements) are used only when batch > 1 and must
  *                    then be >= 0.
- *   dtype_in  in {HGEMM_F16, HGEMM_BF16} (applies to both A and B).
+ *   dtype_in  in {HGEMM_F16, HGEMM_BF16, HGEMM_E4M3, HGEMM_E5M2} (applies to
+ *                    both A and B).
  *   dtype_out in {HGEMM_F32, HGEMM_F16, HGEMM_BF16}.
+ * 8-bit inputs (HGEMM_E4M3 / HGEMM_E5M2) are multiplied exactly and summed in
+ * fp32 like the 16-bit ones, at the tensor cores' 8-bit rate: the
+ * "tensor-cores-cutlass-and-cute" page lists FP8 e4m3 with fp32
+ * accumulation among the tensor-core input types, notes that an instruction
+ * consumes a fixed number of bytes along K (so twice the K of a 16-bit type),
+ * and takes K blocks of 128 one-byte elements where bf16 takes 64 (its
+ * section on vLLM's FP8 kernels).  They take the
+ * layout those units read without a copy, and anything else is
+ * HGEMM_ERR_UNSUPPORTED: B stored N x K (options.trans_b = 1, so both
+ * operands are contiguous along K); lda and ldb multiples of 16; with
+ * batch > 1, strideA and strideB multiples of 16; A and B 16-byte aligned
+ * (checked by hgemm_run); no force_repack; tile_n 0, 128 or 256,
+ * pair_k_blocks 0 or 2, skinny_tile_n 0, 128 or 256.  Per-tensor or
+ * per-channel dequantisation scales go in the epilogue (alpha, row_scale,
+ * col_scale of hgemm_run_ex).
  * Validation needs no GPU; on valid arguments the current device must be an
  * sm_103 GPU (else HGEMM_ERR_NO_DEVICE).  Device workspace is allocated here.
  * On success *plan receives a handle the caller must destroy. */

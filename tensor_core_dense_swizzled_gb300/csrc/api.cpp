@@ -64,6 +64,10 @@ inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 inline int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int out_bytes(hgemm_dtype_t d) { return d == HGEMM_F32 ? 4 : 2; }
+inline bool is_f8(hgemm_dtype_t d) { return d == HGEMM_E4M3 || d == HGEMM_E5M2; }
+inline int in_bytes(hgemm_dtype_t d) { return is_f8(d) ? 1 : 2; }
+// Elements per K block: 128 bytes of the input type (one swizzled row).
+inline int kblock(hgemm_dtype_t d) { return is_f8(d) ? 128 : 64; }
 inline int out_type(hgemm_dtype_t d) {
     return d == HGEMM_F32 ? hg::OUT_F32 : (d == HGEMM_BF16 ? hg::OUT_BF16 : hg::OUT_F16);
 }
@@ -97,25 +101,26 @@ hgemm_status_t encode_3d(CUtensorMap *map, const void *base, CUtensorMapDataType
     return HGEMM_OK;
 }
 
-// 4-D view of a row-major rows x cols 16-bit operand (cols a multiple of 64)
-// that splits the contiguous dimension in 64-element blocks: dims (64, rows,
-// cols / 64, batch), strides ld (rows), 128 bytes (blocks), stride (batch);
-// box 64 x box_rows x box_blocks; 128-byte swizzle, zero fill outside.
-// A (M x K) with box_blocks = K blocks per stage and B (K x N) with
-// box_rows = K rows per stage, box_blocks = 64-column blocks per CTA.
+// 4-D view of a row-major rows x cols operand whose contiguous dimension is
+// a multiple of blk = 128 bytes / esize elements (64 16-bit or 128 8-bit),
+// split in blk-element blocks: dims (blk, rows, cols / blk, batch), strides
+// ld (rows), 128 bytes (blocks), stride (batch); box blk x box_rows x
+// box_blocks; 128-byte swizzle, zero fill outside.  A (M x K) with
+// box_blocks = K blocks per stage and B (K x N) with box_rows = K rows per
+// stage, box_blocks = 64-column blocks per CTA.
 hgemm_status_t encode_split_4d(CUtensorMap *map, const void *base, CUtensorMapDataType dt,
-                               int64_t cols, int64_t rows, int64_t batch, int64_t ld,
+                               int esize, int64_t cols, int64_t rows, int64_t batch, int64_t ld,
                                int64_t stride, uint32_t box_rows, uint32_t box_blocks) {
     auto fn = encode_fn();
     if (!fn) return fail(HGEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const int esize = 2;
+    const int64_t blk = 128 / esize;
     int64_t bstride = stride * esize;
     if (batch == 1) bstride = round_up(rows * ld * esize, 16);
-    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64),
-                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(blk), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(cols / blk), static_cast<cuuint64_t>(batch)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(ld * esize), 128,
                              static_cast<cuuint64_t>(bstride)};
-    cuuint32_t box[4] = {64, box_rows, box_blocks, 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(blk), box_rows, box_blocks, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -176,8 +181,9 @@ int64_t span_elems(int64_t rows, int64_t cols, int64_t ld, int64_t batch, int64_
 hgemm_status_t validate(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                         int64_t batch, int64_t sA, int64_t sB, int64_t sC, bool trans_b, hgemm_dtype_t din,
                         hgemm_dtype_t dout) {
-    if (din != HGEMM_F16 && din != HGEMM_BF16)
-        return fail(HGEMM_ERR_INVALID_ARG, "dtype_in must be HGEMM_F16 or HGEMM_BF16 (got %d)",
+    if (din != HGEMM_F16 && din != HGEMM_BF16 && !is_f8(din))
+        return fail(HGEMM_ERR_INVALID_ARG,
+                    "dtype_in must be HGEMM_F16, HGEMM_BF16, HGEMM_E4M3 or HGEMM_E5M2 (got %d)",
                     static_cast<int>(din));
     if (dout != HGEMM_F16 && dout != HGEMM_BF16 && dout != HGEMM_F32)
         return fail(HGEMM_ERR_INVALID_ARG, "dtype_out must be HGEMM_F32, HGEMM_F16 or HGEMM_BF16 (got %d)",
@@ -204,6 +210,17 @@ hgemm_status_t validate(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
                     static_cast<long long>(sC));
     const int64_t tiles = batch * ceil_div(M, 128) * ceil_div(N, 128);
     if (tiles > kMaxDim) return fail(HGEMM_ERR_UNSUPPORTED, "too many output tiles");
+    if (is_f8(din) && M > 0 && N > 0 && K > 0) {
+        // 8-bit operands are read in place (no aligned copy is made): both
+        // contiguous along K, rows and batches on 16-byte boundaries
+        if (!trans_b)
+            return fail(HGEMM_ERR_UNSUPPORTED, "8-bit inputs need B stored N x K (trans_b = 1)");
+        if (lda % 16 != 0 || ldb % 16 != 0)
+            return fail(HGEMM_ERR_UNSUPPORTED, "8-bit inputs need lda and ldb multiples of 16 (got %lld, %lld)",
+                        static_cast<long long>(lda), static_cast<long long>(ldb));
+        if (batch > 1 && (sA % 16 != 0 || sB % 16 != 0))
+            return fail(HGEMM_ERR_UNSUPPORTED, "8-bit inputs need strideA and strideB multiples of 16");
+    }
     return HGEMM_OK;
 }
 
@@ -243,11 +260,12 @@ int choose_split(int64_t work_tiles, int num_kb, int num_sms) {
 // its width: on GB300 at 4096^3, 128 x 224 tiles (4 B blocks, 4 waves) ran
 // at 98.3 us against 91.1 us for 128 x 256 (3.4 waves), and 128 x 192 at
 // 104.5 us.  Ties go to the wider tile.
-int choose_tile_n(int64_t batch, int64_t M, int64_t N, int sms) {
+int choose_tile_n(int64_t batch, int64_t M, int64_t N, int sms, bool f8) {
     static const int cands[] = {256, 224, 192, 128};
     int best = 256;
     double best_t = 1e300;
     for (int bn : cands) {
+        if (f8 && bn != 256 && bn != 128) continue;  // the 8-bit kernels built
         const int64_t tiles = batch * ceil_div(M, 128) * ceil_div(N, bn);
         const int64_t waves = ceil_div(tiles, sms);
         const double t = static_cast<double>(waves) * (16 + 8 * ((bn + 63) / 64));
@@ -303,8 +321,8 @@ hgemm_status_t alloc_workspace(hgemm_plan_s *p) {
         // B stored K x N, or N x K with trans_b: rows x cols of the stored matrix
         p->ldb_p = round_up(p->opt.trans_b ? p->K : p->N, 8);
         p->sB_p = (p->opt.trans_b ? p->N : p->K) * p->ldb_p;
-        p->apack_bytes = static_cast<size_t>(p->batch * p->sA_p * 2);
-        p->bpack_bytes = static_cast<size_t>(p->batch * p->sB_p * 2);
+        p->apack_bytes = static_cast<size_t>(p->batch * p->sA_p * in_bytes(p->din));
+        p->bpack_bytes = static_cast<size_t>(p->batch * p->sB_p * in_bytes(p->din));
     }
     p->ws_bytes = off;
     p->off_apack = p->off_bpack = 0;
@@ -402,6 +420,16 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         return fail(HGEMM_ERR_INVALID_ARG, "skinny_prefetch must be in [-1, 64]");
     if (opt.cta_pair == 1 && opt.tile_n != 0 && opt.tile_n != 256 && opt.tile_n != 224)
         return fail(HGEMM_ERR_INVALID_ARG, "CTA-pair tiles are 256 x 256 or 256 x 224 (tile_n 0, 256 or 224)");
+    if (is_f8(din) && M > 0 && N > 0 && K > 0) {
+        if (opt.force_repack)
+            return fail(HGEMM_ERR_UNSUPPORTED, "8-bit inputs are never copied (force_repack)");
+        if (opt.tile_n != 0 && opt.tile_n != 128 && opt.tile_n != 256)
+            return fail(HGEMM_ERR_UNSUPPORTED, "8-bit inputs: tile_n must be 0, 128 or 256");
+        if (opt.pair_k_blocks == 1)
+            return fail(HGEMM_ERR_UNSUPPORTED, "8-bit inputs: pair_k_blocks must be 0 or 2");
+        if (opt.skinny_tile_n != 0 && opt.skinny_tile_n != 128 && opt.skinny_tile_n != 256)
+            return fail(HGEMM_ERR_UNSUPPORTED, "8-bit inputs: skinny_tile_n must be 0, 128 or 256");
+    }
     if (opt.force_path == HGEMM_PATH_SKINNY && M > 32)
         return fail(HGEMM_ERR_UNSUPPORTED, "the skinny path handles M <= 32 (got %lld)", static_cast<long long>(M));
 
@@ -440,8 +468,9 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
     }
 
     const int ob = out_bytes(dout);
-    p->ld_repack_a = (lda * 2) % 16 != 0 || (batch > 1 && (p->sA * 2) % 16 != 0);
-    p->ld_repack_b = (ldb * 2) % 16 != 0 || (batch > 1 && (p->sB * 2) % 16 != 0);
+    const int ib = in_bytes(din);
+    p->ld_repack_a = (lda * ib) % 16 != 0 || (batch > 1 && (p->sA * ib) % 16 != 0);
+    p->ld_repack_b = (ldb * ib) % 16 != 0 || (batch > 1 && (p->sB * ib) % 16 != 0);
     // TMA stores write whole 16-byte chunks: a row whose byte length is not a
     // multiple of 16 would have the elements after column N-1 overwritten (up
     // to the next 16-byte boundary, past the end of the last row too), so the
@@ -449,9 +478,9 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
     p->ldc_tma = (ldc * ob) % 16 == 0 && (N * ob) % 16 == 0 &&
                  (batch == 1 || (p->sC * ob) % 16 == 0) && !opt.force_generic_store;
 
-    const int num_kb = static_cast<int>(ceil_div(K, 64));
+    const int num_kb = static_cast<int>(ceil_div(K, kblock(din)));
     if (p->path == HGEMM_PATH_TILED) {
-        p->bn = opt.tile_n ? opt.tile_n : choose_tile_n(batch, M, N, sms);
+        p->bn = opt.tile_n ? opt.tile_n : choose_tile_n(batch, M, N, sms, is_f8(din));
         const int64_t tiles = batch * ceil_div(M, 128) * ceil_div(N, p->bn);
         p->grid = static_cast<int>(tiles < sms ? tiles : sms);
         p->pair = false;
@@ -496,7 +525,7 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
                 //    ranges run at unrelated K steps and lose L2 reuse.
                 const int64_t T = ptiles % max_pairs;
                 p->pair_ks = opt.pair_k_blocks ? opt.pair_k_blocks : 2;
-                const int64_t num_steps = ceil_div(ceil_div(K, 64), p->pair_ks);
+                const int64_t num_steps = ceil_div(num_kb, p->pair_ks);
                 const bool can_sk = T > 0 && ptiles >= max_pairs;
                 const bool can_halves = T > 0 && 2 * T <= max_pairs && num_steps >= 2;
                 // first-wave dealing: the T * num_steps steps cover every pair
@@ -528,6 +557,7 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
     } else if (p->path == HGEMM_PATH_SKINNY) {
         p->nu = M <= 16 ? 16 : 32;
         p->nb = opt.skinny_tile_n ? opt.skinny_tile_n / 64 : hg::pick_skinny_nb(N, batch, sms);
+        if (is_f8(din) && p->nb != 2 && p->nb != 4) p->nb = 4;  // the 8-bit kernels built
         const int64_t work = batch * ceil_div(N, 64 * p->nb);
         const int64_t steps = work * num_kb;
         // Deal mode (stream-K, on request only): every SM streams an equal
@@ -566,8 +596,12 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
 
 hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *C, bool tma_store) {
     if (p->maps_ok && A == p->mA && B == p->mB && C == p->mC) return HGEMM_OK;
-    const CUtensorMapDataType dt =
-        p->din == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType dt = is_f8(p->din)         ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : p->din == HGEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // every staged row is one 128-byte K block: 64 16-bit or 128 8-bit elements
+    const int ib = in_bytes(p->din);
+    const int bke = kblock(p->din);
     const bool packed_a = p->have_apack && A == p->ws + p->off_apack;
     const bool packed_b = p->have_bpack && B == p->ws + p->off_bpack;
     const int64_t lda = packed_a ? p->lda_p : p->lda;
@@ -584,20 +618,23 @@ hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *
         // be a multiple of 64.
         const bool tb = p->opt.trans_b != 0;
         p->wide = false;
-        if (p->pair && p->bn == 256 && p->K % 64 == 0 && (tb || p->N % 64 == 0)) {
-            p->wide = encode_split_4d(&p->tmA, A, dt, p->K, p->M, p->batch, lda, sA, 128,
+        if (p->pair && p->bn == 256 && p->K % bke == 0 && (tb || p->N % 64 == 0)) {
+            p->wide = encode_split_4d(&p->tmA, A, dt, ib, p->K, p->M, p->batch, lda, sA, 128,
                                       static_cast<uint32_t>(p->pair_ks)) == HGEMM_OK &&
-                      (tb ? encode_split_4d(&p->tmB, B, dt, p->K, p->N, p->batch, ldb, sB, 128,
+                      (tb ? encode_split_4d(&p->tmB, B, dt, ib, p->K, p->N, p->batch, ldb, sB, 128,
                                             static_cast<uint32_t>(p->pair_ks))
-                          : encode_split_4d(&p->tmB, B, dt, p->N, p->K, p->batch, ldb, sB,
+                          : encode_split_4d(&p->tmB, B, dt, ib, p->N, p->K, p->batch, ldb, sB,
                                             static_cast<uint32_t>(64 * p->pair_ks), 2)) == HGEMM_OK;
         }
         if (!p->wide) {
-            st = encode_3d(&p->tmA, A, dt, 2, p->K, p->M, p->batch, lda, sA, 64, 128);
+            st = encode_3d(&p->tmA, A, dt, ib, p->K, p->M, p->batch, lda, sA,
+                           static_cast<uint32_t>(bke), 128);
             if (st != HGEMM_OK) return st;
-            // 64 x 64 boxes of B either way: (n, k) MN-major, (k, n) K-major
-            st = tb ? encode_3d(&p->tmB, B, dt, 2, p->K, p->N, p->batch, ldb, sB, 64, 64)
-                    : encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64);
+            // boxes of 64 rows of B either way: (n, k) MN-major 64 x 64, (k, n)
+            // K-major one K block x 64
+            st = tb ? encode_3d(&p->tmB, B, dt, ib, p->K, p->N, p->batch, ldb, sB,
+                                static_cast<uint32_t>(bke), 64)
+                    : encode_3d(&p->tmB, B, dt, ib, p->N, p->K, p->batch, ldb, sB, 64, 64);
             if (st != HGEMM_OK) return st;
         }
         if (tma_store) {
@@ -613,15 +650,16 @@ hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *
             std::memset(&p->tmC, 0, sizeof(p->tmC));
         }
     } else {
-        st = encode_3d(&p->tmA, A, dt, 2, p->K, p->M, p->batch, lda, sA, 64,
+        st = encode_3d(&p->tmA, A, dt, ib, p->K, p->M, p->batch, lda, sA, static_cast<uint32_t>(bke),
                        static_cast<uint32_t>(p->nu));
         if (st != HGEMM_OK) return st;
         // streamed once: 128-byte L2 fills (256-byte promotion measured 1.3 %
         // slower on 8 x 28672 x 4096)
         st = p->opt.trans_b
-                 ? encode_3d(&p->tmB, B, dt, 2, p->K, p->N, p->batch, ldb, sB, 64, 64,
-                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)
-                 : encode_3d(&p->tmB, B, dt, 2, p->N, p->K, p->batch, ldb, sB, 64, 64,
+                 ? encode_3d(&p->tmB, B, dt, ib, p->K, p->N, p->batch, ldb, sB,
+                             static_cast<uint32_t>(bke), 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B)
+                 : encode_3d(&p->tmB, B, dt, ib, p->N, p->K, p->batch, ldb, sB, 64, 64,
                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
         if (st != HGEMM_OK) return st;
         std::memset(&p->tmC, 0, sizeof(p->tmC));
@@ -652,8 +690,11 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "zero-fill launch");
     }
     if (!A || !B) return fail(HGEMM_ERR_INVALID_ARG, "A or B is NULL");
-    if ((reinterpret_cast<uintptr_t>(A) & 1) || (reinterpret_cast<uintptr_t>(B) & 1))
+    if (in_bytes(p->din) == 2 &&
+        ((reinterpret_cast<uintptr_t>(A) & 1) || (reinterpret_cast<uintptr_t>(B) & 1)))
         return fail(HGEMM_ERR_INVALID_ARG, "A or B is not element-aligned");
+    if (is_f8(p->din) && (!aligned16(A) || !aligned16(B)))
+        return fail(HGEMM_ERR_UNSUPPORTED, "8-bit A and B must be 16-byte aligned (no copy is made)");
 
     const bool pack_a = p->ld_repack_a || p->opt.force_repack || !aligned16(A);
     const bool pack_b = p->ld_repack_b || p->opt.force_repack || !aligned16(B);
@@ -680,6 +721,8 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     }
     int32_t *err = reinterpret_cast<int32_t *>(p->ws);
     const uint32_t bf = p->din == HGEMM_BF16 ? 1u : 0u;
+    const bool f8 = is_f8(p->din);
+    const uint32_t f8fmt = p->din == HGEMM_E5M2 ? 1u : 0u;  // kind::f8f6f4 codes: E4M3 0, E5M2 1
     if (p->path == HGEMM_PATH_TILED) {
         const bool ts = p->ldc_tma && aligned16(C);
         st = encode_maps(p, Ae, Be, C, ts);
@@ -691,12 +734,14 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.batch = static_cast<int32_t>(p->batch);
         tp.num_m = static_cast<int32_t>(ceil_div(p->M, p->pair ? 256 : 128));
         tp.num_n = static_cast<int32_t>(ceil_div(p->N, p->bn));
-        tp.num_kb = static_cast<int32_t>(ceil_div(p->K, 64));
+        tp.num_kb = static_cast<int32_t>(ceil_div(p->K, kblock(p->din)));
         tp.tiles = tp.batch * tp.num_m * tp.num_n;
         tp.group_m = p->opt.group_m ? p->opt.group_m : 16;
         // B MN-major (stored K x N, N contiguous) or K-major (trans_b: N x K)
-        tp.idesc = hg::idesc_f16(bf, 0, p->opt.trans_b ? 0 : 1, p->pair ? 256 : 128,
-                                 static_cast<uint32_t>(p->bn));
+        tp.idesc = f8 ? hg::idesc_f8(f8fmt, f8fmt, 0, 0, p->pair ? 256 : 128, static_cast<uint32_t>(p->bn))
+                      : hg::idesc_f16(bf, 0, p->opt.trans_b ? 0 : 1, p->pair ? 256 : 128,
+                                      static_cast<uint32_t>(p->bn));
+        tp.f8 = f8 ? 1 : 0;
         tp.b_kmajor = p->opt.trans_b ? 1 : 0;
         tp.C = C;
         tp.ep = ep;
@@ -728,7 +773,7 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     sp.K = static_cast<int32_t>(p->K);
     sp.batch = static_cast<int32_t>(p->batch);
     sp.num_tiles = static_cast<int32_t>(ceil_div(p->N, 64 * p->nb));
-    sp.num_kb = static_cast<int32_t>(ceil_div(p->K, 64));
+    sp.num_kb = static_cast<int32_t>(ceil_div(p->K, kblock(p->din)));
     sp.split = p->split;
     sp.kb_per_split = p->kb_per;
     sp.units = sp.batch * sp.split * sp.num_tiles;
@@ -738,7 +783,9 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     sp.prefetch = p->opt.skinny_prefetch > 0 ? p->opt.skinny_prefetch : 0;
     // the MMA's A operand is B^T: MN-major from a K x N B, K-major from an
     // N x K B (trans_b)
-    sp.idesc = hg::idesc_f16(bf, p->opt.trans_b ? 0 : 1, 0, 128, static_cast<uint32_t>(p->nu));
+    sp.idesc = f8 ? hg::idesc_f8(f8fmt, f8fmt, 0, 0, 128, static_cast<uint32_t>(p->nu))
+                  : hg::idesc_f16(bf, p->opt.trans_b ? 0 : 1, 0, 128, static_cast<uint32_t>(p->nu));
+    sp.f8 = f8 ? 1 : 0;
     sp.b_kmajor = p->opt.trans_b ? 1 : 0;
     sp.C = C;
     sp.ep = ep;
@@ -814,10 +861,11 @@ hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void 
     if (!C_host || (p->path != HGEMM_PATH_ZERO_FILL && (!A_host || !B_host)))
         return fail(HGEMM_ERR_INVALID_ARG, "host pointer is NULL");
     const int ob = out_bytes(p->dout);
-    const size_t a_bytes = static_cast<size_t>(span_elems(p->M, p->K, p->lda, p->batch, p->sA)) * 2;
+    const int ib = in_bytes(p->din);
+    const size_t a_bytes = static_cast<size_t>(span_elems(p->M, p->K, p->lda, p->batch, p->sA)) * ib;
     const size_t b_bytes =
         static_cast<size_t>(p->opt.trans_b ? span_elems(p->N, p->K, p->ldb, p->batch, p->sB)
-                                           : span_elems(p->K, p->N, p->ldb, p->batch, p->sB)) * 2;
+                                           : span_elems(p->K, p->N, p->ldb, p->batch, p->sB)) * ib;
     const size_t c_bytes = static_cast<size_t>(span_elems(p->M, p->N, p->ldc, p->batch, p->sC)) * ob;
     cudaError_t e;
     auto grow = [&](char **buf, size_t *have, size_t want) -> cudaError_t {
@@ -888,13 +936,13 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     if (!plan || !info) return fail(HGEMM_ERR_INVALID_ARG, "plan or info is NULL");
     hgemm_plan_info_t r{};
     r.path = plan->path;
-    r.tile_k = 64;
+    r.tile_k = kblock(plan->din);
     r.split_k = 1;
     if (plan->path == HGEMM_PATH_TILED) {
         r.tile_m = plan->pair ? 256 : 128;
         r.tile_n = plan->bn;
         r.stages = plan->pair ? hg::pair_stages(plan->pair_ks) : hg::tiled_stages(plan->bn);
-        if (plan->pair) r.tile_k = 64 * plan->pair_ks;
+        if (plan->pair) r.tile_k = kblock(plan->din) * plan->pair_ks;
         r.tma_store = plan->ldc_tma ? 1 : 0;
     } else if (plan->path == HGEMM_PATH_SKINNY) {
         r.tile_m = plan->nu;
@@ -915,7 +963,8 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
                  : plan->path == HGEMM_PATH_SKINNY && plan->skinny_deal ? 1
                                                                        : 0;
     r.wide_boxes = plan->path == HGEMM_PATH_TILED && plan->pair && plan->bn == 256 &&
-                           plan->K % 64 == 0 && (plan->opt.trans_b || plan->N % 64 == 0) &&
+                           plan->K % kblock(plan->din) == 0 &&
+                           (plan->opt.trans_b || plan->N % 64 == 0) &&
                            (plan->wide || !plan->maps_ok)
                        ? 1
                        : 0;

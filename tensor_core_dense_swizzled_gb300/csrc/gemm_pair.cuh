@@ -251,10 +251,13 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t pari
     return false;
 }
 
-template <int PN, int KS, int OUT, bool TMA_STORE, bool EPI>
+// F8: 8-bit inputs (kind::f8f6f4), K blocks of 128 elements (the same 128
+// bytes per staged row), both operands K-major.
+template <int PN, int KS, int OUT, bool TMA_STORE, bool EPI, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     hgemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const TiledParams p) {
+    constexpr int BKE = F8 ? 128 : 64;  // elements per K block (128 bytes either way)
     using Cfg = PairCfg<PN, KS>;
     constexpr int BNH = Cfg::BNH;
     extern __shared__ uint8_t smem_raw[];
@@ -356,14 +359,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int s = 0; s < KS; ++s) {
                             if (s >= nsub) break;
                             const int kb = ks * KS + s;
-                            tma_load_3d_pair(dA + s * Cfg::A_SUB, &tmA, fb, kb * BK, m0, b);
+                            tma_load_3d_pair(dA + s * Cfg::A_SUB, &tmA, fb, kb * BKE, m0, b);
                             if (p.b_kmajor) {
                                 // K-major: 64-row blocks j of K block s stacked, so
                                 // the CTA's 128 rows of B are contiguous
 #pragma unroll
                                 for (int j = 0; j < Cfg::B_BLOCKS; ++j)
                                     tma_load_3d_pair(dB + s * Cfg::B_SUB + j * Cfg::B_BLOCK, &tmB, fb,
-                                                     kb * BK, n0 + j * 64, b);
+                                                     kb * BKE, n0 + j * 64, b);
                             } else {
 #pragma unroll
                                 for (int j = 0; j < Cfg::B_BLOCKS; ++j)
@@ -447,7 +450,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const uint64_t bd =
                                 b_st + (bk ? ((s * Cfg::B_SUB + k * 32) >> 4)
                                            : ((s * Cfg::B_BLOCK + k * 16 * 128) >> 4));
-                            umma_f16_pair(d_tmem, ad, bd, p.idesc, (s > 0 || k > 0) ? 1u : acc0);
+                            if constexpr (F8)
+                                umma_f8_pair(d_tmem, ad, bd, p.idesc, (s > 0 || k > 0) ? 1u : acc0);
+                            else
+                                umma_f16_pair(d_tmem, ad, bd, p.idesc, (s > 0 || k > 0) ? 1u : acc0);
                         }
                     }
                     umma_commit_pair(empty(stage), 0x3);
@@ -617,10 +623,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int PN, int KS, int OUT, bool TS, bool EPI>
+template <int PN, int KS, int OUT, bool TS, bool EPI, bool F8 = false>
 cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const TiledParams &p, int grid, cudaStream_t stream) {
-    auto kern = hgemm_pair_kernel<PN, KS, OUT, TS, EPI>;
+    auto kern = hgemm_pair_kernel<PN, KS, OUT, TS, EPI, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PairCfg<PN, KS>::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
@@ -650,6 +656,15 @@ cudaError_t launch_pair_typed(int pn, int ks, bool ts, const CUtensorMap &tmA,
                               int grid, cudaStream_t s) {
     const int v = (pn == 256 ? 0 : 8) | (ks == 2 ? 0 : 4) | (ts ? 0 : 2) | (p.ep.on ? 1 : 0);
     if ((pn != 256 && pn != 224) || (ks != 1 && ks != 2)) return cudaErrorInvalidValue;
+    if (p.f8) {  // 8-bit inputs: 256 x 256 tiles, two K blocks per stage only
+        switch (v) {
+            case 0: return launch_impl<256, 2, OUT, true, false, true>(tmA, tmB, tmC, p, grid, s);
+            case 1: return launch_impl<256, 2, OUT, true, true, true>(tmA, tmB, tmC, p, grid, s);
+            case 2: return launch_impl<256, 2, OUT, false, false, true>(tmA, tmB, tmC, p, grid, s);
+            case 3: return launch_impl<256, 2, OUT, false, true, true>(tmA, tmB, tmC, p, grid, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (v) {
         case 0: return launch_impl<256, 2, OUT, true, false>(tmA, tmB, tmC, p, grid, s);
         case 1: return launch_impl<256, 2, OUT, true, true>(tmA, tmB, tmC, p, grid, s);

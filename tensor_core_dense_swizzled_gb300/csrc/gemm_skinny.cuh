@@ -153,10 +153,13 @@ struct SkinnySched {
     }
 };
 
-template <int NU, int NB, int OUT, bool EPI>
+// F8: 8-bit inputs (kind::f8f6f4), K blocks of 128 elements, both operands
+// K-major.
+template <int NU, int NB, int OUT, bool EPI, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     hgemm_skinny_kernel(const __grid_constant__ CUtensorMap tmX,
                         const __grid_constant__ CUtensorMap tmW, const SkinnyParams p) {
+    constexpr int BKE = F8 ? 128 : 64;  // elements per K block (128 bytes either way)
     using Cfg = SkinnyCfg<NU, NB>;
     constexpr int NT = Cfg::NT;
     constexpr int UW = NB * 64;  // columns of C per work unit
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int kb = w.kb0; kb < w.kb1 && n < p.prefetch; ++kb, ++n)
                         for (int j = 0; j < Cfg::W_BLOCKS; ++j)
                             if (p.b_kmajor)
-                                tma_prefetch_3d(&tmW, kb * BK, w.nt * UW + j * 64, w.b);
+                                tma_prefetch_3d(&tmW, kb * BKE, w.nt * UW + j * 64, w.b);
                             else
                                 tma_prefetch_3d(&tmW, w.nt * UW + j * 64, kb * BK, w.b);
                 }
@@ -253,12 +256,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // stored N x K (blocks stack into rows = columns of C)
                         if (p.b_kmajor)
                             tma_load_3d(sW + stage * Cfg::W_BYTES + j * Cfg::W_BLOCK, &tmW,
-                                        full(stage), kb * BK, nt * UW + j * 64, b);
+                                        full(stage), kb * BKE, nt * UW + j * 64, b);
                         else
                             tma_load_3d(sW + stage * Cfg::W_BYTES + j * Cfg::W_BLOCK, &tmW,
                                         full(stage), nt * UW + j * 64, kb * BK, b);
                     }
-                    tma_load_3d(sX + stage * Cfg::X_BYTES, &tmX, full(stage), kb * BK, 0, b);
+                    tma_load_3d(sX + stage * Cfg::X_BYTES, &tmX, full(stage), kb * BKE, 0, b);
                     ++issued;
                     if (++stage == Cfg::STAGES) {
                         stage = 0;
@@ -317,7 +320,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     ? sdesc_sw128(w0 + 2 * j * Cfg::W_BLOCK + k * 32, 16, 1024)
                                     : sdesc_sw128(w0 + 2 * j * Cfg::W_BLOCK + k * 16 * 128,
                                                   Cfg::W_BLOCK, 1024);
-                            umma_f16(d0 + j * NU, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                            if constexpr (F8)
+                                umma_f8(d0 + j * NU, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                            else
+                                umma_f16(d0 + j * NU, ad, bd, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                         }
                     }
                     umma_commit(empty(stage));
@@ -436,10 +442,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int NU, int NB, int OUT, bool EPI>
+template <int NU, int NB, int OUT, bool EPI, bool F8 = false>
 cudaError_t launch_impl(const CUtensorMap &tmX, const CUtensorMap &tmW, const SkinnyParams &p,
                         int grid, cudaStream_t stream) {
-    auto kern = hgemm_skinny_kernel<NU, NB, OUT, EPI>;
+    auto kern = hgemm_skinny_kernel<NU, NB, OUT, EPI, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SkinnyCfg<NU, NB>::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
@@ -450,6 +456,13 @@ cudaError_t launch_impl(const CUtensorMap &tmX, const CUtensorMap &tmW, const Sk
 template <int NU, int NB, int OUT>
 cudaError_t launch_epi(const CUtensorMap &tmX, const CUtensorMap &tmW, const SkinnyParams &p,
                        int grid, cudaStream_t s) {
+    if constexpr (NB == 2 || NB == 4) {  // 8-bit inputs: 128- and 256-column units
+        if (p.f8)
+            return p.ep.on ? launch_impl<NU, NB, OUT, true, true>(tmX, tmW, p, grid, s)
+                           : launch_impl<NU, NB, OUT, false, true>(tmX, tmW, p, grid, s);
+    } else {
+        if (p.f8) return cudaErrorInvalidValue;
+    }
     return p.ep.on ? launch_impl<NU, NB, OUT, true>(tmX, tmW, p, grid, s)
                    : launch_impl<NU, NB, OUT, false>(tmX, tmW, p, grid, s);
 }

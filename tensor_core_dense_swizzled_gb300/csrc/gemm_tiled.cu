@@ -85,11 +85,14 @@ __device__ __forceinline__ void tile_coords(const TiledParams &p, int t, int &b,
     grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);
 }
 
-template <int BN, int OUT, bool TMA_STORE, bool EPI>
+// F8: 8-bit inputs (kind::f8f6f4), K blocks of 128 elements, both operands
+// K-major.
+template <int BN, int OUT, bool TMA_STORE, bool EPI, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     hgemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const TiledParams p) {
+    constexpr int BKE = F8 ? 128 : 64;  // elements per K block (128 bytes either way)
     using Cfg = TiledCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -159,14 +162,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full(stage), Cfg::TX_BYTES);
-                    tma_load_3d(sA + stage * Cfg::A_BYTES, &tmA, full(stage), kb * BK, mt * BM, b);
+                    tma_load_3d(sA + stage * Cfg::A_BYTES, &tmA, full(stage), kb * BKE, mt * BM, b);
                     // 64 x 64 blocks of B: (n, k) MN-major, or (k, n) K-major
                     // when B is stored N x K (the blocks stack into BN rows)
 #pragma unroll
                     for (int j = 0; j < Cfg::B_BLOCKS; ++j) {
                         if (p.b_kmajor)
                             tma_load_3d(sB + stage * Cfg::B_BYTES + j * Cfg::B_BLOCK, &tmB,
-                                        full(stage), kb * BK, nt * BN + j * 64, b);
+                                        full(stage), kb * BKE, nt * BN + j * 64, b);
                         else
                             tma_load_3d(sB + stage * Cfg::B_BYTES + j * Cfg::B_BLOCK, &tmB,
                                         full(stage), nt * BN + j * 64, kb * BK, b);
@@ -221,7 +224,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t bd = p.b_kmajor
                                                 ? sdesc_sw128(b0 + k * 32, 16, 1024)
                                                 : sdesc_sw128(b0 + k * 16 * 128, Cfg::B_BLOCK, 1024);
-                        umma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                        if constexpr (F8)
+                            umma_f8(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                        else
+                            umma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     umma_commit(empty(stage));
                     if (++stage == Cfg::STAGES) {
@@ -273,10 +279,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int BN, int OUT, bool TS, bool EPI>
+template <int BN, int OUT, bool TS, bool EPI, bool F8 = false>
 cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const TiledParams &p, int grid, cudaStream_t stream) {
-    auto kern = hgemm_tiled_kernel<BN, OUT, TS, EPI>;
+    auto kern = hgemm_tiled_kernel<BN, OUT, TS, EPI, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TiledCfg<BN>::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
@@ -287,7 +293,19 @@ cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
 template <int BN, int OUT>
 cudaError_t launch_ts(bool ts, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const CUtensorMap &tmC, const TiledParams &p, int grid, cudaStream_t s) {
-    // p.ep.on: the fused-epilogue variant
+    // p.f8: 8-bit inputs (tile widths 128 and 256 only); p.ep.on: the
+    // fused-epilogue variant
+    if constexpr (BN == 128 || BN == 256) {
+        if (p.f8) {
+            if (p.ep.on)
+                return ts ? launch_impl<BN, OUT, true, true, true>(tmA, tmB, tmC, p, grid, s)
+                          : launch_impl<BN, OUT, false, true, true>(tmA, tmB, tmC, p, grid, s);
+            return ts ? launch_impl<BN, OUT, true, false, true>(tmA, tmB, tmC, p, grid, s)
+                      : launch_impl<BN, OUT, false, false, true>(tmA, tmB, tmC, p, grid, s);
+        }
+    } else {
+        if (p.f8) return cudaErrorInvalidValue;
+    }
     if (p.ep.on)
         return ts ? launch_impl<BN, OUT, true, true>(tmA, tmB, tmC, p, grid, s)
                   : launch_impl<BN, OUT, false, true>(tmA, tmB, tmC, p, grid, s);

@@ -21,6 +21,18 @@ constexpr uint32_t idesc_f16(uint32_t ab_bf16, uint32_t a_mn, uint32_t b_mn,
            ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// Instruction descriptor of tcgen05.mma .kind::f8f6f4 with an fp32
+// accumulator: the same fields as idesc_f16, A / B formats 0 = E4M3,
+// 1 = E5M2.
+constexpr uint32_t idesc_f8(uint32_t a_fmt, uint32_t b_fmt, uint32_t a_mn, uint32_t b_mn,
+                            uint32_t m, uint32_t n) {
+    return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (a_mn << 15) | (b_mn << 16) |
+           ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Elements per 128-byte K block: 64 of a 16-bit type, 128 of an 8-bit one.
+constexpr int kblock_elems(bool f8) { return f8 ? 128 : 64; }
+
 // Fused epilogue of the final values of C (see hgemm_epilogue_t):
 // D = act(alpha * rs[i] * cs[j] * acc + beta * C_prev + bias[j]).  `on` = 0:
 // D = acc (nothing else is read).
@@ -67,6 +79,9 @@ struct TiledParams {
     // 1: B is stored N x K (K contiguous) and staged K-major; 0: K x N,
     // staged MN-major.
     int32_t b_kmajor;
+    // 1: 8-bit inputs (E4M3 / E5M2, both operands K-major); a K block is 128
+    // elements (num_kb counts those).
+    int32_t f8;
 };
 
 // Skinny kernel: C^T = B^T . A^T, NB x 64 output columns of C per work
@@ -98,6 +113,8 @@ struct SkinnyParams {
     // 1: B is stored N x K (K contiguous): the MMA's A operand (B^T) is
     // staged K-major, rows = columns of C; 0: K x N, staged MN-major.
     int32_t b_kmajor;
+    // 1: 8-bit inputs (K-major only); K blocks of 128 elements.
+    int32_t f8;
 };
 
 // Shared memory the tiled kernel needs for a given BN (bytes, incl. alignment slack).

@@ -13,7 +13,7 @@ import os
 import threading
 
 __all__ = [
-    "HGEMM_F16", "HGEMM_BF16", "HGEMM_F32", "HGEMM_PATH_EMPTY", "HGEMM_PATH_ZERO_FILL",
+    "HGEMM_F16", "HGEMM_BF16", "HGEMM_F32", "HGEMM_E4M3", "HGEMM_E5M2", "HGEMM_PATH_EMPTY", "HGEMM_PATH_ZERO_FILL",
     "HGEMM_PATH_TILED", "HGEMM_PATH_SKINNY", "HgemmError", "Options", "PlanInfo", "lib_path",
     "load", "hgemm_plan_create", "hgemm_plan_create_ex", "hgemm_run", "hgemm_run_host",
     "hgemm_check", "hgemm_plan_destroy", "hgemm_plan_get_info", "hgemm", "hgemm_cache_clear",
@@ -23,7 +23,7 @@ __all__ = [
     "STATUS",
 ]
 
-HGEMM_F16, HGEMM_BF16, HGEMM_F32 = 0, 1, 2
+HGEMM_F16, HGEMM_BF16, HGEMM_F32, HGEMM_E4M3, HGEMM_E5M2 = 0, 1, 2, 3, 4
 HGEMM_PATH_EMPTY, HGEMM_PATH_ZERO_FILL, HGEMM_PATH_TILED, HGEMM_PATH_SKINNY = 0, 1, 2, 3
 STATUS = {
     0: "HGEMM_OK", 1: "HGEMM_ERR_INVALID_ARG", 2: "HGEMM_ERR_UNSUPPORTED",

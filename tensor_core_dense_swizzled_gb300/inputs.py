@@ -21,7 +21,15 @@ name                        shape / values
 ``ragged4095_h``            the same inputs, fp16 out
 ``skinny``                  M=8, N=28672, K=4096 bf16; A N(0,1), B N(0,0.02), seed 4,
                             bf16 out
+``*_tn``                    the same draws with B stored N x K
+``square4096_fp8``          4096^3 E4M3, N(0,1), seed 1, B stored N x K, bf16 out
+``skinny_fp8``              8 x 28672 x 4096 E4M3; A N(0,1), B N(0,1), seed 4, B
+                            stored N x K, bf16 out
 ==========================  =========================================================
+
+8-bit draws are rounded by ``.to(torch.float8_e4m3fn / float8_e5m2)``; the
+distributions stay far inside both formats' ranges (448 and 57344), so no
+value saturates or overflows.
 """
 from __future__ import annotations
 
@@ -32,7 +40,8 @@ import torch
 
 __all__ = ["Workload", "WORKLOADS", "make_inputs", "make_random", "torch_dtype"]
 
-_TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+_TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+       "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
 def torch_dtype(name: str) -> torch.dtype:
@@ -46,7 +55,7 @@ class Workload:
     N: int
     K: int
     batch: int
-    dtype_in: str   # "f16" | "bf16"
+    dtype_in: str   # "f16" | "bf16" | "e4m3" | "e5m2"
     dtype_out: str  # "f32" | "f16" | "bf16"
     dist_a: str     # "int4" | "normal" | "uniform"
     dist_b: str
@@ -98,6 +107,11 @@ WORKLOADS = {
         Workload("batched_qk_tn", 1024, 1024, 128, 64, "bf16", "f32", "normal", "normal",
                  1.0 / math.sqrt(128.0), 1.0 / math.sqrt(128.0), 3, trans_b=True),
         Workload("square4096_tn", 4096, 4096, 4096, 1, "bf16", "bf16", "normal", "normal", 1.0, 1.0, 1,
+                 trans_b=True),
+        # 8-bit inputs (B stored N x K, the layout 8-bit tensor-core operands take)
+        Workload("square4096_fp8", 4096, 4096, 4096, 1, "e4m3", "bf16", "normal", "normal", 1.0, 1.0,
+                 1, trans_b=True),
+        Workload("skinny_fp8", 8, 28672, 4096, 1, "e4m3", "bf16", "normal", "normal", 1.0, 1.0, 4,
                  trans_b=True),
     ]
 }

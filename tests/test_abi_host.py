@@ -115,6 +115,39 @@ def test_bad_options_are_refused(lib):
     assert st == 2
 
 
+def test_fp8_layout_rules(lib):
+    """8-bit inputs are read in place: B must be stored N x K (trans_b),
+    rows and batch strides on 16-byte boundaries, and only the 8-bit tile
+    set; each breach is HGEMM_ERR_UNSUPPORTED, found before any device is
+    touched.  8-bit outputs do not exist (HGEMM_ERR_INVALID_ARG)."""
+    h = ctypes.c_void_p()
+    E4 = H.HGEMM_E4M3
+
+    def create(M, N, K, lda, ldb, batch=1, sA=0, sB=0, din=E4, dout=H.HGEMM_BF16, **kw):
+        opt = H.Options(**{"trans_b": 1, **kw})
+        return lib.hgemm_plan_create_ex(ctypes.byref(h), M, N, K, lda, ldb, N, batch, sA, sB,
+                                        M * N * batch, din, dout, ctypes.byref(opt))
+
+    assert create(64, 64, 64, 64, 64, trans_b=0) == 2
+    assert create(64, 64, 64, 72, 64) == 2          # lda not a multiple of 16
+    assert create(64, 64, 40, 48, 40) == 2          # ldb not a multiple of 16
+    assert create(64, 64, 64, 64, 64, batch=2, sA=64 * 64 + 8, sB=64 * 64) == 2
+    assert create(64, 64, 64, 64, 64, tile_n=192) == 2
+    assert create(64, 64, 64, 64, 64, pair_k_blocks=1) == 2
+    assert create(8, 64, 64, 64, 64, skinny_tile_n=192) == 2
+    assert create(64, 64, 64, 64, 64, force_repack=1) == 2
+    assert create(64, 64, 64, 64, 64, din=H.HGEMM_E5M2, trans_b=0) == 2
+    assert create(64, 64, 64, 64, 64, dout=H.HGEMM_E4M3) == 1
+    assert create(64, 64, 64, 64, 64, dout=H.HGEMM_E5M2) == 1
+    # K == 0 writes zeros whatever the layout; a well-formed request reaches
+    # the device check
+    import torch
+    if not torch.cuda.is_available():
+        assert create(64, 64, 0, 64, 64, trans_b=0) == 3
+        assert create(64, 64, 200, 208, 224) == 3
+        assert create(64, 64, 64, 64, 64, din=H.HGEMM_E5M2, batch=2, sA=64 * 64, sB=64 * 64) == 3
+
+
 def test_valid_request_without_gpu_reports_no_device(lib):
     import torch
     if torch.cuda.is_available():
