@@ -70,6 +70,9 @@ def _load():
             lib.oracle_decode_e5m2.restype = ctypes.c_double
             lib.oracle_decode_array.argtypes = [p, ctypes.c_int, i64, p]
             lib.oracle_decode_array.restype = None
+            lib.oracle_attention.argtypes = [p, p, p, ctypes.c_int, i64, i64, i64, ctypes.c_double,
+                                             ctypes.c_int, i64, p, p, p, p, p, p, ctypes.c_int]
+            lib.oracle_attention.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -287,3 +290,49 @@ def epilogue(Cref: np.ndarray, Den: np.ndarray, *, alpha: float = 1.0, beta: flo
     if act in (ACT_GELU, ACT_GELU_TANH):
         den = den * GELU_MAX_SLOPE
     return activation(t, act), den
+
+
+# ---------------------------------------------------------------- attention
+
+def attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, dtype_in: int, BH: int, SQ: int,
+              SKV: int, D: int, scale: float, causal: bool = False, rows=None,
+              threads: int | None = None):
+    """Attention forward, the plain definition (``oracle_attention`` in
+    ``hgemm_oracle.c``): O = softmax(scale * Q K^T [causal mask]) V per
+    (bh, query row), in fp64.  ``Q`` is a flat uint16 buffer [BH][SQ][D],
+    ``K`` and ``V`` [BH][SKV][D].  Causal: key j is allowed for query i when
+    j <= i + SKV - SQ.
+
+    ``rows``: None for every row, else a pair of index arrays ``(b, i)``.
+    Returns ``(O, Den, lse, sden)``: O and Den shaped (BH, SQ, D) or (n, D);
+    lse and sden (BH, SQ) or (n,).  ``Den[c] = sum_j p_j |v_j[c]| / l`` is the
+    error normaliser; ``sden`` bounds |scale * q.k| by the sum of magnitudes."""
+    lib = _load()
+    Q, K, V = _u16(Q), _u16(K), _u16(V)
+    if Q.size < BH * SQ * D or K.size < BH * SKV * D or V.size < BH * SKV * D:
+        raise ValueError("attention operands are smaller than [BH][seq][D]")
+    if rows is None:
+        rb = np.repeat(np.arange(BH, dtype=np.int64), SQ)
+        ri = np.tile(np.arange(SQ, dtype=np.int64), BH)
+        shape = (BH, SQ)
+    else:
+        rb = np.ascontiguousarray(rows[0], dtype=np.int64)
+        ri = np.ascontiguousarray(rows[1], dtype=np.int64)
+        if rb.size != ri.size:
+            raise ValueError("row index arrays differ in length")
+        if rb.size and (rb.min() < 0 or rb.max() >= BH or ri.min() < 0 or ri.max() >= SQ):
+            raise ValueError("row indices out of range")
+        shape = (rb.size,)
+    n = rb.size
+    O = np.empty((n, D), dtype=np.float64)
+    Den = np.empty((n, D), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    sden = np.empty(n, dtype=np.float64)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    rc = lib.oracle_attention(_ptr(Q), _ptr(K), _ptr(V), dtype_in, SQ, SKV, D, float(scale),
+                              int(bool(causal)), n, _ptr(rb), _ptr(ri), _ptr(O), _ptr(Den),
+                              _ptr(lse), _ptr(sden), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_attention rejected its arguments")
+    return (O.reshape(*shape, D), Den.reshape(*shape, D), lse.reshape(shape), sden.reshape(shape))

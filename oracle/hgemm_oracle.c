@@ -240,3 +240,129 @@ int oracle_gemm_entries(const uint16_t *A, const uint16_t *B, int dtype_in,
 void oracle_decode_array(const uint16_t *h, int dtype, int64_t n, double *out) {
     for (int64_t e = 0; e < n; ++e) out[e] = decode(h[e], dtype);
 }
+
+/* ---- attention forward ------------------------------------------------- */
+
+/*
+ * The attention block the GEMM pages build toward ("post_1787550000",
+ * sections 1-2: the FlashAttention kernel's two products S = Q K^T and
+ * O = P V moved to tensor cores, with the softmax between them; the causal
+ * mask is named there too).  Its plain definition, per (bh, i):
+ *
+ *   s_j   = scale * sum_{c<D} q_i[c] * k_j[c]          for allowed j
+ *   p_j   = exp(s_j - max_j s_j)                       (softmax, shifted)
+ *   l     = sum_j p_j
+ *   O[c]  = sum_j p_j * v_j[c] / l
+ *   Den[c]= sum_j p_j * |v_j[c]| / l                   (error normaliser)
+ *   lse   = max_j s_j + log(l)
+ *   sden  = max_j scale * sum_c |q_i[c]| * |k_j[c]|    (bound on |s_j|'s sum)
+ *
+ * all in IEEE binary64, j and c ascending.  Allowed keys: j < SKV and, when
+ * `causal`, j <= i + (SKV - SQ) (the last query row sees every key).  A row
+ * with no allowed key has O = Den = 0, lse = -inf, sden = 0.
+ *
+ * Layout: Q [BH][SQ][D], K and V [BH][SKV][D], row-major and dense; 16-bit
+ * patterns read with `dtype_in` as above.  Rows (rb[r], ri[r]) for r < nrows
+ * are computed into O[r][D], Den[r][D], lse[r], sden[r].
+ */
+typedef struct {
+    const uint16_t *Q, *K, *V;
+    const double *table;
+    int64_t SQ, SKV, D;
+    double scale;
+    int causal;
+    const int64_t *rb, *ri;
+    double *O, *Den, *lse, *sden;
+    double *s; /* SKV scores of the current row */
+    int64_t row_begin, row_end;
+} attn_job_t;
+
+static void *attention_rows(void *arg) {
+    attn_job_t *J = (attn_job_t *)arg;
+    const int64_t D = J->D;
+    for (int64_t r = J->row_begin; r < J->row_end; ++r) {
+        const int64_t b = J->rb[r], i = J->ri[r];
+        const uint16_t *q = J->Q + (b * J->SQ + i) * D;
+        const uint16_t *Kb = J->K + b * J->SKV * D;
+        const uint16_t *Vb = J->V + b * J->SKV * D;
+        double *o = J->O + r * D;
+        double *den = J->Den + r * D;
+        for (int64_t c = 0; c < D; ++c) { o[c] = 0.0; den[c] = 0.0; }
+        int64_t nkeys = J->SKV;
+        if (J->causal) {
+            int64_t last = i + (J->SKV - J->SQ); /* last allowed key */
+            nkeys = last + 1 < 0 ? 0 : (last + 1 < J->SKV ? last + 1 : J->SKV);
+        }
+        if (nkeys == 0) { J->lse[r] = -INFINITY; J->sden[r] = 0.0; continue; }
+        double m = -INFINITY, sd = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            const uint16_t *k = Kb + j * D;
+            double acc = 0.0, mag = 0.0;
+            for (int64_t c = 0; c < D; ++c) {
+                double qv = J->table[q[c]], kv = J->table[k[c]];
+                acc += qv * kv;
+                mag += fabs(qv) * fabs(kv);
+            }
+            J->s[j] = J->scale * acc;
+            if (J->s[j] > m) m = J->s[j];
+            if (fabs(J->scale) * mag > sd) sd = fabs(J->scale) * mag;
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < nkeys; ++j) {
+            double p = exp(J->s[j] - m);
+            l += p;
+            const uint16_t *v = Vb + j * D;
+            for (int64_t c = 0; c < D; ++c) {
+                double vv = J->table[v[c]];
+                o[c] += p * vv;
+                den[c] += p * fabs(vv);
+            }
+        }
+        for (int64_t c = 0; c < D; ++c) { o[c] /= l; den[c] /= l; }
+        J->lse[r] = m + log(l);
+        J->sden[r] = sd;
+    }
+    return NULL;
+}
+
+/* Returns 0 on success, -1 on bad arguments or no memory.  Rows are split
+ * over `threads` worker threads; each row is computed inside one thread, so
+ * the result does not depend on `threads`. */
+int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int dtype_in,
+                     int64_t SQ, int64_t SKV, int64_t D, double scale, int causal,
+                     int64_t nrows, const int64_t *rb, const int64_t *ri,
+                     double *O, double *Den, double *lse, double *sden, int threads) {
+    if (SQ < 0 || SKV < 0 || D < 0 || nrows < 0 || dtype_in < 0 || dtype_in > 3) return -1;
+    if (threads < 1) threads = 1;
+    if (threads > nrows && nrows > 0) threads = (int)nrows;
+    double *table = make_table(dtype_in);
+    attn_job_t *jobs = (attn_job_t *)calloc((size_t)threads, sizeof(attn_job_t));
+    pthread_t *tid = (pthread_t *)calloc((size_t)threads, sizeof(pthread_t));
+    double *scratch = (double *)malloc((size_t)threads * (size_t)(SKV > 0 ? SKV : 1) * sizeof(double));
+    if (!table || !jobs || !tid || !scratch) {
+        free(table); free(jobs); free(tid); free(scratch);
+        return -1;
+    }
+    for (int t = 0; t < threads; ++t) {
+        attn_job_t *J = &jobs[t];
+        J->Q = Q; J->K = K; J->V = V; J->table = table;
+        J->SQ = SQ; J->SKV = SKV; J->D = D; J->scale = scale; J->causal = causal;
+        J->rb = rb; J->ri = ri;
+        J->O = O; J->Den = Den; J->lse = lse; J->sden = sden;
+        J->s = scratch + (size_t)t * (size_t)(SKV > 0 ? SKV : 1);
+        J->row_begin = nrows * t / threads;
+        J->row_end = nrows * (t + 1) / threads;
+    }
+    int started = 0, rc = 0;
+    for (int t = 1; t < threads; ++t) {
+        if (pthread_create(&tid[t], NULL, attention_rows, &jobs[t]) != 0) { rc = -1; break; }
+        started = t;
+    }
+    attention_rows(&jobs[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(tid[t], NULL);
+    if (rc != 0) {
+        for (int t = started + 1; t < threads; ++t) attention_rows(&jobs[t]);
+    }
+    free(table); free(jobs); free(tid); free(scratch);
+    return 0;
+}
