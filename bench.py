@@ -492,14 +492,227 @@ def run_ours(args, w, world, rank, local, pg):
     return 0
 
 
+# ---------------------------------------------------------------- attention
+
+def attn_flops(w) -> int:
+    """2 * bh * sq * skv * d for each of S = Q K^T and O = P V; under the
+    causal mask only the allowed (query, key) pairs count."""
+    if w.causal:
+        pairs = sum(min(w.skv, i + 1 + w.skv - w.sq) for i in range(w.sq))
+    else:
+        pairs = w.sq * w.skv
+    return 4 * w.bh * pairs * 128
+
+
+def attn_config(w, world, extra=None):
+    c = {"workload": w.name, "batch_heads": w.bh, "seq_q": w.sq, "seq_kv": w.skv, "head_dim": 128,
+         "dtype_in": w.dtype, "dtype_out": w.dtype, "causal": w.causal, "scale": w.scale,
+         "seed": w.seed, "parallelism": "replicas" if world > 1 else "single",
+         "layout": "Q, K, V, O [bh][seq][128] row-major"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def attn_oracle_time(w, qb, kb, vb, rows: int, threads: int) -> float:
+    """Oracle attention on query rows 0 .. rows-1 of head 0 (the longest rows
+    of a causal head are the last ones: rows are taken from the end then)."""
+    import numpy as np
+
+    import oracle
+    ri = np.arange(w.sq - rows, w.sq) if w.causal else np.arange(rows)
+    rb = np.zeros(rows, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.attention(qb, kb, vb, ORACLE_IN[w.dtype], w.bh, w.sq, w.skv, 128, w.scale, w.causal,
+                     rows=(rb, ri), threads=threads)
+    return time.perf_counter() - t0
+
+
+def attn_cpu_inputs(w):
+    import numpy as np
+    import torch
+
+    from tensor_core_dense_swizzled_gb300 import inputs
+    Q, K, V = inputs.make_attention_inputs(w)
+    conv = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)  # noqa: E731
+    return conv(Q), conv(K), conv(V)
+
+
+def attn_pairs_of_rows(w, rows: int) -> int:
+    if not w.causal:
+        return rows * w.skv
+    return sum(min(w.skv, i + 1 + w.skv - w.sq) for i in range(w.sq - rows, w.sq))
+
+
+def attn_cpu_baseline(w, target_s: float = 12.0):
+    qb, kb, vb = attn_cpu_inputs(w)
+    threads = os.cpu_count() or 1
+    rows = min(w.sq, 4 * threads)
+    t = attn_oracle_time(w, qb, kb, vb, rows, threads)
+    rows = int(min(w.sq, max(threads, math.floor(target_s / max(t / rows, 1e-9) / threads) * threads)))
+    t = attn_oracle_time(w, qb, kb, vb, rows, threads)
+    fl = 4 * attn_pairs_of_rows(w, rows) * 128
+    return {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": min(threads, rows), "kind": "oracle",
+            "sample": f"{rows} query rows of head 0 of {w.name} ({rows} x {w.skv} keys x 128), "
+                      f"fp64 loops, {t:.1f} s"}
+
+
+def run_attention_reference(args, w, rank, world):
+    if rank != 0:
+        return 0
+    qb, kb, vb = attn_cpu_inputs(w)
+    threads = os.cpu_count() or 1
+    t1 = attn_oracle_time(w, qb, kb, vb, min(w.sq, threads), threads) / min(w.sq, threads)
+    per_step_budget = 90.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(w.sq, math.floor(per_step_budget / max(t1, 1e-9)))))
+    for _ in range(args.warmup):
+        attn_oracle_time(w, qb, kb, vb, rows, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        attn_oracle_time(w, qb, kb, vb, rows, threads)
+    dt = time.perf_counter() - t0
+    value = 4 * attn_pairs_of_rows(w, rows) * 128 * args.steps / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": attn_config(w, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": min(threads, rows), "kind": "oracle",
+                         "sample": f"each step: {rows} query rows of head 0 of {w.name}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_attention_ours(args, w, world, rank, local, pg):
+    import torch
+
+    import __graft_entry__
+    from tensor_core_dense_swizzled_gb300 import hgemm as H
+    from tensor_core_dense_swizzled_gb300 import inputs
+
+    __graft_entry__.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    DT = {"f16": H.HGEMM_F16, "bf16": H.HGEMM_BF16}
+    Q, K, V = inputs.make_attention_inputs(w)
+    flops = attn_flops(w)
+    set_bytes = (Q.numel() + K.numel() + V.numel() + Q.numel()) * 2
+    nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes))
+    sets = [(Q.to(dev), K.to(dev), V.to(dev), torch.empty_like(Q, device=dev)) for _ in range(nsets)]
+    plan = H.hgemm_attention_plan_create(w.bh, w.sq, w.skv, 128, w.scale, int(w.causal), DT[w.dtype])
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        q, k, v, o = sets[i % nsets]
+        H.hgemm_attention_run(plan, q, k, v, o, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    st = H.hgemm_attention_check(plan, stream)
+    if st != 0:
+        raise RuntimeError(f"warm-up failed: {H.STATUS.get(st)} {H.hgemm_last_error_detail()}")
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    ev_start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    t_wall1 = time.time()
+    region_ms = ev_start.elapsed_time(ev_end)
+    probe_until = t_wall0 + args.probe_seconds
+    j = 0
+    while time.time() < probe_until:
+        for _ in range(50):
+            step(j)
+            j += 1
+        torch.cuda.synchronize(dev)
+    t_wall2 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0 - 0.05, max(t_wall1, t_wall2) + 0.05)
+    clocks["window"] = "timed" if t_wall1 - t_wall0 >= 1.0 else "timed+probe"
+    st = H.hgemm_attention_check(plan, stream)
+    if st != 0:
+        raise RuntimeError(f"timed run failed: {H.STATUS.get(st)} {H.hgemm_last_error_detail()}")
+    region_ms = max_over_ranks(pg, region_ms, dev)
+    value = whole_job_tflops(flops, args.steps, world, region_ms)
+    avg_launch_ms = region_ms / args.steps
+    peaks = load_peaks()
+    sustained = region_ms > 1000.0
+    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+    peak = peaks["bf16_sustained"] if sustained else peaks["bf16"]
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": committed_traffic(w.name),
+            "peak_kind": ("sustained" if sustained else "burst") + f" bf16, {peaks['source']}",
+            "algorithmic_per_launch": flops, "launch_ms": avg_launch_ms, "kernels_per_launch": 1}
+    e2e = None
+    if args.e2e_steps > 0:
+        Qh, Kh, Vh = Q.pin_memory(), K.pin_memory(), V.pin_memory()
+        Oh = torch.empty_like(Q).pin_memory()
+        H.hgemm_attention_run_host(plan, Qh, Kh, Vh, Oh, stream)
+        barrier(pg)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            H.hgemm_attention_run_host(plan, Qh, Kh, Vh, Oh, stream)
+        dt = time.perf_counter() - t0
+        dt = max_over_ranks(pg, dt, dev)
+        e2e = {"value": flops * args.e2e_steps * world / dt / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": (Q.numel() + K.numel() + V.numel()) * 2,
+               "d2h_bytes_per_step": Q.numel() * 2, "steps": args.e2e_steps}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = attn_cpu_baseline(w)
+    H.hgemm_attention_plan_destroy(plan)
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": attn_config(w, world, {
+            "l2": f"{nsets} rotating input/output sets ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)",
+            "path": "attention", "tile": [128, 128, 128], "grid": w.bh * ((w.sq + 127) // 128)}),
+        "pct_nominal_tensor_peak": 100.0 * value / world / NOMINAL_TC_TFLOPS,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     from tensor_core_dense_swizzled_gb300 import inputs
-    if args.workload not in inputs.WORKLOADS:
-        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(inputs.WORKLOADS)}")
-    w = inputs.WORKLOADS[args.workload]
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.workload in inputs.ATTENTION_WORKLOADS:
+        w = inputs.ATTENTION_WORKLOADS[args.workload]
+        world, rank, local, pg = dist_setup(args)
+        try:
+            if args.impl == "reference":
+                return run_attention_reference(args, w, rank, world)
+            return run_attention_ours(args, w, world, rank, local, pg)
+        finally:
+            if pg is not None:
+                pg.destroy_process_group()
+    if args.workload not in inputs.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from "
+                         f"{sorted(inputs.WORKLOADS) + sorted(inputs.ATTENTION_WORKLOADS)}")
+    w = inputs.WORKLOADS[args.workload]
     world, rank, local, pg = dist_setup(args)
     try:
         if args.impl == "reference":

@@ -275,6 +275,57 @@ hgemm_status_t hgemm_skinny_noalloc(const void *A, const void *B, void *C, int64
                                     int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                                     hgemm_dtype_t dtype_in, hgemm_dtype_t dtype_out, void *stream);
 
+/* ---------------------------------------------------------------- attention
+ *
+ * Fused attention forward: the block the "post_1787550000" experiment builds
+ * its tensor-core work toward (its sections 1-2: the products S = Q K^T and
+ * O = P V of a FlashAttention kernel on the tensor cores, the softmax of S
+ * between them, P handed to the second product without a trip through
+ * memory, and a causal mask), with the row-wise max and sum of S the
+ * "hgemm_mma_m16n8k16_mma2x4_warp4x4_kernel" page describes (its section 2).
+ * For every head b < batch_heads and query row i < seq_q:
+ *
+ *     O[b][i] = sum_j p_j V[b][j] / sum_j p_j,
+ *     p_j     = exp(scale * Q[b][i] . K[b][j] - max_j(...)),
+ *
+ * over the allowed keys j: every j < seq_kv, or with `causal`
+ * j <= i + seq_kv - seq_q (the last query row sees every key).
+ *   Q  [batch_heads][seq_q][head_dim], K and V [batch_heads][seq_kv][head_dim],
+ *   O  [batch_heads][seq_q][head_dim]: dense row-major device arrays of
+ *      `dtype` (HGEMM_F16 or HGEMM_BF16, O included), 16-byte aligned.
+ * Scores and softmax are fp32; the probabilities are rounded to `dtype` for
+ * the product with V, which accumulates in fp32; O is rounded once.
+ * head_dim must be 128 (else HGEMM_ERR_UNSUPPORTED); scale finite and > 0;
+ * causal needs seq_q <= seq_kv, so that every row has a key (else
+ * HGEMM_ERR_INVALID_ARG).  seq_q == 0 does nothing; seq_kv == 0 writes
+ * zeros (the empty sum).  Plans own a small device workspace (the error
+ * word) and the staging buffers of hgemm_attention_run_host. */
+typedef struct hgemm_attn_plan_s *hgemm_attn_plan_t;
+
+hgemm_status_t hgemm_attention_plan_create(hgemm_attn_plan_t *plan, int64_t batch_heads,
+                                           int64_t seq_q, int64_t seq_kv, int64_t head_dim,
+                                           float scale, int causal, hgemm_dtype_t dtype);
+
+/* Enqueues the attention forward on `stream` (device pointers; returns once
+ * enqueued).  INVALID_ARG for a null or misaligned pointer. */
+hgemm_status_t hgemm_attention_run(hgemm_attn_plan_t plan, const void *Q, const void *K,
+                                   const void *V, void *O, void *stream);
+
+/* As hgemm_attention_run with Q, K, V and O in host memory: copies the
+ * inputs to plan-owned device buffers, runs, copies O back and synchronises
+ * `stream`. */
+hgemm_status_t hgemm_attention_run_host(hgemm_attn_plan_t plan, const void *Q_host,
+                                        const void *K_host, const void *V_host, void *O_host,
+                                        void *stream);
+
+/* Synchronises `stream` and reads the plan's device error word, as
+ * hgemm_check does for GEMM plans (HGEMM_ERR_TIMEOUT after a watchdog
+ * timeout; the word is cleared on read). */
+hgemm_status_t hgemm_attention_check(hgemm_attn_plan_t plan, void *stream);
+
+/* Frees the plan (NULL accepted); no run of it may still be executing. */
+hgemm_status_t hgemm_attention_plan_destroy(hgemm_attn_plan_t plan);
+
 const char *hgemm_status_string(hgemm_status_t status);
 const char *hgemm_last_error_detail(void);
 

@@ -1,6 +1,6 @@
 """Builds libhgemm.so in-tree for sm_103a with nvcc (no cmake, no torch).
 
-Each ``csrc/*.cu`` and ``csrc/api.cpp`` is compiled in parallel into
+Each ``csrc/*.cu`` and ``csrc/*.cpp`` is compiled in parallel into
 ``_build/`` and linked into ``tensor_core_dense_swizzled_gb300/libhgemm.so``
 against the shared CUDA runtime.  A rebuild happens only when a source or
 header is newer than the library.
@@ -33,7 +33,7 @@ def _cuda_home() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu"))) + [os.path.join(CSRC, "api.cpp")]
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu"))) + sorted(glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():

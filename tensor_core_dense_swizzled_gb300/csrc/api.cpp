@@ -1052,6 +1052,14 @@ hgemm_status_t encode_map_3d(CUtensorMap *map, const void *base, int bf16, int64
                      cols, rows, 1, ld, 0, box_cols, box_rows);
 }
 
+hgemm_status_t encode_map_batched(CUtensorMap *map, const void *base, int bf16, int64_t cols,
+                                  int64_t rows, int64_t batch, int64_t ld, int64_t stride,
+                                  uint32_t box_cols, uint32_t box_rows) {
+    return encode_3d(map, base,
+                     bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                     cols, rows, batch, ld, stride, box_cols, box_rows);
+}
+
 int pick_split(int64_t work_tiles, int num_kb, int num_sms) {
     return choose_split(work_tiles, num_kb, num_sms);
 }

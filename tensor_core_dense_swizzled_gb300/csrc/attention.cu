@@ -1,0 +1,379 @@
+// attention.cu -- fused attention forward on tcgen05 for sm_103a.
+//
+// O = softmax(scale * Q K^T [causal]) V per (batch x head, query row), the
+// block "post_1787550000" builds its tensor-core work toward (sections 1-2:
+// S = Q K^T and O = P V moved onto the tensor cores with the softmax between
+// them, P = softmax(S) fed to the second product without leaving the chip;
+// "hgemm_mma_m16n8k16_mma2x4_warp4x4_kernel" section 2 on the row-wise max
+// and sum of S and the accumulator of one product becoming the operand of
+// the next).  Head dimension 128, fp16 or bf16 in and out, fp32 scores,
+// probabilities rounded to the input type for the second product (as the
+// register hand-over of the pages does), fp32 accumulation.
+//
+// One CTA computes a 128-row query tile of one head, streaming the keys and
+// values in blocks of 128 rows:
+//   warp 0, one thread   TMA: the Q tile once, then K_j and V_j into a ring
+//                        of two stages (separate full / empty barriers for K
+//                        and V, so S_j can start before V_j lands).
+//   warp 1, one thread   MMA: S_j = Q K_j^T into TMEM buffer j % 2 (8 MMAs
+//                        of K = 16 over the head dimension), then, once the
+//                        softmax warps have written P_{j-1}, O += P_{j-1}
+//                        V_{j-1} (8 MMAs of 16 keys) into the O accumulator
+//                        in TMEM.  The tensor core therefore computes
+//                        S_{j+1} and P_{j-1} V_{j-1} while the softmax of
+//                        S_j runs.
+//   warps 2-5            online softmax, one query row per thread (the TMEM
+//                        lane of its row): tcgen05.ld the 128 scores of S_j,
+//                        release the buffer, mask, take the row max, form
+//                        p = 2^(s * scale * log2 e - m) with the SFU's ex2,
+//                        sum the row, rescale O in TMEM when the reference
+//                        max moved, and store P (16-bit) into 128-byte-
+//                        swizzled shared memory as the K-major A operand of
+//                        the second product.  After the last block: O / l,
+//                        rounded to the output type, stored to global memory.
+//
+// The reference max m is raised only when a block's max exceeds it by more
+// than 8 (in log2 units): p then stays <= 2^8, and O and l, always scaled by
+// the same 2^-m, give the same quotient O / l as with the running max, while
+// the O rescale (a TMEM load / multiply / store of the warp's 32 rows)
+// happens only when some row of the warp raised its reference.
+//
+// Every wait is bounded (watchdog.cuh); a timeout records its code in the
+// error word, the CTA's roles leave their loops, the MMA thread waits for
+// its MMAs and the producer for its copies, and TMEM is freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_common.cuh"
+#include "watchdog.cuh"
+
+namespace hg {
+namespace {
+
+constexpr int ATT_THREADS = 192;              // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr uint32_t ATT_TILE = 128 * 128 * 2;  // 128 rows x 128 16-bit elements
+constexpr uint32_t ATT_HALF = ATT_TILE / 2;   // one 64-element column block
+constexpr int ATT_STAGES = 2;                 // K / V ring depth
+
+// shared memory, from a 1024-byte-aligned base
+constexpr uint32_t SM_Q = 0;
+constexpr uint32_t SM_K = SM_Q + ATT_TILE;
+constexpr uint32_t SM_V = SM_K + ATT_STAGES * ATT_TILE;
+constexpr uint32_t SM_P = SM_V + ATT_STAGES * ATT_TILE;
+constexpr uint32_t SM_BAR = SM_P + ATT_TILE;
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
+// s_free[2], p_full, o_done, drain
+constexpr int ATT_NBAR = 1 + 4 * ATT_STAGES + 2 + 2 + 3;
+constexpr uint32_t SM_MISC = SM_BAR + 8 * ATT_NBAR;
+constexpr uint32_t ATT_SMEM = SM_MISC + 16 + 1024;  // + alignment slack
+
+// TMEM columns: S buffers at 0 and 128, O at 256 (512 allocated)
+constexpr uint32_t TM_S = 0;
+constexpr uint32_t TM_O = 256;
+constexpr uint32_t TM_COLS = 512;
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+template <bool BF16>
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+    attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    constexpr int OUT = BF16 ? OUT_BF16 : OUT_F16;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + SM_Q, sK = sbase + SM_K, sV = sbase + SM_V, sP = sbase + SM_P;
+    const uint32_t bar0 = sbase + SM_BAR;
+    const uint32_t q_full = bar0;
+    auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto k_empty = [&](int s) { return bar0 + 8u * (1 + ATT_STAGES + s); };
+    auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * ATT_STAGES + s); };
+    auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * ATT_STAGES + s); };
+    auto s_full = [&](int b) { return bar0 + 8u * (1 + 4 * ATT_STAGES + b); };
+    auto s_free = [&](int b) { return bar0 + 8u * (3 + 4 * ATT_STAGES + b); };
+    const uint32_t p_full = bar0 + 8u * (5 + 4 * ATT_STAGES);
+    const uint32_t o_done = bar0 + 8u * (6 + 4 * ATT_STAGES);
+    const uint32_t drain = bar0 + 8u * (7 + 4 * ATT_STAGES);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + SM_MISC);
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + SM_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // query tiles in descending order: under the causal mask the longest
+    // tiles start first
+    const int qt = p.nqt - 1 - static_cast<int>(blockIdx.x) / p.bh;
+    const int bh = static_cast<int>(blockIdx.x) % p.bh;
+    const int q0 = qt * 128;
+    // key blocks this tile reads: the last row q0 + 127 sees keys up to
+    // q0 + 127 + skv - sq under the causal mask
+    int kv_end = p.skv;
+    if (p.causal) kv_end = min(p.skv, q0 + 128 + (p.skv - p.sq));
+    const int nkv = (kv_end + 127) / 128;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < ATT_STAGES; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(s_full(b), 1);
+            mbar_init(s_free(b), 4);
+        }
+        mbar_init(p_full, 4);
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, ATT_TILE);
+            tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
+            tma_load_3d(sQ + ATT_HALF, &tmQ, q_full, 64, q0, bh);
+            int issued_k = 0, issued_v = 0;
+            for (int j = 0; j < nkv; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+                if (!wait_bounded(k_empty(s), ph ^ 1u, wc, timeout_code(ROLE_PRODUCER, s))) break;
+                mbar_arrive_expect_tx(k_full(s), ATT_TILE);
+                tma_load_3d(sK + s * ATT_TILE, &tmK, k_full(s), 0, j * 128, bh);
+                tma_load_3d(sK + s * ATT_TILE + ATT_HALF, &tmK, k_full(s), 64, j * 128, bh);
+                ++issued_k;
+                if (!wait_bounded(v_empty(s), ph ^ 1u, wc, timeout_code(ROLE_PRODUCER, 2 + s))) break;
+                mbar_arrive_expect_tx(v_full(s), ATT_TILE);
+                tma_load_3d(sV + s * ATT_TILE, &tmV, v_full(s), 0, j * 128, bh);
+                tma_load_3d(sV + s * ATT_TILE + ATT_HALF, &tmV, v_full(s), 64, j * 128, bh);
+                ++issued_v;
+            }
+            // copies still in flight land before the CTA leaves (immediate on
+            // the normal path: the MMAs consumed them)
+            wait_bounded(q_full, 0, wc, 0, /*honor_abort=*/false);
+            for (int j = max(0, issued_k - ATT_STAGES); j < issued_k; ++j)
+                wait_bounded(k_full(j & 1), static_cast<uint32_t>(j >> 1) & 1u, wc, 0, false);
+            for (int j = max(0, issued_v - ATT_STAGES); j < issued_v; ++j)
+                wait_bounded(v_full(j & 1), static_cast<uint32_t>(j >> 1) & 1u, wc, 0, false);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t tO = tmem_base + TM_O;
+            bool ok = wait_bounded(q_full, 0, wc, timeout_code(ROLE_MMA, 0x300));
+            const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);
+            const uint64_t pdesc = sdesc_sw128(sP, 16, 1024);
+            // O += P_t V_t: P K-major (two 64-key blocks 16 KB apart, 32 bytes
+            // per 16 keys); V MN-major (two 64-column blocks 16 KB apart,
+            // 2 KB per 16 keys)
+            auto issue_pv = [&](int t) -> bool {
+                const int ts = t & 1;
+                if (!wait_bounded(p_full, static_cast<uint32_t>(t) & 1u, wc, timeout_code(ROLE_MMA, 0x301)))
+                    return false;
+                if (!wait_bounded(v_full(ts), static_cast<uint32_t>(t >> 1) & 1u, wc,
+                                  timeout_code(ROLE_MMA, 0x302 + ts)))
+                    return false;
+                tc_fence_after();
+                const uint64_t vdesc = sdesc_sw128(sV + ts * ATT_TILE, ATT_HALF, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t poff = (kk >> 2) * ATT_HALF + (kk & 3) * 32;
+                    umma_f16(tO, pdesc + (poff >> 4), vdesc + ((kk * 2048u) >> 4), p.idesc_o,
+                             (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(v_empty(ts));
+                umma_commit(o_done);
+                return true;
+            };
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int s = j & 1;
+                if (!wait_bounded(k_full(s), static_cast<uint32_t>(j >> 1) & 1u, wc,
+                                  timeout_code(ROLE_MMA, s))) {
+                    ok = false;
+                    break;
+                }
+                if (j >= 2 && !wait_bounded(s_free(s), static_cast<uint32_t>((j - 2) >> 1) & 1u, wc,
+                                            timeout_code(ROLE_MMA, 0x100 + s))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t kdesc = sdesc_sw128(sK + s * ATT_TILE, 16, 1024);
+                const uint32_t tS = tmem_base + TM_S + 128u * s;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * ATT_HALF + (kk & 3) * 32;
+                    umma_f16(tS, qdesc + (off >> 4), kdesc + (off >> 4), p.idesc_s, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(k_empty(s));
+                umma_commit(s_full(s));
+                if (j >= 1 && !issue_pv(j - 1)) ok = false;
+            }
+            if (ok) issue_pv(nkv - 1);
+            umma_commit(drain);
+            wait_bounded(drain, 0, wc, 0, /*honor_abort=*/false);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        const uint32_t quarter = static_cast<uint32_t>(warp & 3);
+        const int row = static_cast<int>(quarter) * 32 + lane;
+        const uint32_t lane_addr = (quarter * 32u) << 16;
+        const int qi = q0 + row;
+        int lim = p.skv;  // keys < lim are allowed for this row
+        if (p.causal) lim = min(lim, qi + 1 + (p.skv - p.sq));
+        const float c = p.scale_log2;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        uint32_t sv[4][32];
+        for (int j = 0; j < nkv; ++j) {
+            const int b = j & 1;
+            if (!wait_bounded_warp(s_full(b), static_cast<uint32_t>(j >> 1) & 1u, wc,
+                                   timeout_code(ROLE_EPILOGUE, b))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(tmem_base + lane_addr + TM_S + 128u * b + 32u * q, sv[q]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free(b));
+            const int kbase = j * 128;
+            if (kbase + 128 > lim) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (kbase + q * 32 + i >= lim) sv[q][i] = f2u(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, u2f(sv[q][i]));
+            mx *= c;
+            float alpha = 1.f;
+            const bool raise = mx > m_ref + 8.f;
+            if (raise) {
+                alpha = ex2_approx(m_ref - mx);
+                m_ref = mx;
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float e = ex2_approx(fmaf(u2f(sv[q][i]), c, -m_ref));
+                    sum += e;
+                    sv[q][i] = f2u(e);
+                }
+            l = l * alpha + sum;
+            if (j >= 1) {
+                // P_{j-1} V_{j-1} has finished: the P buffer is free and O holds
+                // every earlier block
+                if (!wait_bounded_warp(o_done, static_cast<uint32_t>(j - 1) & 1u, wc,
+                                       timeout_code(ROLE_EPILOGUE, 0x10))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xFFFFFFFFu, raise)) {
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t o[32];
+                        tmem_ld32(tmem_base + lane_addr + TM_O + 32u * q, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+                        tmem_st32(tmem_base + lane_addr + TM_O + 32u * q, o);
+                    }
+                }
+            }
+            // P row into the swizzled K-major operand: keys 64 * kb .. 64 * kb + 63
+            // in block kb; 16-byte chunk ch of the row at chunk ch ^ (row & 7)
+            const uint32_t prow = sP + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t ch = static_cast<uint32_t>((q & 1) * 4 + t);
+                    const uint32_t addr = prow + (q >> 1) * ATT_HALF + ((ch ^ (row & 7)) << 4);
+                    st_shared_v4(addr, pack2<OUT>(sv[q][8 * t], sv[q][8 * t + 1]),
+                                 pack2<OUT>(sv[q][8 * t + 2], sv[q][8 * t + 3]),
+                                 pack2<OUT>(sv[q][8 * t + 4], sv[q][8 * t + 5]),
+                                 pack2<OUT>(sv[q][8 * t + 6], sv[q][8 * t + 7]));
+                }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok && wait_bounded_warp(o_done, static_cast<uint32_t>(nkv - 1) & 1u, wc,
+                                    timeout_code(ROLE_EPILOGUE, 0x11))) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            const bool store = qi < p.sq;
+            uint8_t *orow = static_cast<uint8_t *>(p.O) +
+                            (static_cast<int64_t>(bh) * p.sq + (store ? qi : 0)) * 256;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tmem_base + lane_addr + TM_O + 32u * q, o);
+                if (store) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + q * 64);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        uint4 v;
+                        v.x = pack2<OUT>(f2u(u2f(o[8 * t]) * inv), f2u(u2f(o[8 * t + 1]) * inv));
+                        v.y = pack2<OUT>(f2u(u2f(o[8 * t + 2]) * inv), f2u(u2f(o[8 * t + 3]) * inv));
+                        v.z = pack2<OUT>(f2u(u2f(o[8 * t + 4]) * inv), f2u(u2f(o[8 * t + 5]) * inv));
+                        v.w = pack2<OUT>(f2u(u2f(o[8 * t + 6]) * inv), f2u(u2f(o[8 * t + 7]) * inv));
+                        dst[t] = v;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_attention(bool bf16, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                             const CUtensorMap &tmV, const AttnParams &p, cudaStream_t stream) {
+    auto kern = bf16 ? attention_fwd_kernel<true> : attention_fwd_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(ATT_SMEM));
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(p.bh) * static_cast<unsigned>(p.nqt);
+    kern<<<grid, ATT_THREADS, ATT_SMEM, stream>>>(tmQ, tmK, tmV, p);
+    return cudaGetLastError();
+}
+
+}  // namespace hg

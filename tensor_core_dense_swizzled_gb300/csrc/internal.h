@@ -14,6 +14,13 @@ namespace hg {
 hgemm_status_t encode_map_3d(CUtensorMap *map, const void *base, int bf16, int64_t cols,
                              int64_t rows, int64_t ld, uint32_t box_cols, uint32_t box_rows);
 
+// 3-D tiled, 128-byte-swizzled map over a row-major 16-bit array of `batch`
+// matrices of `rows` x `cols` (leading dimension `ld`, batch stride
+// `stride`, elements), zero fill outside.
+hgemm_status_t encode_map_batched(CUtensorMap *map, const void *base, int bf16, int64_t cols,
+                                  int64_t rows, int64_t batch, int64_t ld, int64_t stride,
+                                  uint32_t box_cols, uint32_t box_rows);
+
 // The skinny path's split-K choice (units per wave >= 90% when possible).
 int pick_split(int64_t work_tiles, int num_kb, int num_sms);
 

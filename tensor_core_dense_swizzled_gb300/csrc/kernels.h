@@ -176,4 +176,23 @@ cudaError_t launch_epilogue_fill(void *C, int64_t ldc, int64_t strideC, int64_t 
 // One-warp kernel waiting on an mbarrier nothing signals (watchdog self-test).
 cudaError_t launch_watchdog_selftest(int32_t *err, uint64_t timeout_ns, cudaStream_t stream);
 
+// Attention forward (attention.cu): O = softmax(scale Q K^T [causal]) V with
+// Q [bh][sq][128], K, V [bh][skv][128], O [bh][sq][128], 16-bit, dense.
+// One CTA per 128-query tile; the tensor maps cover Q, K and V as
+// (128 elements, rows, bh) with 64 x 128 boxes.
+struct AttnParams {
+    int32_t bh, sq, skv;  // heads x batch, query rows, key rows
+    int32_t nqt;          // query tiles per head: ceil(sq / 128)
+    int32_t causal;       // key j allowed for query i when j <= i + skv - sq
+    float scale_log2;     // softmax scale x log2(e), > 0
+    uint32_t idesc_s;     // S = Q K^T: M 128, N 128 keys, both K-major
+    uint32_t idesc_o;     // O += P V: M 128, N 128, P K-major, V MN-major
+    void *O;
+    int32_t *err;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_attention(bool bf16, const CUtensorMap &tmQ, const CUtensorMap &tmK,
+                             const CUtensorMap &tmV, const AttnParams &p, cudaStream_t stream);
+
 }  // namespace hg

@@ -19,7 +19,9 @@ __all__ = [
     "hgemm_check", "hgemm_plan_destroy", "hgemm_plan_get_info", "hgemm", "hgemm_cache_clear",
     "hgemm_watchdog_selftest", "hgemm_skinny_noalloc", "hgemm_status_string", "Epilogue",
     "hgemm_run_ex", "HGEMM_ACT_NONE", "HGEMM_ACT_RELU", "HGEMM_ACT_GELU", "HGEMM_ACT_GELU_TANH",
-    "hgemm_last_error_detail", "hgemm_version",
+    "hgemm_last_error_detail", "hgemm_version", "hgemm_attention_plan_create",
+    "hgemm_attention_run", "hgemm_attention_run_host", "hgemm_attention_check",
+    "hgemm_attention_plan_destroy",
     "STATUS",
 ]
 
@@ -134,8 +136,16 @@ def load():
         lib.hgemm_watchdog_selftest.argtypes = [ctypes.c_uint64, p, ctypes.POINTER(ctypes.c_int32)]
         lib.hgemm_skinny_noalloc.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int,
                                              ctypes.c_int, p]
+        lib.hgemm_attention_plan_create.argtypes = [plan_p, i64, i64, i64, i64, ctypes.c_float,
+                                                    ctypes.c_int, ctypes.c_int]
+        lib.hgemm_attention_run.argtypes = [p, p, p, p, p, p]
+        lib.hgemm_attention_run_host.argtypes = [p, p, p, p, p, p]
+        lib.hgemm_attention_check.argtypes = [p, p]
+        lib.hgemm_attention_plan_destroy.argtypes = [p]
         for name in ("hgemm_plan_create", "hgemm_plan_create_ex", "hgemm_run", "hgemm_run_host",
-                     "hgemm_run_ex",
+                     "hgemm_run_ex", "hgemm_attention_plan_create", "hgemm_attention_run",
+                     "hgemm_attention_run_host", "hgemm_attention_check",
+                     "hgemm_attention_plan_destroy",
                      "hgemm_check", "hgemm_plan_destroy", "hgemm_plan_get_info", "hgemm",
                      "hgemm_cache_clear", "hgemm_watchdog_selftest", "hgemm_skinny_noalloc"):
             getattr(lib, name).restype = st
@@ -272,3 +282,34 @@ def hgemm_last_error_detail() -> str:
 
 def hgemm_version() -> int:
     return load().hgemm_version()
+
+
+# ---------------------------------------------------------------- attention
+
+def hgemm_attention_plan_create(batch_heads, seq_q, seq_kv, head_dim, scale, causal, dtype) -> int:
+    lib = load()
+    h = ctypes.c_void_p()
+    _check(lib.hgemm_attention_plan_create(ctypes.byref(h), batch_heads, seq_q, seq_kv, head_dim,
+                                           float(scale), int(causal), dtype),
+           "hgemm_attention_plan_create")
+    return h.value
+
+
+def hgemm_attention_run(plan: int, Q, K, V, O, stream=None):
+    _check(load().hgemm_attention_run(plan, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _stream(stream)),
+           "hgemm_attention_run")
+
+
+def hgemm_attention_run_host(plan: int, Q_host, K_host, V_host, O_host, stream=None):
+    _check(load().hgemm_attention_run_host(plan, _ptr(Q_host), _ptr(K_host), _ptr(V_host),
+                                           _ptr(O_host), _stream(stream)),
+           "hgemm_attention_run_host")
+
+
+def hgemm_attention_check(plan: int, stream=None) -> int:
+    """Status instead of an exception (HGEMM_ERR_TIMEOUT = 6 after a watchdog timeout)."""
+    return load().hgemm_attention_check(plan, _stream(stream))
+
+
+def hgemm_attention_plan_destroy(plan: int):
+    _check(load().hgemm_attention_plan_destroy(plan), "hgemm_attention_plan_destroy")

@@ -27,6 +27,12 @@ name                        shape / values
                             stored N x K, bf16 out
 ==========================  =========================================================
 
+Attention workloads (``ATTENTION_WORKLOADS``): ``attn`` is 64 heads x
+(1024 queries, 1024 keys, head dimension 128) bf16 -- the batched S = Q K^T
+shape above, followed by the softmax and O = P V -- with Q, K, V drawn
+N(0, 1) in that order from seed 5 and scale 1/sqrt(128); ``attn_causal`` the
+same with the causal mask.
+
 8-bit draws are rounded by ``.to(torch.float8_e4m3fn / float8_e5m2)``; the
 distributions stay far inside both formats' ranges (448 and 57344), so no
 value saturates or overflows.
@@ -38,7 +44,8 @@ from dataclasses import dataclass
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "make_random", "torch_dtype"]
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "make_random", "torch_dtype",
+           "AttentionWorkload", "ATTENTION_WORKLOADS", "make_attention_inputs"]
 
 _TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
        "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
@@ -146,3 +153,36 @@ def make_random(shape, dtype_in: str, seed: int, dist: str = "normal", scale: fl
     """One seeded tensor of the given shape (for the small parity cases)."""
     gen = torch.Generator().manual_seed(seed)
     return _draw(gen, tuple(shape), dist, scale).to(_TD[dtype_in])
+
+
+@dataclass(frozen=True)
+class AttentionWorkload:
+    name: str
+    bh: int      # batch x heads
+    sq: int      # query rows per head
+    skv: int     # key / value rows per head
+    dtype: str   # "bf16" | "f16" (inputs and output)
+    causal: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(128.0)
+
+
+ATTENTION_WORKLOADS = {
+    w.name: w
+    for w in [
+        AttentionWorkload("attn", 64, 1024, 1024, "bf16", False, 5),
+        AttentionWorkload("attn_causal", 64, 1024, 1024, "bf16", True, 5),
+    ]
+}
+
+
+def make_attention_inputs(w: AttentionWorkload):
+    """CPU tensors ``(Q, K, V)`` shaped (bh, seq, 128), contiguous, N(0, 1)."""
+    gen = torch.Generator().manual_seed(w.seed)
+    Q = _draw(gen, (w.bh, w.sq, 128), "normal", 1.0).to(_TD[w.dtype])
+    K = _draw(gen, (w.bh, w.skv, 128), "normal", 1.0).to(_TD[w.dtype])
+    V = _draw(gen, (w.bh, w.skv, 128), "normal", 1.0).to(_TD[w.dtype])
+    return Q, K, V

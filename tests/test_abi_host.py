@@ -148,6 +148,28 @@ def test_fp8_layout_rules(lib):
         assert create(64, 64, 64, 64, 64, din=H.HGEMM_E5M2, batch=2, sA=64 * 64, sB=64 * 64) == 3
 
 
+def test_attention_argument_checks_need_no_gpu(lib):
+    """The attention plan's checks run before any device is touched."""
+    h = ctypes.c_void_p()
+    bad = [((0, 16, 16, 128, 1.0, 0, H.HGEMM_BF16), 1),     # no heads
+           ((2, -1, 16, 128, 1.0, 0, H.HGEMM_BF16), 1),     # negative seq_q
+           ((2, 16, 16, 128, 0.0, 0, H.HGEMM_BF16), 1),     # scale 0
+           ((2, 16, 16, 128, -1.0, 0, H.HGEMM_BF16), 1),    # negative scale
+           ((2, 32, 16, 128, 1.0, 1, H.HGEMM_BF16), 1),     # causal, seq_q > seq_kv
+           ((2, 16, 16, 128, 1.0, 2, H.HGEMM_BF16), 1),     # causal not 0 / 1
+           ((2, 16, 16, 128, 1.0, 0, H.HGEMM_E4M3), 1),     # 8-bit inputs
+           ((2, 16, 16, 64, 1.0, 0, H.HGEMM_BF16), 2)]      # head_dim 64
+    for args, want in bad:
+        assert lib.hgemm_attention_plan_create(ctypes.byref(h), *args) == want, args
+    assert lib.hgemm_attention_plan_create(None, 2, 16, 16, 128, 1.0, 0, H.HGEMM_BF16) == 1
+    assert lib.hgemm_attention_run(None, None, None, None, None, None) == 1
+    assert lib.hgemm_attention_check(None, None) == 1
+    assert lib.hgemm_attention_plan_destroy(None) == 0
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.hgemm_attention_plan_create(ctypes.byref(h), 2, 16, 16, 128, 1.0, 0, H.HGEMM_BF16) == 3
+
+
 def test_valid_request_without_gpu_reports_no_device(lib):
     import torch
     if torch.cuda.is_available():
