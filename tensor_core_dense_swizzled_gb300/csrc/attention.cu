@@ -10,33 +10,39 @@
 // probabilities rounded to the input type for the second product (as the
 // register hand-over of the pages does), fp32 accumulation.
 //
-// One CTA computes a 128-row query tile of one head, streaming the keys and
-// values in blocks of 128 rows:
+// One CTA computes a 128-row query tile of one head, streaming keys and
+// values in blocks of 64 rows; two CTAs share an SM (96 KB of shared memory
+// and 256 TMEM columns each), so that one CTA's softmax runs while the
+// other's products occupy the tensor core, and one CTA's start-up and
+// epilogue hide behind the other's main loop.
 //   warp 0, one thread   TMA: the Q tile once, then K_j and V_j into a ring
 //                        of two stages (separate full / empty barriers for K
 //                        and V, so S_j can start before V_j lands).
 //   warp 1, one thread   MMA: S_j = Q K_j^T into TMEM buffer j % 2 (8 MMAs
-//                        of K = 16 over the head dimension), then, once the
-//                        softmax warps have written P_{j-1}, O += P_{j-1}
-//                        V_{j-1} (8 MMAs of 16 keys) into the O accumulator
-//                        in TMEM.  The tensor core therefore computes
-//                        S_{j+1} and P_{j-1} V_{j-1} while the softmax of
-//                        S_j runs.
+//                        of K = 16 over the head dimension, N = 64 keys),
+//                        then, once the softmax warps have written P_{j-1},
+//                        O += P_{j-1} V_{j-1} (4 MMAs of 16 keys, N = 128)
+//                        with P read straight from TMEM -- the Blackwell
+//                        form of the pages' register hand-over: P never
+//                        touches shared memory.
 //   warps 2-5            online softmax, one query row per thread (the TMEM
-//                        lane of its row): tcgen05.ld the 128 scores of S_j,
-//                        release the buffer, mask, take the row max, form
-//                        p = 2^(s * scale * log2 e - m) with the SFU's ex2,
-//                        sum the row, rescale O in TMEM when the reference
-//                        max moved, and store P (16-bit) into 128-byte-
-//                        swizzled shared memory as the K-major A operand of
-//                        the second product.  After the last block: O / l,
-//                        rounded to the output type, stored to global memory.
+//                        lane of its row): tcgen05.ld the 64 scores of S_j,
+//                        mask, take the row max, form p = 2^(s * scale *
+//                        log2 e - m) with the SFU's ex2, sum the row, rescale
+//                        O in TMEM when the reference max moved, and
+//                        tcgen05.st P (16-bit pairs) over the first 32
+//                        columns of S_j's buffer.  After the last block:
+//                        O / l, rounded to the output type, stored to global
+//                        memory.
+// A buffer's next S (block j + 2) is issued only once P_j V_j has completed,
+// since P_j lives in it.
 //
 // The reference max m is raised only when a block's max exceeds it by more
 // than 8 (in log2 units): p then stays <= 2^8, and O and l, always scaled by
 // the same 2^-m, give the same quotient O / l as with the running max, while
-// the O rescale (a TMEM load / multiply / store of the warp's 32 rows)
-// happens only when some row of the warp raised its reference.
+// the O rescale (a TMEM load / multiply / store of the warp's 32 rows, after
+// waiting for the previous P V) happens only when some row of the warp
+// raised its reference.
 //
 // Every wait is bounded (watchdog.cuh); a timeout records its code in the
 // error word, the CTA's roles leave their loops, the MMA thread waits for
@@ -55,33 +61,35 @@
 namespace hg {
 namespace {
 
-constexpr int ATT_THREADS = 192;              // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
-constexpr uint32_t ATT_TILE = 128 * 128 * 2;  // 128 rows x 128 16-bit elements
-constexpr uint32_t ATT_HALF = ATT_TILE / 2;   // one 64-element column block
-constexpr int ATT_STAGES = 2;                 // K / V ring depth
+constexpr int ATT_THREADS = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int ATT_BN = 64;                     // keys per block
+constexpr uint32_t ATT_QTILE = 128 * 128 * 2;  // Q: 128 rows x 128 16-bit elements
+constexpr uint32_t ATT_QHALF = ATT_QTILE / 2;  // one 64-element column block of Q
+constexpr uint32_t ATT_KTILE = ATT_BN * 128 * 2;   // K or V block: 64 rows x 128 elements
+constexpr uint32_t ATT_KHALF = ATT_KTILE / 2;      // one 64-element column block
+constexpr int ATT_STAGES = 2;                  // K / V ring depth
 
 // shared memory, from a 1024-byte-aligned base
 constexpr uint32_t SM_Q = 0;
-constexpr uint32_t SM_K = SM_Q + ATT_TILE;
-constexpr uint32_t SM_V = SM_K + ATT_STAGES * ATT_TILE;
-constexpr uint32_t SM_P = SM_V + ATT_STAGES * ATT_TILE;
-constexpr uint32_t SM_BAR = SM_P + ATT_TILE;
+constexpr uint32_t SM_K = SM_Q + ATT_QTILE;
+constexpr uint32_t SM_V = SM_K + ATT_STAGES * ATT_KTILE;
+constexpr uint32_t SM_BAR = SM_V + ATT_STAGES * ATT_KTILE;
 // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-// s_free[2], p_full, o_done, drain
+// p_full[2], o_done, o_final, drain
 constexpr int ATT_NBAR = 1 + 4 * ATT_STAGES + 2 + 2 + 3;
 constexpr uint32_t SM_MISC = SM_BAR + 8 * ATT_NBAR;
 constexpr uint32_t ATT_SMEM = SM_MISC + 16 + 1024;  // + alignment slack
 
-// TMEM columns: S buffers at 0 and 128, O at 256 (512 allocated)
+// TMEM columns: S / P buffers at 0 and 64, O at 128 (256 allocated)
 constexpr uint32_t TM_S = 0;
-constexpr uint32_t TM_O = 256;
-constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t TM_O = 128;
+constexpr uint32_t TM_COLS = 256;
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
 template <bool BF16>
-__global__ void __launch_bounds__(ATT_THREADS, 1)
+__global__ void __launch_bounds__(ATT_THREADS, 2)
     attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     constexpr int OUT = BF16 ? OUT_BF16 : OUT_F16;
@@ -89,7 +97,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + SM_Q, sK = sbase + SM_K, sV = sbase + SM_V, sP = sbase + SM_P;
+    const uint32_t sQ = sbase + SM_Q, sK = sbase + SM_K, sV = sbase + SM_V;
     const uint32_t bar0 = sbase + SM_BAR;
     const uint32_t q_full = bar0;
     auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
@@ -97,9 +105,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * ATT_STAGES + s); };
     auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * ATT_STAGES + s); };
     auto s_full = [&](int b) { return bar0 + 8u * (1 + 4 * ATT_STAGES + b); };
-    auto s_free = [&](int b) { return bar0 + 8u * (3 + 4 * ATT_STAGES + b); };
-    const uint32_t p_full = bar0 + 8u * (5 + 4 * ATT_STAGES);
-    const uint32_t o_done = bar0 + 8u * (6 + 4 * ATT_STAGES);
+    // one P barrier per buffer: the softmax may finish P_{j+1} before the
+    // MMA thread has seen P_j, which would complete two phases of a single
+    // barrier unobserved
+    auto p_full = [&](int b) { return bar0 + 8u * (3 + 4 * ATT_STAGES + b); };
+    // o_done completes once per P V; the softmax warps wait on it only when
+    // they rescale O, so they may fall two phases behind -- the end of the
+    // last P V therefore has a barrier of its own
+    const uint32_t o_done = bar0 + 8u * (5 + 4 * ATT_STAGES);
+    const uint32_t o_final = bar0 + 8u * (6 + 4 * ATT_STAGES);
     const uint32_t drain = bar0 + 8u * (7 + 4 * ATT_STAGES);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + SM_MISC);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + SM_MISC + 4);
@@ -115,7 +129,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     // q0 + 127 + skv - sq under the causal mask
     int kv_end = p.skv;
     if (p.causal) kv_end = min(p.skv, q0 + 128 + (p.skv - p.sq));
-    const int nkv = (kv_end + 127) / 128;
+    const int nkv = (kv_end + ATT_BN - 1) / ATT_BN;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -127,10 +141,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full(b), 1);
-            mbar_init(s_free(b), 4);
+            mbar_init(p_full(b), 4);
         }
-        mbar_init(p_full, 4);
         mbar_init(o_done, 1);
+        mbar_init(o_final, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -151,22 +165,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, ATT_TILE);
+            mbar_arrive_expect_tx(q_full, ATT_QTILE);
             tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
-            tma_load_3d(sQ + ATT_HALF, &tmQ, q_full, 64, q0, bh);
+            tma_load_3d(sQ + ATT_QHALF, &tmQ, q_full, 64, q0, bh);
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < nkv; ++j) {
                 const int s = j & 1;
                 const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
                 if (!wait_bounded(k_empty(s), ph ^ 1u, wc, timeout_code(ROLE_PRODUCER, s))) break;
-                mbar_arrive_expect_tx(k_full(s), ATT_TILE);
-                tma_load_3d(sK + s * ATT_TILE, &tmK, k_full(s), 0, j * 128, bh);
-                tma_load_3d(sK + s * ATT_TILE + ATT_HALF, &tmK, k_full(s), 64, j * 128, bh);
+                mbar_arrive_expect_tx(k_full(s), ATT_KTILE);
+                tma_load_3d(sK + s * ATT_KTILE, &tmK, k_full(s), 0, j * ATT_BN, bh);
+                tma_load_3d(sK + s * ATT_KTILE + ATT_KHALF, &tmK, k_full(s), 64, j * ATT_BN, bh);
                 ++issued_k;
                 if (!wait_bounded(v_empty(s), ph ^ 1u, wc, timeout_code(ROLE_PRODUCER, 2 + s))) break;
-                mbar_arrive_expect_tx(v_full(s), ATT_TILE);
-                tma_load_3d(sV + s * ATT_TILE, &tmV, v_full(s), 0, j * 128, bh);
-                tma_load_3d(sV + s * ATT_TILE + ATT_HALF, &tmV, v_full(s), 64, j * 128, bh);
+                mbar_arrive_expect_tx(v_full(s), ATT_KTILE);
+                tma_load_3d(sV + s * ATT_KTILE, &tmV, v_full(s), 0, j * ATT_BN, bh);
+                tma_load_3d(sV + s * ATT_KTILE + ATT_KHALF, &tmV, v_full(s), 64, j * ATT_BN, bh);
                 ++issued_v;
             }
             // copies still in flight land before the CTA leaves (immediate on
@@ -181,27 +195,25 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t tO = tmem_base + TM_O;
-            bool ok = wait_bounded(q_full, 0, wc, timeout_code(ROLE_MMA, 0x300));
+            bool ok = wait_bounded(q_full, 0, wc, timeout_code(ROLE_MMA, 0x200));
             const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);
-            const uint64_t pdesc = sdesc_sw128(sP, 16, 1024);
-            // O += P_t V_t: P K-major (two 64-key blocks 16 KB apart, 32 bytes
-            // per 16 keys); V MN-major (two 64-column blocks 16 KB apart,
-            // 2 KB per 16 keys)
+            // O += P_t V_t: P from TMEM (8 columns per 16 keys); V MN-major
+            // (two 64-column blocks 8 KB apart, 2 KB per 16 keys)
             auto issue_pv = [&](int t) -> bool {
                 const int ts = t & 1;
-                if (!wait_bounded(p_full, static_cast<uint32_t>(t) & 1u, wc, timeout_code(ROLE_MMA, 0x301)))
+                if (!wait_bounded(p_full(ts), static_cast<uint32_t>(t >> 1) & 1u, wc,
+                                  timeout_code(ROLE_MMA, 0x300 + ts)))
                     return false;
                 if (!wait_bounded(v_full(ts), static_cast<uint32_t>(t >> 1) & 1u, wc,
                                   timeout_code(ROLE_MMA, 0x302 + ts)))
                     return false;
                 tc_fence_after();
-                const uint64_t vdesc = sdesc_sw128(sV + ts * ATT_TILE, ATT_HALF, 1024);
+                const uint64_t vdesc = sdesc_sw128(sV + ts * ATT_KTILE, ATT_KHALF, 1024);
+                const uint32_t tP = tmem_base + TM_S + 64u * ts;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t poff = (kk >> 2) * ATT_HALF + (kk & 3) * 32;
-                    umma_f16(tO, pdesc + (poff >> 4), vdesc + ((kk * 2048u) >> 4), p.idesc_o,
-                             (t > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < ATT_BN / 16; ++kk)
+                    umma_f16_tmem_a(tO, tP + 8u * kk, vdesc + ((kk * 2048u) >> 4), p.idesc_o,
+                                    (t > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(v_empty(ts));
                 umma_commit(o_done);
                 return true;
@@ -213,24 +225,26 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     ok = false;
                     break;
                 }
-                if (j >= 2 && !wait_bounded(s_free(s), static_cast<uint32_t>((j - 2) >> 1) & 1u, wc,
+                // buffer s holds P_{j-2} until P_{j-2} V_{j-2} has completed
+                if (j >= 2 && !wait_bounded(o_done, static_cast<uint32_t>(j - 2) & 1u, wc,
                                             timeout_code(ROLE_MMA, 0x100 + s))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t kdesc = sdesc_sw128(sK + s * ATT_TILE, 16, 1024);
-                const uint32_t tS = tmem_base + TM_S + 128u * s;
+                const uint64_t kdesc = sdesc_sw128(sK + s * ATT_KTILE, 16, 1024);
+                const uint32_t tS = tmem_base + TM_S + 64u * s;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * ATT_HALF + (kk & 3) * 32;
-                    umma_f16(tS, qdesc + (off >> 4), kdesc + (off >> 4), p.idesc_s, kk > 0 ? 1u : 0u);
+                    const uint32_t qoff = (kk >> 2) * ATT_QHALF + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * ATT_KHALF + (kk & 3) * 32;
+                    umma_f16(tS, qdesc + (qoff >> 4), kdesc + (koff >> 4), p.idesc_s, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(k_empty(s));
                 umma_commit(s_full(s));
                 if (j >= 1 && !issue_pv(j - 1)) ok = false;
             }
-            if (ok) issue_pv(nkv - 1);
+            if (ok && issue_pv(nkv - 1)) umma_commit(o_final);
             umma_commit(drain);
             wait_bounded(drain, 0, wc, 0, /*honor_abort=*/false);
         }
@@ -245,33 +259,32 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         const float c = p.scale_log2;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        uint32_t sv[4][32];
+        uint32_t sv[64];
         for (int j = 0; j < nkv; ++j) {
             const int b = j & 1;
+            const uint32_t tS = tmem_base + lane_addr + TM_S + 64u * b;
             if (!wait_bounded_warp(s_full(b), static_cast<uint32_t>(j >> 1) & 1u, wc,
                                    timeout_code(ROLE_EPILOGUE, b))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            tmem_ld64(tS, sv);
+            const int kbase = j * ATT_BN;
+            if (kbase + ATT_BN > lim) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32(tmem_base + lane_addr + TM_S + 128u * b + 32u * q, sv[q]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(b));
-            const int kbase = j * 128;
-            if (kbase + 128 > lim) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (kbase + q * 32 + i >= lim) sv[q][i] = f2u(-INFINITY);
+                for (int i = 0; i < 64; ++i)
+                    if (kbase + i >= lim) sv[i] = f2u(-INFINITY);
             }
-            float mx = -INFINITY;
+            // row max and sum in 8 independent partials (short dependency
+            // chains: few warps share an SM sub-partition)
+            float pm[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int t = 0; t < 8; ++t) pm[t] = fmaxf(u2f(sv[t]), u2f(sv[t + 8]));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, u2f(sv[q][i]));
+            for (int i = 16; i < 64; ++i) pm[i & 7] = fmaxf(pm[i & 7], u2f(sv[i]));
+            float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             mx *= c;
             float alpha = 1.f;
             const bool raise = mx > m_ref + 8.f;
@@ -279,57 +292,45 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 alpha = ex2_approx(m_ref - mx);
                 m_ref = mx;
             }
-            float sum = 0.f;
+            float ps[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int t = 0; t < 8; ++t) ps[t] = 0.f;
+            uint32_t pk[32];  // P as 16-bit pairs, key 2i in the low half of pk[i]
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float e = ex2_approx(fmaf(u2f(sv[q][i]), c, -m_ref));
-                    sum += e;
-                    sv[q][i] = f2u(e);
-                }
+            for (int i = 0; i < 64; i += 2) {
+                const float e0 = ex2_approx(fmaf(u2f(sv[i]), c, -m_ref));
+                const float e1 = ex2_approx(fmaf(u2f(sv[i + 1]), c, -m_ref));
+                ps[i & 7] += e0;
+                ps[(i + 1) & 7] += e1;
+                pk[i / 2] = pack2<OUT>(f2u(e0), f2u(e1));
+            }
+            const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             l = l * alpha + sum;
-            if (j >= 1) {
-                // P_{j-1} V_{j-1} has finished: the P buffer is free and O holds
-                // every earlier block
+            if (j >= 1 && __any_sync(0xFFFFFFFFu, raise)) {
+                // O must hold every earlier block before it is rescaled
                 if (!wait_bounded_warp(o_done, static_cast<uint32_t>(j - 1) & 1u, wc,
                                        timeout_code(ROLE_EPILOGUE, 0x10))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xFFFFFFFFu, raise)) {
 #pragma unroll 1
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem_base + lane_addr + TM_O + 32u * q, o);
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem_base + lane_addr + TM_O + 32u * q, o);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-                        tmem_st32(tmem_base + lane_addr + TM_O + 32u * q, o);
-                    }
+                    for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+                    tmem_st32(tmem_base + lane_addr + TM_O + 32u * q, o);
                 }
             }
-            // P row into the swizzled K-major operand: keys 64 * kb .. 64 * kb + 63
-            // in block kb; 16-byte chunk ch of the row at chunk ch ^ (row & 7)
-            const uint32_t prow = sP + static_cast<uint32_t>(row) * 128u;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t ch = static_cast<uint32_t>((q & 1) * 4 + t);
-                    const uint32_t addr = prow + (q >> 1) * ATT_HALF + ((ch ^ (row & 7)) << 4);
-                    st_shared_v4(addr, pack2<OUT>(sv[q][8 * t], sv[q][8 * t + 1]),
-                                 pack2<OUT>(sv[q][8 * t + 2], sv[q][8 * t + 3]),
-                                 pack2<OUT>(sv[q][8 * t + 4], sv[q][8 * t + 5]),
-                                 pack2<OUT>(sv[q][8 * t + 6], sv[q][8 * t + 7]));
-                }
-            fence_proxy_async_smem();
+            // P over the first 32 columns of the buffer (its scores are in
+            // registers already)
+            tmem_st32(tS, pk);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_full(b));
         }
-        if (ok && wait_bounded_warp(o_done, static_cast<uint32_t>(nkv - 1) & 1u, wc,
-                                    timeout_code(ROLE_EPILOGUE, 0x11))) {
+        if (ok && wait_bounded_warp(o_final, 0, wc, timeout_code(ROLE_EPILOGUE, 0x11))) {
             tc_fence_after();
             const float inv = 1.f / l;
             const bool store = qi < p.sq;

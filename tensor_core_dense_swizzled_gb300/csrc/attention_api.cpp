@@ -80,9 +80,10 @@ hgemm_status_t attn_run(hgemm_attn_plan_s *p, const void *Q, const void *K, cons
         hgemm_status_t st;
         st = hg::encode_map_batched(&p->tmQ, Q, bf, p->d, p->sq, p->bh, p->d, p->sq * p->d, 64, 128);
         if (st != HGEMM_OK) return st;
-        st = hg::encode_map_batched(&p->tmK, K, bf, p->d, p->skv, p->bh, p->d, p->skv * p->d, 64, 128);
+        // K and V stream in blocks of 64 rows
+        st = hg::encode_map_batched(&p->tmK, K, bf, p->d, p->skv, p->bh, p->d, p->skv * p->d, 64, 64);
         if (st != HGEMM_OK) return st;
-        st = hg::encode_map_batched(&p->tmV, V, bf, p->d, p->skv, p->bh, p->d, p->skv * p->d, 64, 128);
+        st = hg::encode_map_batched(&p->tmV, V, bf, p->d, p->skv, p->bh, p->d, p->skv * p->d, 64, 64);
         if (st != HGEMM_OK) return st;
         p->mQ = Q; p->mK = K; p->mV = V;
         p->maps_ok = true;
@@ -94,8 +95,9 @@ hgemm_status_t attn_run(hgemm_attn_plan_s *p, const void *Q, const void *K, cons
     ap.nqt = static_cast<int32_t>((p->sq + 127) / 128);
     ap.causal = p->causal;
     ap.scale_log2 = static_cast<float>(static_cast<double>(p->scale) * 1.4426950408889634);
-    // S = Q K^T: both operands K-major; O += P V: P K-major, V MN-major
-    ap.idesc_s = hg::idesc_f16(static_cast<uint32_t>(bf), 0, 0, 128, 128);
+    // S = Q K^T (N = 64 keys): both operands K-major; O += P V: P from
+    // tensor memory, V MN-major
+    ap.idesc_s = hg::idesc_f16(static_cast<uint32_t>(bf), 0, 0, 128, 64);
     ap.idesc_o = hg::idesc_f16(static_cast<uint32_t>(bf), 0, 1, 128, 128);
     ap.O = O;
     ap.err = p->err;

@@ -178,15 +178,15 @@ cudaError_t launch_watchdog_selftest(int32_t *err, uint64_t timeout_ns, cudaStre
 
 // Attention forward (attention.cu): O = softmax(scale Q K^T [causal]) V with
 // Q [bh][sq][128], K, V [bh][skv][128], O [bh][sq][128], 16-bit, dense.
-// One CTA per 128-query tile; the tensor maps cover Q, K and V as
-// (128 elements, rows, bh) with 64 x 128 boxes.
+// One CTA per 128-query tile, two per SM; the tensor maps cover Q, K and V
+// as (128 elements, rows, bh) with 64 x 128 boxes for Q and 64 x 64 for K, V.
 struct AttnParams {
     int32_t bh, sq, skv;  // heads x batch, query rows, key rows
     int32_t nqt;          // query tiles per head: ceil(sq / 128)
     int32_t causal;       // key j allowed for query i when j <= i + skv - sq
     float scale_log2;     // softmax scale x log2(e), > 0
-    uint32_t idesc_s;     // S = Q K^T: M 128, N 128 keys, both K-major
-    uint32_t idesc_o;     // O += P V: M 128, N 128, P K-major, V MN-major
+    uint32_t idesc_s;     // S = Q K^T: M 128, N 64 keys, both K-major
+    uint32_t idesc_o;     // O += P V: M 128, N 128, P from TMEM, V MN-major
     void *O;
     int32_t *err;
     uint64_t timeout_ns;
