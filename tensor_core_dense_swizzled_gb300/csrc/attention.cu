@@ -18,14 +18,17 @@
 //   warp 0, one thread   TMA: the Q tile once, then K_j and V_j into a ring
 //                        of two stages (separate full / empty barriers for K
 //                        and V, so S_j can start before V_j lands).
-//   warp 1, one thread   MMA: S_j = Q K_j^T into TMEM buffer j % 2 (8 MMAs
-//                        of K = 16 over the head dimension, N = 64 keys),
-//                        then, once the softmax warps have written P_{j-1},
-//                        O += P_{j-1} V_{j-1} (4 MMAs of 16 keys, N = 128)
-//                        with P read straight from TMEM -- the Blackwell
-//                        form of the pages' register hand-over: P never
-//                        touches shared memory.
-//   warps 2-5            online softmax, one query row per thread (the TMEM
+//   warp 1, one thread   MMA for the scores: S_j = Q K_j^T into TMEM buffer
+//                        j % 2 (8 MMAs of K = 16 over the head dimension,
+//                        N = 64 keys).
+//   warp 2, one thread   MMA for the output: once the softmax warps have
+//                        written P_j, O += P_j V_j (4 MMAs of 16 keys,
+//                        N = 128) with P read straight from TMEM -- the
+//                        Blackwell form of the pages' register hand-over: P
+//                        never touches shared memory.  Issuing a tcgen05.mma
+//                        costs its thread about as long as a 64-key MMA
+//                        runs, so the two products get a thread each.
+//   warps 3-6            online softmax, one query row per thread (the TMEM
 //                        lane of its row): tcgen05.ld the 64 scores of S_j,
 //                        mask, take the row max, form p = 2^(s * scale *
 //                        log2 e - m) with the SFU's ex2, sum the row, rescale
@@ -35,7 +38,8 @@
 //                        O / l, rounded to the output type, stored to global
 //                        memory.
 // A buffer's next S (block j + 2) is issued only once P_j V_j has completed,
-// since P_j lives in it.
+// since P_j lives in it; a K or V stage is reloaded once the S, or the P V,
+// that read it has completed (their own barriers say so).
 //
 // The reference max m is raised only when a block's max exceeds it by more
 // than 8 (in log2 units): p then stays <= 2^8, and O and l, always scaled by
@@ -61,7 +65,7 @@
 namespace hg {
 namespace {
 
-constexpr int ATT_THREADS = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int ATT_THREADS = 224;               // warp 0 TMA, warps 1-2 MMA, warps 3-6 softmax
 constexpr int ATT_BN = 64;                     // keys per block
 constexpr uint32_t ATT_QTILE = 128 * 128 * 2;  // Q: 128 rows x 128 16-bit elements
 constexpr uint32_t ATT_QHALF = ATT_QTILE / 2;  // one 64-element column block of Q
@@ -74,9 +78,9 @@ constexpr uint32_t SM_Q = 0;
 constexpr uint32_t SM_K = SM_Q + ATT_QTILE;
 constexpr uint32_t SM_V = SM_K + ATT_STAGES * ATT_KTILE;
 constexpr uint32_t SM_BAR = SM_V + ATT_STAGES * ATT_KTILE;
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-// p_full[2], o_done, o_final, drain
-constexpr int ATT_NBAR = 1 + 4 * ATT_STAGES + 2 + 2 + 3;
+// barriers: q_full, k_full[2], v_full[2], s_full[2], pv_done[2], p_full[2],
+// o_final, drain[2]
+constexpr int ATT_NBAR = 1 + 2 * ATT_STAGES + 2 + 2 + 2 + 1 + 2;
 constexpr uint32_t SM_MISC = SM_BAR + 8 * ATT_NBAR;
 constexpr uint32_t ATT_SMEM = SM_MISC + 16 + 1024;  // + alignment slack
 
@@ -100,21 +104,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 2)
     const uint32_t sQ = sbase + SM_Q, sK = sbase + SM_K, sV = sbase + SM_V;
     const uint32_t bar0 = sbase + SM_BAR;
     const uint32_t q_full = bar0;
+    // Every [2] barrier entry below completes once per use of its stage or
+    // buffer, in order, and no waiter can fall two phases behind an entry
+    // (each wait names the event the entry's next phase needs).
     auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
-    auto k_empty = [&](int s) { return bar0 + 8u * (1 + ATT_STAGES + s); };
-    auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * ATT_STAGES + s); };
-    auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * ATT_STAGES + s); };
-    auto s_full = [&](int b) { return bar0 + 8u * (1 + 4 * ATT_STAGES + b); };
-    // one P barrier per buffer: the softmax may finish P_{j+1} before the
-    // MMA thread has seen P_j, which would complete two phases of a single
-    // barrier unobserved
-    auto p_full = [&](int b) { return bar0 + 8u * (3 + 4 * ATT_STAGES + b); };
-    // o_done completes once per P V; the softmax warps wait on it only when
-    // they rescale O, so they may fall two phases behind -- the end of the
-    // last P V therefore has a barrier of its own
-    const uint32_t o_done = bar0 + 8u * (5 + 4 * ATT_STAGES);
-    const uint32_t o_final = bar0 + 8u * (6 + 4 * ATT_STAGES);
-    const uint32_t drain = bar0 + 8u * (7 + 4 * ATT_STAGES);
+    auto v_full = [&](int s) { return bar0 + 8u * (3 + s); };
+    auto s_full = [&](int b) { return bar0 + 8u * (5 + b); };   // S_j done (also: K_j read)
+    auto pv_done = [&](int b) { return bar0 + 8u * (7 + b); };  // P_j V_j done (also: V_j read)
+    auto p_full = [&](int b) { return bar0 + 8u * (9 + b); };
+    const uint32_t o_final = bar0 + 8u * 11;
+    auto drain = [&](int r) { return bar0 + 8u * (12 + r); };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + SM_MISC);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + SM_MISC + 4);
 
@@ -133,19 +132,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 2)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < ATT_STAGES; ++s) {
-            mbar_init(k_full(s), 1);
-            mbar_init(k_empty(s), 1);
-            mbar_init(v_full(s), 1);
-            mbar_init(v_empty(s), 1);
-        }
         for (int b = 0; b < 2; ++b) {
+            mbar_init(k_full(b), 1);
+            mbar_init(v_full(b), 1);
             mbar_init(s_full(b), 1);
+            mbar_init(pv_done(b), 1);
             mbar_init(p_full(b), 4);
+            mbar_init(drain(b), 1);
         }
-        mbar_init(o_done, 1);
         mbar_init(o_final, 1);
-        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmQ);
@@ -172,12 +167,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 2)
             for (int j = 0; j < nkv; ++j) {
                 const int s = j & 1;
                 const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-                if (!wait_bounded(k_empty(s), ph ^ 1u, wc, timeout_code(ROLE_PRODUCER, s))) break;
+                if (j >= 2 && !wait_bounded(s_full(s), ph ^ 1u, wc, timeout_code(ROLE_PRODUCER, s))) break;
                 mbar_arrive_expect_tx(k_full(s), ATT_KTILE);
                 tma_load_3d(sK + s * ATT_KTILE, &tmK, k_full(s), 0, j * ATT_BN, bh);
                 tma_load_3d(sK + s * ATT_KTILE + ATT_KHALF, &tmK, k_full(s), 64, j * ATT_BN, bh);
                 ++issued_k;
-                if (!wait_bounded(v_empty(s), ph ^ 1u, wc, timeout_code(ROLE_PRODUCER, 2 + s))) break;
+                if (j >= 2 && !wait_bounded(pv_done(s), ph ^ 1u, wc, timeout_code(ROLE_PRODUCER, 2 + s))) break;
                 mbar_arrive_expect_tx(v_full(s), ATT_KTILE);
                 tma_load_3d(sV + s * ATT_KTILE, &tmV, v_full(s), 0, j * ATT_BN, bh);
                 tma_load_3d(sV + s * ATT_KTILE + ATT_KHALF, &tmV, v_full(s), 64, j * ATT_BN, bh);
@@ -192,45 +187,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 2)
                 wait_bounded(v_full(j & 1), static_cast<uint32_t>(j >> 1) & 1u, wc, 0, false);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA: scores
         if (lane == 0) {
-            const uint32_t tO = tmem_base + TM_O;
             bool ok = wait_bounded(q_full, 0, wc, timeout_code(ROLE_MMA, 0x200));
             const uint64_t qdesc = sdesc_sw128(sQ, 16, 1024);
-            // O += P_t V_t: P from TMEM (8 columns per 16 keys); V MN-major
-            // (two 64-column blocks 8 KB apart, 2 KB per 16 keys)
-            auto issue_pv = [&](int t) -> bool {
-                const int ts = t & 1;
-                if (!wait_bounded(p_full(ts), static_cast<uint32_t>(t >> 1) & 1u, wc,
-                                  timeout_code(ROLE_MMA, 0x300 + ts)))
-                    return false;
-                if (!wait_bounded(v_full(ts), static_cast<uint32_t>(t >> 1) & 1u, wc,
-                                  timeout_code(ROLE_MMA, 0x302 + ts)))
-                    return false;
-                tc_fence_after();
-                const uint64_t vdesc = sdesc_sw128(sV + ts * ATT_KTILE, ATT_KHALF, 1024);
-                const uint32_t tP = tmem_base + TM_S + 64u * ts;
-#pragma unroll
-                for (int kk = 0; kk < ATT_BN / 16; ++kk)
-                    umma_f16_tmem_a(tO, tP + 8u * kk, vdesc + ((kk * 2048u) >> 4), p.idesc_o,
-                                    (t > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(v_empty(ts));
-                umma_commit(o_done);
-                return true;
-            };
             for (int j = 0; ok && j < nkv; ++j) {
                 const int s = j & 1;
                 if (!wait_bounded(k_full(s), static_cast<uint32_t>(j >> 1) & 1u, wc,
-                                  timeout_code(ROLE_MMA, s))) {
-                    ok = false;
+                                  timeout_code(ROLE_MMA, s)))
                     break;
-                }
                 // buffer s holds P_{j-2} until P_{j-2} V_{j-2} has completed
-                if (j >= 2 && !wait_bounded(o_done, static_cast<uint32_t>(j - 2) & 1u, wc,
-                                            timeout_code(ROLE_MMA, 0x100 + s))) {
-                    ok = false;
+                if (j >= 2 && !wait_bounded(pv_done(s), static_cast<uint32_t>((j - 2) >> 1) & 1u, wc,
+                                            timeout_code(ROLE_MMA, 0x100 + s)))
                     break;
-                }
                 tc_fence_after();
                 const uint64_t kdesc = sdesc_sw128(sK + s * ATT_KTILE, 16, 1024);
                 const uint32_t tS = tmem_base + TM_S + 64u * s;
@@ -240,13 +209,38 @@ __global__ void __launch_bounds__(ATT_THREADS, 2)
                     const uint32_t koff = (kk >> 2) * ATT_KHALF + (kk & 3) * 32;
                     umma_f16(tS, qdesc + (qoff >> 4), kdesc + (koff >> 4), p.idesc_s, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(k_empty(s));
                 umma_commit(s_full(s));
-                if (j >= 1 && !issue_pv(j - 1)) ok = false;
             }
-            if (ok && issue_pv(nkv - 1)) umma_commit(o_final);
-            umma_commit(drain);
-            wait_bounded(drain, 0, wc, 0, /*honor_abort=*/false);
+            umma_commit(drain(0));
+            wait_bounded(drain(0), 0, wc, 0, /*honor_abort=*/false);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ MMA: output
+        if (lane == 0) {
+            const uint32_t tO = tmem_base + TM_O;
+            bool ok = true;
+            // O += P_t V_t: P from TMEM (8 columns per 16 keys); V MN-major
+            // (two 64-column blocks 8 KB apart, 2 KB per 16 keys)
+            for (int t = 0; t < nkv; ++t) {
+                const int ts = t & 1;
+                const uint32_t ph = static_cast<uint32_t>(t >> 1) & 1u;
+                if (!wait_bounded(p_full(ts), ph, wc, timeout_code(ROLE_MMA, 0x300 + ts)) ||
+                    !wait_bounded(v_full(ts), ph, wc, timeout_code(ROLE_MMA, 0x302 + ts))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t vdesc = sdesc_sw128(sV + ts * ATT_KTILE, ATT_KHALF, 1024);
+                const uint32_t tP = tmem_base + TM_S + 64u * ts;
+#pragma unroll
+                for (int kk = 0; kk < ATT_BN / 16; ++kk)
+                    umma_f16_tmem_a(tO, tP + 8u * kk, vdesc + ((kk * 2048u) >> 4), p.idesc_o,
+                                    (t > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(pv_done(ts));
+            }
+            if (ok) umma_commit(o_final);
+            umma_commit(drain(1));
+            wait_bounded(drain(1), 0, wc, 0, /*honor_abort=*/false);
         }
     } else {
         // ------------------------------------------------------------ softmax warps
@@ -308,7 +302,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 2)
             l = l * alpha + sum;
             if (j >= 1 && __any_sync(0xFFFFFFFFu, raise)) {
                 // O must hold every earlier block before it is rescaled
-                if (!wait_bounded_warp(o_done, static_cast<uint32_t>(j - 1) & 1u, wc,
+                if (!wait_bounded_warp(pv_done((j - 1) & 1), static_cast<uint32_t>((j - 1) >> 1) & 1u, wc,
                                        timeout_code(ROLE_EPILOGUE, 0x10))) {
                     ok = false;
                     break;

@@ -32,6 +32,8 @@ __host__ __device__ constexpr int32_t timeout_code(uint32_t role, uint32_t index
 
 // Hard cap on polling iterations, independent of the clock.
 constexpr uint32_t kMaxWaitIterations = 1u << 30;
+// mbarrier polls between two reads of the clock and the abort flag.
+constexpr int kPollsPerCheck = 16;
 
 struct WaitCtl {
     volatile int32_t *abort_flag;  // shared memory, CTA scope
@@ -46,7 +48,11 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0; it < kMaxWaitIterations; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        // several polls per clock and abort check: those reads would
+        // otherwise dominate the loop and delay seeing the phase complete
+#pragma unroll 1
+        for (int k = 0; k < kPollsPerCheck; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
         if (honor_abort && *c.abort_flag) return false;
         if (globaltimer_ns() - t0 > c.timeout_ns) break;
     }
