@@ -189,15 +189,21 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- helpers
 
-def kernel_hash() -> str:
+def kernel_hash(attention: bool = False) -> str:
+    """Hash of the sources the workload's kernels are built from: the GEMM
+    files, or the attention files, plus the shared headers."""
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "tensor_core_dense_swizzled_gb300", "csrc", "*"))):
+        base = os.path.basename(f)
+        shared = base.endswith((".h", ".cuh"))
+        if not shared and base.startswith("attention") != attention:
+            continue
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload: str):
+def committed_traffic(workload: str, attention: bool = False):
     """DRAM bytes per launch of the main kernel from a committed ncu capture,
     or None when absent or taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -205,7 +211,7 @@ def committed_traffic(workload: str):
         with open(path) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("kernel_hash") == kernel_hash():
+        if e and e.get("kernel_hash") == kernel_hash(attention):
             return e.get("dram_bytes_per_launch")
     except Exception:
         pass
@@ -653,7 +659,7 @@ def run_attention_ours(args, w, world, rank, local, pg):
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
     peak = peaks["bf16_sustained"] if sustained else peaks["bf16"]
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": committed_traffic(w.name),
+            "frac": achieved / peak, "traffic": committed_traffic(w.name, attention=True),
             "peak_kind": ("sustained" if sustained else "burst") + f" bf16, {peaks['source']}",
             "algorithmic_per_launch": flops, "launch_ms": avg_launch_ms, "kernels_per_launch": 1}
     e2e = None

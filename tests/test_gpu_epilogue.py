@@ -4,8 +4,10 @@ D = act(alpha * rs[i] * cs[j] * (A.B) + beta * C_prev + bias[j]) on every
 path that writes C: CTA pairs (whole tiles, K halves, stream-K closing,
 first-wave dealing), single-CTA tiles with TMA or predicated stores, the
 skinny path unsplit and split-K, and K = 0.  The oracle's epilogue gives
-the bound: |D - Dref| <= tol * DenD (tol 1e-3 for fp32 C, 4e-3 for 16-bit
-C), entries with DenD = 0 exact.  C_prev is read in the output type, so the
+the bound: |D - Dref| <= tol * DenD (tol 1e-3 for fp32 C, 4e-3 for fp16 and
+5e-3 for bf16 C: the product's fp32 sums plus one rounding to the output
+type, whose unit roundoff is 2^-11 for fp16 and 2^-8 for bf16), entries with
+DenD = 0 exact.  C_prev is read in the output type, so the
 oracle takes the same decoded values.
 """
 import types
@@ -20,7 +22,7 @@ from test_gpu_parity import DT, ORACLE_DT, TORCH, bits, dev, read_c, span  # noq
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"f32": 1e-3, "f16": 4e-3, "bf16": 4e-3}
+TOL = {"f32": 1e-3, "f16": 4e-3, "bf16": 5e-3}
 
 EPILOGUES = {
     "bias_relu": dict(alpha=1.5, beta=0.0, bias=True, rs=False, cs=False, act=H.HGEMM_ACT_RELU),

@@ -5,7 +5,8 @@ fp32 accumulation, its instruction taking twice the K of a 16-bit type, and
 the same page's FP8 kernel configurations take K blocks of 128 one-byte
 elements where bf16 takes 64.  Each product of two 8-bit values is exact in
 fp32, so the bound is the 16-bit inputs' one: max |C - Cref| / sum |a||b|
-<= 1e-3 (fp32 out) or 4e-3 (16-bit out), and bit-exact for small integers.
+<= 1e-3 (fp32 out), 4e-3 (fp16 out) or 5e-3 (bf16 out), and bit-exact for
+small integers.
 
 8-bit operands are read in place in the layout the tensor cores take: A
 M x K and B stored N x K (trans_b), 16-byte aligned rows.  Every case runs
@@ -143,7 +144,7 @@ def test_fp8_dequant_epilogue(dev):
     D, DenD = oracle.epilogue(Cref[0], Den[0], alpha=0.5, bias=bias.double().numpy(),
                               row_scale=rs[:8].double().numpy(), col_scale=cs.double().numpy(),
                               act=oracle.ACT_RELU)
-    assert oracle.normalized_error(got[0], D, DenD) <= 4e-3
+    assert oracle.normalized_error(got[0], D, DenD) <= TOL["bf16"]
 
 
 def test_fp8_host_buffers(dev):

@@ -2,12 +2,14 @@
 
 Acceptance (fixed by the method's statement of the target):
   * integer-valued inputs whose sums are exact in fp32: bit-exact;
-  * otherwise ``max |C - Cref| / Den <= 1e-3`` for fp32 output and
-    ``<= 4e-3`` for fp16/bf16 output, with ``Den = sum_k |A_ik||B_kj|``
-    (entries with ``Den == 0`` must be exactly zero).
+  * otherwise ``max |C - Cref| / Den <= 1e-3`` for fp32 output, ``<= 4e-3``
+    for fp16 and ``<= 5e-3`` for bf16 output, with
+    ``Den = sum_k |A_ik||B_kj|`` (entries with ``Den == 0`` must be exactly
+    zero).
 These are bounds, not fudge: fp32 accumulation of K products in any order is
-within about K * 2^-24 * Den (4.9e-4 at K = 8192) and rounding the result to
-fp16 / bf16 adds at most 2^-11 / 2^-9 relative to |C| <= Den.
+within K * 2^-24 * Den (K * 2^-23 * Den if the hardware truncates; 9.8e-4 at
+K = 8192) and rounding the result to fp16 / bf16 adds at most its unit
+roundoff, 2^-11 / 2^-8 (11 / 8 significant bits), relative to |C| <= Den.
 
 Small cases are compared element by element with the full oracle product;
 the full-size workloads, in the launch configuration the bench times, are
@@ -25,7 +27,7 @@ pytestmark = pytest.mark.gpu
 
 DT = {"f16": H.HGEMM_F16, "bf16": H.HGEMM_BF16, "f32": H.HGEMM_F32}
 ORACLE_DT = {"f16": 0, "bf16": 1}
-TOL = {"f32": 1e-3, "f16": 4e-3, "bf16": 4e-3}
+TOL = {"f32": 1e-3, "f16": 4e-3, "bf16": 5e-3}
 TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 
 

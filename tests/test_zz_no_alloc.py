@@ -6,7 +6,8 @@ cudaMalloc's synchronisation).  Its scratch is a fixed array inside the
 library that every call shares, so two calls in a row must both give the
 same answer as the planned path (hgemm_plan_create / hgemm_run), within the
 tolerance the other parity tests use: max |C - Cref| / sum_k |A_ik||B_kj|
-<= 4e-3 for bf16 output.  This file is collected last on purpose and builds
+<= 5e-3 for bf16 output (fp32 sums plus one rounding to bf16, unit roundoff
+2^-8), 4e-3 for fp16 output.  This file is collected last on purpose and builds
 everything it needs, so it also passes alone in a fresh process.
 """
 import ctypes
@@ -60,7 +61,7 @@ def test_no_alloc_matches_planned_path_twice(dev):
         H.hgemm_plan_destroy(plan)
     Cref, Den = oracle.gemm(bits(A), bits(B), 1, w.M, w.N, w.K, w.lda, w.ldb)
     planned = oracle.decode(bits(C_plan), 1).reshape(1, w.M, w.N)
-    assert oracle.normalized_error(planned, Cref, Den) <= 4e-3
+    assert oracle.normalized_error(planned, Cref, Den) <= 5e-3
     # two calls in a row through the C ABI: the shared scratch keeps the first
     # call's contents and must not disturb the second
     outs = []
@@ -72,8 +73,8 @@ def test_no_alloc_matches_planned_path_twice(dev):
         got = oracle.decode(bits(C), 1).reshape(1, w.M, w.N)
         diff = np.abs(got - planned)
         nz = Den > 0
-        assert np.max(diff[nz] / Den[nz]) <= 4e-3
-        assert oracle.normalized_error(got, Cref, Den) <= 4e-3
+        assert np.max(diff[nz] / Den[nz]) <= 5e-3
+        assert oracle.normalized_error(got, Cref, Den) <= 5e-3
         outs.append(C.cpu())
     assert torch.equal(outs[0], outs[1])
 
@@ -93,7 +94,8 @@ def test_no_alloc_small_shapes_and_outputs(dev):
             Cref, Den = oracle.gemm(bits(A), bits(B), 0, M, N, K, K, N)
             got = C.cpu().double().numpy()[None] if dout == H.HGEMM_F32 else \
                 oracle.decode(bits(C), 0 if dout == H.HGEMM_F16 else 1).reshape(1, M, N)
-            assert oracle.normalized_error(got, Cref, Den) <= (1e-3 if dout == H.HGEMM_F32 else 4e-3)
+            tol = {H.HGEMM_F32: 1e-3, H.HGEMM_F16: 4e-3, H.HGEMM_BF16: 5e-3}[dout]
+            assert oracle.normalized_error(got, Cref, Den) <= tol
 
 
 def test_no_alloc_refuses_what_it_cannot_do(dev):
