@@ -271,14 +271,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 2)
                     if (kbase + i >= lim) sv[i] = f2u(-INFINITY);
             }
             // row max and sum in 8 independent partials (short dependency
-            // chains: few warps share an SM sub-partition)
+            // chains: few warps share an SM sub-partition), with three-input
+            // max and packed fp32 pairs to halve the instruction count
             float pm[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) pm[t] = fmaxf(u2f(sv[t]), u2f(sv[t + 8]));
 #pragma unroll
-            for (int i = 16; i < 64; ++i) pm[i & 7] = fmaxf(pm[i & 7], u2f(sv[i]));
-            float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+            for (int i = 16; i < 64; i += 16)
+#pragma unroll
+                for (int t = 0; t < 8; ++t) pm[t] = fmax3(pm[t], u2f(sv[i + t]), u2f(sv[i + 8 + t]));
+            float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
             mx *= c;
             float alpha = 1.f;
             const bool raise = mx > m_ref + 8.f;
@@ -292,10 +294,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 2)
             uint32_t pk[32];  // P as 16-bit pairs, key 2i in the low half of pk[i]
 #pragma unroll
             for (int i = 0; i < 64; i += 2) {
-                const float e0 = ex2_approx(fmaf(u2f(sv[i]), c, -m_ref));
-                const float e1 = ex2_approx(fmaf(u2f(sv[i + 1]), c, -m_ref));
-                ps[i & 7] += e0;
-                ps[(i + 1) & 7] += e1;
+                float a0, a1;
+                ffma2(a0, a1, u2f(sv[i]), u2f(sv[i + 1]), c, c, -m_ref, -m_ref);
+                const float e0 = ex2_approx(a0);
+                const float e1 = ex2_approx(a1);
+                fadd2(ps[i & 7], ps[(i & 7) + 1], ps[i & 7], ps[(i & 7) + 1], e0, e1);
                 pk[i / 2] = pack2<OUT>(f2u(e0), f2u(e1));
             }
             const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
