@@ -189,29 +189,42 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- helpers
 
-def kernel_hash(attention: bool = False) -> str:
-    """Hash of the sources the workload's kernels are built from: the GEMM
-    files, or the attention files, plus the shared headers."""
+def kernel_family(kernel_name: str) -> str:
+    for fam in ("pair", "tiled", "skinny"):
+        if f"hgemm_{fam}_kernel" in kernel_name:
+            return fam
+    return "attention" if "attention" in kernel_name else "other"
+
+
+def kernel_hash(family: str) -> str:
+    """Hash of the sources a kernel family is built and launched from: its
+    own files, its host entry points and the shared headers."""
+    own = {
+        "pair": ("gemm_pair", "api.cpp"),
+        "tiled": ("gemm_tiled", "api.cpp"),
+        "skinny": ("gemm_skinny", "api.cpp"),
+        "attention": ("attention",),
+    }.get(family, ())
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "tensor_core_dense_swizzled_gb300", "csrc", "*"))):
         base = os.path.basename(f)
-        shared = base.endswith((".h", ".cuh"))
-        if not shared and base.startswith("attention") != attention:
+        shared = base.endswith((".h", ".cuh")) and not base.startswith(("gemm_", "attention"))
+        if not shared and not base.startswith(own):
             continue
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload: str, attention: bool = False):
+def committed_traffic(workload: str):
     """DRAM bytes per launch of the main kernel from a committed ncu capture,
-    or None when absent or taken on other kernel sources."""
+    or None when absent or taken on other sources of that kernel family."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("kernel_hash") == kernel_hash(attention):
+        if e and e.get("kernel_hash") == kernel_hash(kernel_family(e.get("kernel", ""))):
             return e.get("dram_bytes_per_launch")
     except Exception:
         pass
@@ -659,7 +672,7 @@ def run_attention_ours(args, w, world, rank, local, pg):
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
     peak = peaks["bf16_sustained"] if sustained else peaks["bf16"]
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": committed_traffic(w.name, attention=True),
+            "frac": achieved / peak, "traffic": committed_traffic(w.name),
             "peak_kind": ("sustained" if sustained else "burst") + f" bf16, {peaks['source']}",
             "algorithmic_per_launch": flops, "launch_ms": avg_launch_ms, "kernels_per_launch": 1}
     e2e = None
