@@ -191,7 +191,8 @@ hgemm_status_t hgemm_run(hgemm_plan_t plan, const void *A, const void *B, void *
 typedef enum {
     HGEMM_ACT_NONE = 0,
     HGEMM_ACT_RELU = 1, /* max(x, 0) */
-    HGEMM_ACT_GELU = 2, /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)) */
+    HGEMM_ACT_GELU = 2, /* x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)); erf by Abramowitz &
+                           Stegun 7.1.26 (absolute error <= 1.5e-7) */
     HGEMM_ACT_GELU_TANH = 3 /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), the tanh form
                                (tanh from the hardware approximation) */
 } hgemm_activation_t;

@@ -108,12 +108,32 @@ __device__ __forceinline__ float tanh_approx(float x) {
     return y;
 }
 
+// GELU in the erf form, x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), with erf
+// from Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26: for z >= 0, erf(z) = 1 - q(z), q = (a1 t + ... + a5 t^5) e^(-z^2),
+// t = 1 / (1 + p z), absolute error <= 1.5e-7 (plus fp32 rounding and the
+// SFU's ex2 and the reciprocal); erf is odd.
+__device__ __forceinline__ float gelu_erf(float x) {
+    const float z = fabsf(x) * 0.70710678118654752f;
+    float t;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, z, 1.f)));
+    float poly = fmaf(1.061405429f, t, -1.453152027f);
+    poly = fmaf(poly, t, 1.421413741f);
+    poly = fmaf(poly, t, -0.284496736f);
+    poly = fmaf(poly, t, 0.254829592f);
+    poly *= t;
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-z * z * 1.4426950408889634f));
+    const float q = poly * e;  // 1 - erf(|x| / sqrt 2)
+    return 0.5f * x * (x >= 0.f ? 2.f - q : q);
+}
+
 // Activation of the fused epilogue: 1 ReLU; 2 GELU in the erf form
 // x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)); 3 GELU in the tanh form
 // 0.5 x (1 + tanh(sqrt(2 / pi) (x + 0.044715 x^3))).
 __device__ __forceinline__ float epi_act(float x, int act) {
     if (act == 1) return fmaxf(x, 0.f);
-    if (act == 2) return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+    if (act == 2) return gelu_erf(x);
     if (act == 3) {
         const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
         return 0.5f * x * (1.f + tanh_approx(u));
