@@ -488,12 +488,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int buf = local & 1;
             const uint32_t tph = (local >> 1) & 1;
             ++local;
+            const int row0 = mt * (2 * BM) + static_cast<int>(rank) * BM + q * 32;
+            const int col0 = nt * PN;
+            if constexpr (EPI) prefetch_c_prev<OUT>(epi, row0 + lane, col0, PN, b);
             if (!wait_bounded_warp(tfull(buf), tph, wc, timeout_code(ROLE_EPILOGUE, buf))) break;
             tc_fence_after();
             const uint32_t tbase =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::TMEM_STRIDE;
-            const int row0 = mt * (2 * BM) + static_cast<int>(rank) * BM + q * 32;
-            const int col0 = nt * PN;
             const uint32_t release_bar = mapa_shared(tempty(buf), 0);
             auto release = [&] {
                 if (lane == 0) mbar_arrive_cluster(release_bar);

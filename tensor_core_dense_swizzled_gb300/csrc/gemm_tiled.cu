@@ -256,12 +256,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tile_coords(p, t, b, mt, nt);
             const int buf = local & 1;
             const uint32_t tph = (local >> 1) & 1;
+            const int row0 = mt * BM + q * 32;
+            const int col0 = nt * BN;
+            if constexpr (EPI) prefetch_c_prev<OUT>(epi, row0 + lane, col0, BN, b);
             if (!wait_bounded_warp(tfull(buf), tph, wc, timeout_code(ROLE_EPILOGUE, buf))) break;
             tc_fence_after();
             const uint32_t tbase =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::TMEM_STRIDE;
-            const int row0 = mt * BM + q * 32;
-            const int col0 = nt * BN;
             drain_accumulator<OUT, TMA_STORE, BN, false, EPI>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
                                                   [&] {
                                                       if (lane == 0) mbar_arrive(tempty(buf));

@@ -237,6 +237,22 @@ __device__ __forceinline__ void epi_row(uint32_t (&v)[32], int row, int col, int
     }
 }
 
+// beta != 0: asks L2 for C's previous values of row `row`, columns col0 ..
+// col0 + ncols - 1 (clipped to the matrix), while the accumulator of the tile
+// is still being computed, so that the epilogue's reads of them hit L2
+// instead of waiting on DRAM chunk by chunk.
+template <int OUT>
+__device__ __forceinline__ void prefetch_c_prev(const EpiArgs &e, int row, int col0, int ncols, int b) {
+    if (e.ep.beta == 0.f || row >= e.M) return;
+    constexpr int OB = OUT == OUT_F32 ? 4 : 2;
+    const int cols = min(ncols, e.N - col0);
+    if (cols <= 0) return;
+    const char *rowp = static_cast<const char *>(e.C) +
+                       (static_cast<int64_t>(b) * e.strideC + static_cast<int64_t>(row) * e.ldc + col0) * OB;
+    for (int off = 0; off < cols * OB; off += 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(rowp + off));
+}
+
 // Converts 32 fp32 columns (chunk c of a warp's 32 rows, lane = row) and
 // stores them into C: TMA_STORE through the warp's swizzled staging pieces
 // (fp32 rows of 128 bytes: chunk j of row r at j ^ (r & 7); fp16/bf16 rows of
