@@ -697,6 +697,41 @@ def test_one_shot_and_matmul(dev):
     H.hgemm_cache_clear()
 
 
+def test_matmul_transposed_fp8_and_epilogue(dev):
+    """The torch front end's planned paths: B given as W.t() (transposed-B
+    kernels), 8-bit inputs, and the fused epilogue."""
+    import types
+
+    from tensor_core_dense_swizzled_gb300 import matmul, matmul_cache_clear
+    M, N, K = 320, 384, 256
+    A = inputs.make_random((M, K), "bf16", 60)
+    W = inputs.make_random((N, K), "bf16", 61)  # stored N x K
+    C = matmul(A.to(dev), W.to(dev).t(), out_dtype=torch.float32)
+    Cref, Den = oracle.gemm_bt(bits(A), bits(W), 1, M, N, K, K, K)
+    check(C.cpu().double().numpy()[None], Cref, Den, "f32")
+    # 8-bit inputs
+    A8 = inputs.make_random((M, K), "e4m3", 62)
+    W8 = inputs.make_random((N, K), "e4m3", 63)
+    C8 = matmul(A8.to(dev), W8.to(dev).t(), out_dtype=torch.float32)
+    w8 = lambda t: oracle.widen8(t.contiguous().view(torch.uint8).numpy().reshape(-1))  # noqa: E731
+    Cref8, Den8 = oracle.gemm_bt(w8(A8), w8(W8), oracle.E4M3, M, N, K, K, K)
+    check(C8.cpu().double().numpy()[None], Cref8, Den8, "f32")
+    with pytest.raises(ValueError):
+        matmul(A8.to(dev), W8.t().contiguous().to(dev))  # 8-bit B must be W.t()
+    # fused epilogue: bias + GELU, and beta reading out
+    g = torch.Generator().manual_seed(64)
+    bias = torch.randn(N, generator=g)
+    Ce = matmul(A.to(dev), W.to(dev).t(), out_dtype=torch.float32, bias=bias.to(dev), activation="gelu")
+    D, DenD = oracle.epilogue(Cref[0], Den[0], bias=bias.double().numpy(), act=oracle.ACT_GELU)
+    assert oracle.normalized_error(Ce.cpu().double().numpy(), D, DenD) <= 1e-3
+    prev = torch.randn(M, N, generator=g).to(dev)
+    Cb = matmul(A.to(dev), W.to(dev).t(), out_dtype=torch.float32, out=prev.clone(), alpha=0.5, beta=2.0)
+    D, DenD = oracle.epilogue(Cref[0], Den[0], alpha=0.5, beta=2.0, C_prev=prev.cpu().double().numpy())
+    assert oracle.normalized_error(Cb.cpu().double().numpy(), D, DenD) <= 1e-3
+    torch.cuda.synchronize()
+    matmul_cache_clear()
+
+
 def test_run_host_end_to_end(dev):
     M, N, K = 257, 320, 130
     A = inputs.make_random((M, K), "f16", 60).pin_memory()
