@@ -197,13 +197,14 @@ def kernel_family(kernel_name: str) -> str:
 
 
 def kernel_hash(family: str) -> str:
-    """Hash of the sources a kernel family is built and launched from: its
-    own files, its host entry points and the shared headers."""
+    """Hash of the device sources a kernel family is built from: its own
+    files and the shared headers (the stored entry names the kernel variant
+    the capture saw)."""
     own = {
-        "pair": ("gemm_pair", "api.cpp"),
-        "tiled": ("gemm_tiled", "api.cpp"),
-        "skinny": ("gemm_skinny", "api.cpp"),
-        "attention": ("attention",),
+        "pair": ("gemm_pair",),
+        "tiled": ("gemm_tiled",),
+        "skinny": ("gemm_skinny",),
+        "attention": ("attention.cu",),
     }.get(family, ())
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "tensor_core_dense_swizzled_gb300", "csrc", "*"))):

@@ -888,14 +888,25 @@ hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void 
     }
     hgemm_status_t st = plan_run(p, p->dA, p->dB, p->dC, s);
     if (st != HGEMM_OK) return st;
-    // copy back only the M x N block of each batch: host elements between rows stay intact
-    for (int64_t b = 0; b < p->batch; ++b) {
-        const size_t off = static_cast<size_t>(b * p->sC) * ob;
-        e = cudaMemcpy2DAsync(static_cast<char *>(C_host) + off, static_cast<size_t>(p->ldc) * ob,
-                              p->dC + off, static_cast<size_t>(p->ldc) * ob,
-                              static_cast<size_t>(p->N) * ob, static_cast<size_t>(p->M),
-                              cudaMemcpyDeviceToHost, s);
+    // copy back only the M x N block of each batch: host elements between rows stay intact.
+    // Batches stacked at the row pitch (strideC = M * ldc) are one 2-D copy of batch * M
+    // rows, and rows without padding (ldc = N) one contiguous copy.
+    const bool stacked = p->batch == 1 || p->sC == p->M * p->ldc;
+    if (stacked && p->ldc == p->N) {
+        e = cudaMemcpyAsync(C_host, p->dC, static_cast<size_t>(p->batch * p->M * p->N) * ob,
+                            cudaMemcpyDeviceToHost, s);
         if (e != cudaSuccess) return cuda_fail(e, "copy C to host");
+    } else {
+        const int64_t copies = stacked ? 1 : p->batch;
+        const int64_t rows = stacked ? p->batch * p->M : p->M;
+        for (int64_t b = 0; b < copies; ++b) {
+            const size_t off = static_cast<size_t>(b * p->sC) * ob;
+            e = cudaMemcpy2DAsync(static_cast<char *>(C_host) + off, static_cast<size_t>(p->ldc) * ob,
+                                  p->dC + off, static_cast<size_t>(p->ldc) * ob,
+                                  static_cast<size_t>(p->N) * ob, static_cast<size_t>(rows),
+                                  cudaMemcpyDeviceToHost, s);
+            if (e != cudaSuccess) return cuda_fail(e, "copy C to host");
+        }
     }
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

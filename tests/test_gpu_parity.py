@@ -747,6 +747,29 @@ def test_run_host_end_to_end(dev):
     check(C[:, :N].double().numpy()[None], Cref, Den, "f32")
 
 
+@pytest.mark.parametrize("ldc,gap", [(96, 0), (104, 0), (96, 500)])
+def test_run_host_batched_copies(dev, ldc, gap):
+    """hgemm_run_host copies C back as one block (dense), one 2-D copy
+    (batches stacked at the row pitch) or one 2-D copy per batch (gaps
+    between batches); host elements outside the M x N blocks stay intact."""
+    batch, M, N, K = 3, 70, 96, 64
+    sC = M * ldc + gap
+    A = inputs.make_random((batch, M, K), "bf16", 65).pin_memory()
+    B = inputs.make_random((batch, K, N), "bf16", 66).pin_memory()
+    C = torch.full((batch * sC,), -7.0, dtype=torch.float32).pin_memory()
+    plan = H.hgemm_plan_create(M, N, K, K, N, ldc, batch, M * K, K * N, sC, H.HGEMM_BF16, H.HGEMM_F32)
+    try:
+        H.hgemm_run_host(plan, A, B, C)
+    finally:
+        H.hgemm_plan_destroy(plan)
+    view = torch.as_strided(C, (batch, M, N), (sC, ldc, 1))
+    mask = torch.ones(batch * sC, dtype=torch.bool)
+    torch.as_strided(mask, (batch, M, N), (sC, ldc, 1)).fill_(False)
+    assert torch.all(C[mask] == -7.0), "host elements outside C's blocks changed"
+    Cref, Den = oracle.gemm(bits(A), bits(B), 1, M, N, K, K, N, batch, M * K, K * N)
+    check(view.double().numpy(), Cref, Den, "f32")
+
+
 def test_watchdog_selftest(dev):
     """A wait that can never complete gives up after its limit and reports
     HGEMM_ERR_TIMEOUT; the context stays usable afterwards."""
