@@ -315,11 +315,15 @@ hgemm_status_t alloc_workspace(hgemm_plan_s *p) {
     off = static_cast<size_t>(round_up(static_cast<int64_t>(off + partials), 256));
     if (p->path == HGEMM_PATH_TILED || p->path == HGEMM_PATH_SKINNY) {
         // aligned copies of A and B; allocated whenever a copy can be needed
-        // (by the leading dimension now, or by a misaligned pointer later)
-        p->lda_p = round_up(p->K, 8);
+        // (by the leading dimension now, or by a misaligned pointer later).
+        // The tiled path pads their rows to whole 128-byte blocks: the copy
+        // writes zeros past the last column, so the pair kernel's one-copy-
+        // per-stage views apply to a copied operand whatever K and N are.
+        const int64_t pad = p->path == HGEMM_PATH_TILED ? kblock(p->din) : 8;
+        p->lda_p = round_up(p->K, pad);
         p->sA_p = p->M * p->lda_p;
         // B stored K x N, or N x K with trans_b: rows x cols of the stored matrix
-        p->ldb_p = round_up(p->opt.trans_b ? p->K : p->N, 8);
+        p->ldb_p = round_up(p->opt.trans_b ? p->K : p->N, pad);
         p->sB_p = (p->opt.trans_b ? p->N : p->K) * p->ldb_p;
         p->apack_bytes = static_cast<size_t>(p->batch * p->sA_p * in_bytes(p->din));
         p->bpack_bytes = static_cast<size_t>(p->batch * p->sB_p * in_bytes(p->din));
@@ -594,6 +598,29 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
     return HGEMM_OK;
 }
 
+// Extents of the pair kernel's 4-D views of A and B: an operand read from
+// its aligned copy may be viewed up to the next 128-byte block of its
+// contiguous dimension (the copy holds zeros there, which add nothing to the
+// product; extra columns of B only make accumulator columns that are never
+// stored).  The views need those extents to be whole blocks.
+struct WideDims {
+    int64_t ka, kb, nb;  // A's K, B's K (trans_b) or N (otherwise)
+    bool ok;
+};
+WideDims wide_dims(const hgemm_plan_s *p, bool packed_a, bool packed_b) {
+    const int64_t bke = kblock(p->din);
+    const bool tb = p->opt.trans_b != 0;
+    WideDims w;
+    w.ka = packed_a ? round_up(p->K, bke) : p->K;
+    w.kb = tb && packed_b ? round_up(p->K, bke) : p->K;
+    w.nb = !tb && packed_b ? round_up(p->N, 64) : p->N;
+    w.ok = p->path == HGEMM_PATH_TILED && p->pair && p->bn == 256 && w.ka % bke == 0 &&
+           (tb ? w.kb % bke == 0 : w.nb % 64 == 0);
+    if (packed_a && w.ka > p->lda_p) w.ok = false;
+    if (packed_b && (tb ? w.kb : w.nb) > p->ldb_p) w.ok = false;
+    return w;
+}
+
 hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *C, bool tma_store) {
     if (p->maps_ok && A == p->mA && B == p->mB && C == p->mC) return HGEMM_OK;
     const CUtensorMapDataType dt = is_f8(p->din)         ? CU_TENSOR_MAP_DATA_TYPE_UINT8
@@ -610,20 +637,22 @@ hgemm_status_t encode_maps(hgemm_plan_s *p, const void *A, const void *B, void *
     const int64_t sB = packed_b ? p->sB_p : p->sB;
     hgemm_status_t st;
     if (p->path == HGEMM_PATH_TILED) {
-        // Pair tiles 256 wide with K and N multiples of 64: the 4-D views
-        // (one copy per operand per stage); otherwise, or if the driver
-        // rejects them, the 3-D maps.
+        // Pair tiles 256 wide with K and N multiples of 64 (or operands read
+        // from their zero-padded copies, wide_dims): the 4-D views (one copy
+        // per operand per stage); otherwise, or if the driver rejects them,
+        // the 3-D maps.
         // B stored N x K (trans_b) is staged K-major like A: its 4-D view
         // splits K the same way (128 rows of B per CTA), and needs only K to
         // be a multiple of 64.
         const bool tb = p->opt.trans_b != 0;
+        const WideDims wd = wide_dims(p, packed_a, packed_b);
         p->wide = false;
-        if (p->pair && p->bn == 256 && p->K % bke == 0 && (tb || p->N % 64 == 0)) {
-            p->wide = encode_split_4d(&p->tmA, A, dt, ib, p->K, p->M, p->batch, lda, sA, 128,
+        if (wd.ok) {
+            p->wide = encode_split_4d(&p->tmA, A, dt, ib, wd.ka, p->M, p->batch, lda, sA, 128,
                                       static_cast<uint32_t>(p->pair_ks)) == HGEMM_OK &&
-                      (tb ? encode_split_4d(&p->tmB, B, dt, ib, p->K, p->N, p->batch, ldb, sB, 128,
+                      (tb ? encode_split_4d(&p->tmB, B, dt, ib, wd.kb, p->N, p->batch, ldb, sB, 128,
                                             static_cast<uint32_t>(p->pair_ks))
-                          : encode_split_4d(&p->tmB, B, dt, ib, p->N, p->K, p->batch, ldb, sB,
+                          : encode_split_4d(&p->tmB, B, dt, ib, wd.nb, p->K, p->batch, ldb, sB,
                                             static_cast<uint32_t>(64 * p->pair_ks), 2)) == HGEMM_OK;
         }
         if (!p->wide) {
@@ -973,12 +1002,10 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     r.stream_k = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->stream_k
                  : plan->path == HGEMM_PATH_SKINNY && plan->skinny_deal ? 1
                                                                        : 0;
-    r.wide_boxes = plan->path == HGEMM_PATH_TILED && plan->pair && plan->bn == 256 &&
-                           plan->K % kblock(plan->din) == 0 &&
-                           (plan->opt.trans_b || plan->N % 64 == 0) &&
-                           (plan->wide || !plan->maps_ok)
-                       ? 1
-                       : 0;
+    // before the first run: as the plan's own copies (leading dimensions)
+    // decide; after it: what the last run used
+    r.wide_boxes = plan->maps_ok ? (plan->wide ? 1 : 0)
+                                 : (wide_dims(plan, r.repack_a != 0, r.repack_b != 0).ok ? 1 : 0);
     *info = r;
     return HGEMM_OK;
 }

@@ -305,31 +305,45 @@ __device__ __forceinline__ void store_chunk(uint32_t (&v)[32], int c, uint32_t s
 #pragma unroll
         for (int j = 0; j < 32; ++j) stg_f[lane * 32 + (j ^ lane)] = __uint_as_float(v[j]);
         __syncwarp();
+        // Every value of the column is read back before the first store to
+        // C (and, with the fused epilogue, a group's previous C values before
+        // the group's stores): as far as the compiler knows a store to C may
+        // alias a later load, so interleaved loads and stores would run as 32
+        // dependent round trips (about 12 us per 128 x 256 tile on GB300,
+        // against 3.4 us for the TMA-store path).
+        float x[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) x[r] = stg_f[r * 32 + (lane ^ r)];
         const int col = col0 + c * 32 + lane;
-        if (col < e.N) {
-            const int64_t base = static_cast<int64_t>(b) * e.strideC;
+        const int nrows = min(32, e.M - row0);  // rows of the piece inside C
+        if (col < e.N && nrows > 0) {
+            constexpr int OB = OUT == OUT_F32 ? 4 : 2;
+            char *p0 = static_cast<char *>(e.C) +
+                       (static_cast<int64_t>(b) * e.strideC + static_cast<int64_t>(row0) * e.ldc + col) * OB;
+            const int64_t rstep = e.ldc * OB;
             if constexpr (EPI) {
                 const EpiParams &ep = e.ep;
                 const float cs = ep.col_scale ? __ldg(ep.col_scale + col) : 1.f;
                 const float bias = ep.bias ? __ldg(ep.bias + col) : 0.f;
-#pragma unroll 4
-                for (int r = 0; r < 32; ++r) {
-                    const int row = row0 + r;
-                    if (row >= e.M) break;
-                    const int64_t idx = base + static_cast<int64_t>(row) * e.ldc + col;
-                    const float rs = ep.row_scale ? __ldg(ep.row_scale + row) : 1.f;
-                    const float prev = ep.beta != 0.f ? load_one<OUT>(e.C, idx) : 0.f;
-                    store_one<OUT>(e.C, idx,
-                                   epi_value(ep, stg_f[r * 32 + (lane ^ r)], rs, cs, bias, prev));
+#pragma unroll
+                for (int g = 0; g < 32; g += 16) {
+                    float rs[16], prev[16];
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        const bool in = g + r < nrows;
+                        rs[r] = (ep.row_scale && in) ? __ldg(ep.row_scale + row0 + g + r) : 1.f;
+                        prev[r] = (ep.beta != 0.f && in) ? load_one<OUT>(p0 + (g + r) * rstep, 0) : 0.f;
+                    }
+#pragma unroll
+                    for (int r = 0; r < 16; ++r)
+                        if (g + r < nrows)
+                            store_one<OUT>(p0 + (g + r) * rstep, 0,
+                                           epi_value(ep, x[g + r], rs[r], cs, bias, prev[r]));
                 }
             } else {
-#pragma unroll 4
-                for (int r = 0; r < 32; ++r) {
-                    const int row = row0 + r;
-                    if (row >= e.M) break;
-                    store_one<OUT>(e.C, base + static_cast<int64_t>(row) * e.ldc + col,
-                                   stg_f[r * 32 + (lane ^ r)]);
-                }
+#pragma unroll
+                for (int r = 0; r < 32; ++r)
+                    if (r < nrows) store_one<OUT>(p0 + r * rstep, 0, x[r]);
             }
         }
     }

@@ -194,8 +194,26 @@ def test_cta_pair_random_shapes(dev, shape, din, dout, pn, ks):
     got, Cref, Den, info = run_case(dev, M, N, K, din, dout, seed=M + 2 * N + K,
                                     options=H.Options(cta_pair=1, tile_n=pn, pair_k_blocks=ks))
     assert info["tile_m"] == 256 and info["grid"] % 2 == 0 and info["tile_k"] == 64 * ks
-    # one TMA copy per operand per stage exactly when the 4-D views apply
-    assert info["wide_boxes"] == int(pn == 256 and K % 64 == 0 and N % 64 == 0)
+    # one TMA copy per operand per stage exactly when the 4-D views apply: K
+    # and N multiples of 64, or the operand read from its zero-padded copy
+    assert info["wide_boxes"] == int(pn == 256 and (K % 64 == 0 or info["repack_a"] == 1)
+                                     and (N % 64 == 0 or info["repack_b"] == 1))
+    check(got, Cref, Den, dout)
+
+
+@pytest.mark.parametrize("shape", [(600, 333, 333, 2, 0), (1100, 777, 1023, 1, 0), (520, 640, 200, 1, 3),
+                                   (300, 4095, 130, 1, 0)])
+@pytest.mark.parametrize("din,dout", [("f16", "f32"), ("bf16", "bf16")])
+def test_cta_pair_views_over_padded_copies(dev, shape, din, dout):
+    """Operands read from their aligned copies: the copies' rows are padded
+    with zeros to whole 64-element blocks, and the pair kernel views them over
+    the padded extent (one TMA copy per operand per stage) even though K or N
+    is not a multiple of 64.  off_a > 0 puts A's base off the 16-byte grid
+    (a copy made at run time)."""
+    M, N, K, batch, off_a = shape
+    got, Cref, Den, info = run_case(dev, M, N, K, din, dout, batch=batch, off_a=off_a,
+                                    seed=M + N + K, options=H.Options(cta_pair=1), runs=2)
+    assert info["tile_m"] == 256
     check(got, Cref, Den, dout)
 
 

@@ -59,6 +59,11 @@ CASES = {
     "pair_wide": (1024, 1024, 512, 1, H.Options(cta_pair=1), lambda i: i["tile_m"] == 256 and i["wide_boxes"] == 1),
     "pair_ragged_n": (1024, 1000, 512, 1, H.Options(cta_pair=1), lambda i: i["wide_boxes"] == 1),
     "pair_k_not_64": (768, 512, 200, 1, H.Options(cta_pair=1), lambda i: i["wide_boxes"] == 0),
+    # lda = ldb = K = 333 (unaligned rows): both operands copied, rows padded
+    # to 384 with zeros, so the one-copy-per-stage views apply
+    "pair_k_odd_copied": (768, 640, 333, 1, H.Options(cta_pair=1),
+                          lambda i: i["wide_boxes"] == 1 and i["repack_a"] == 1 and i["repack_b"] == 1),
+    "pair_copied_batched": (512, 520, 201, 2, H.Options(cta_pair=1), lambda i: i["wide_boxes"] == 1),
     "pair_ks1": (1024, 768, 640, 1, H.Options(cta_pair=1, pair_k_blocks=1), lambda i: i["tile_k"] == 64),
     "pair_224": (768, 896, 320, 1, H.Options(cta_pair=1, tile_n=224), lambda i: i["tile_n"] == 224),
     "pair_stream_k": (2560, 2048, 256, 1, H.Options(cta_pair=1, tail_mode=3), lambda i: i["stream_k"] == 1),
