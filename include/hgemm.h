@@ -31,8 +31,10 @@
  * Alignment.  Pointers must be element-aligned.  When a base pointer is
  * 16-byte aligned and its leading dimension and batch stride are multiples of
  * 16 bytes, the operand is read by TMA in place; otherwise it is first copied
- * into an aligned workspace buffer.  A misaligned C is written with
- * predicated stores instead of TMA stores.  Nothing is refused for alignment.
+ * into an aligned workspace buffer (rows padded with zeros to whole 64-element
+ * blocks on the tiled path, to 8 elements on the skinny path).  A misaligned C
+ * is written with predicated stores instead of TMA stores.  Nothing is refused
+ * for alignment.
  */
 #ifndef HGEMM_H
 #define HGEMM_H
@@ -124,7 +126,10 @@ typedef struct {
     int64_t workspace_bytes;
     int tail_split;       /* CTA pairs: 2 when the last partial wave's tiles run as two K halves */
     int wide_boxes;       /* CTA pairs: 1 when each pipeline stage of A and of B is one TMA copy
-                             (4-D views; 256-wide tiles, K and N multiples of 64) */
+                             (4-D views; 256-wide tiles, K and N multiples of 64, or the
+                             operand read from its zero-padded aligned copy).  Before the
+                             first run: as the leading dimensions decide; after it: what
+                             the last run used */
     int trans_b;          /* the plan's B layout (hgemm_options_t.trans_b) */
     int stream_k;         /* K steps dealt in equal contiguous ranges: CTA pairs 1 (tail_mode 3)
                              or 2 (tail_mode 4), the skinny path 1 (skinny_stream_k; split_k is

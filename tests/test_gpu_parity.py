@@ -436,8 +436,10 @@ def test_misaligned_base_pointers(dev):
 def test_operand_copy_every_misalignment(dev, off):
     """The aligned copy reads whole 16-byte granules and shifts them: every
     start offset 0..7 elements, odd leading dimensions (so the offset changes
-    from row to row) and rows shorter than a granule."""
-    for (M, N, K) in [(45, 29, 37), (130, 7, 3), (9, 300, 1)]:
+    from row to row), rows shorter than a granule, and rows of several
+    1024-element segments (each copied by its own warp, which takes the
+    granule after its segment from memory)."""
+    for (M, N, K) in [(45, 29, 37), (130, 7, 3), (9, 300, 1), (9, 1100, 2501)]:
         got, Cref, Den, info = run_case(dev, M, N, K, "f16", "f32", lda=K, ldb=N, ldc=N,
                                         off_a=off, off_b=(off * 3) % 8, seed=100 + off + K,
                                         options=H.Options(force_path=H.HGEMM_PATH_TILED))
