@@ -473,8 +473,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;
         const int ew = warp - 2;
         const uint32_t stg = sC + ew * EPI_STG_BUFS * EPI_STG_BYTES;
-        float *stg_f =
-            reinterpret_cast<float *>(smem + Cfg::SMEM_C + ew * EPI_STG_BUFS * EPI_STG_BYTES);
         const EpiArgs epi{&tmC, p.C, p.ldc, p.strideC, p.M, p.N, p.ep};
         int sbuf = 0;
         int local = 0;
@@ -500,7 +498,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) mbar_arrive_cluster(release_bar);
             };
             if (w.role == PIECE_WHOLE) {
-                drain_accumulator<OUT, TMA_STORE, PN, false, EPI>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
+                drain_accumulator<OUT, TMA_STORE, PN, false, EPI>(tbase, stg, sbuf, row0, col0, b, epi,
                                                       release);
                 continue;
             }
@@ -533,7 +531,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 last = __shfl_sync(0xFFFFFFFFu, last, 0);
                 __syncwarp();  // lane 0's acquire before every lane's loads
                 if (last) {
-                    drain_partials<OUT, TMA_STORE, PN, MAX_SEG, EPI>(parts, seg_stride, w.nseg, stg, stg_f,
+                    drain_partials<OUT, TMA_STORE, PN, MAX_SEG, EPI>(parts, seg_stride, w.nseg, stg,
                                                                 sbuf, row0, col0, b, epi);
                     if (lane == 0) *ctr = 0;  // ready for the next run
                 }
@@ -571,7 +569,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     release();
                     break;
                 }
-                drain_accumulator<OUT, TMA_STORE, PN, true, EPI>(tbase, stg, stg_f, sbuf, row0, col0, b,
+                drain_accumulator<OUT, TMA_STORE, PN, true, EPI>(tbase, stg, sbuf, row0, col0, b,
                                                             epi, release, region, 0, NCH);
                 if (lane == 0) *flag = 0;  // read: ready for the next run
                 continue;
@@ -607,7 +605,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 release();
                 break;
             }
-            drain_accumulator<OUT, TMA_STORE, PN, true, EPI>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
+            drain_accumulator<OUT, TMA_STORE, PN, true, EPI>(tbase, stg, sbuf, row0, col0, b, epi,
                                                         release, region + half * (4 * 1024),
                                                         own_lo, own_hi);
             if (lane == 0) flags[half] = 0;  // read: ready for the next run

@@ -247,7 +247,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;   // TMEM lane quarter this warp may read
         const int ew = warp - 2;  // staging slot
         const uint32_t stg = sC + ew * STG_BUFS * STG_BYTES;
-        float *stg_f = reinterpret_cast<float *>(smem + Cfg::SMEM_C + ew * STG_BUFS * STG_BYTES);
         const EpiArgs epi{&tmC, p.C, p.ldc, p.strideC, p.M, p.N, p.ep};
         int sbuf = 0;
         int local = 0;
@@ -263,7 +262,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t tbase =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::TMEM_STRIDE;
-            drain_accumulator<OUT, TMA_STORE, BN, false, EPI>(tbase, stg, stg_f, sbuf, row0, col0, b, epi,
+            drain_accumulator<OUT, TMA_STORE, BN, false, EPI>(tbase, stg, sbuf, row0, col0, b, epi,
                                                   [&] {
                                                       if (lane == 0) mbar_arrive(tempty(buf));
                                                   });

@@ -40,6 +40,16 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_b32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 template <int OUT>
 __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
     const float a = __uint_as_float(lo), b = __uint_as_float(hi);
@@ -266,8 +276,7 @@ __device__ __forceinline__ void prefetch_c_prev(const EpiArgs &e, int row, int c
 // EPI: the fused epilogue (e.ep) is applied first; a separate kernel variant
 // so that plain products carry none of its code or registers.
 template <int OUT, bool TMA_STORE, bool EPI>
-__device__ __forceinline__ void store_chunk(uint32_t (&v)[32], int c, uint32_t stg,
-                                            float *stg_f, int &sbuf, int row0, int col0, int b,
+__device__ __forceinline__ void store_chunk(uint32_t (&v)[32], int c, uint32_t stg, int &sbuf, int row0, int col0, int b,
                                             const EpiArgs &e) {
     const int lane = threadIdx.x & 31;
     if constexpr (TMA_STORE) {
@@ -301,49 +310,58 @@ __device__ __forceinline__ void store_chunk(uint32_t (&v)[32], int c, uint32_t s
         }
         sbuf = (sbuf + 1 == NPIECE) ? 0 : sbuf + 1;
     } else {
+        // The piece goes through the warp's staging area transposed (element
+        // (r, c) at r*32 + (c ^ r), conflict-free both ways), so that lane l
+        // then holds column l of the 32 rows and each store instruction writes
+        // one row's 32 consecutive elements.  Rows are handled in groups of
+        // 16 (8 with the fused epilogue): a group's values (and its previous
+        // C values) are all read before its first store -- as far as the
+        // compiler knows a store to C may alias a later load, so loads and
+        // stores interleaved row by row ran as 32 dependent round trips
+        // (about 12 us per 128 x 256 tile on GB300, against 3.4 us for the
+        // TMA-store path).
         __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) stg_f[lane * 32 + (j ^ lane)] = __uint_as_float(v[j]);
+        for (int j = 0; j < 32; ++j) st_shared_b32(stg + 4u * (lane * 32 + (j ^ lane)), v[j]);
         __syncwarp();
-        // Every value of the column is read back before the first store to
-        // C (and, with the fused epilogue, a group's previous C values before
-        // the group's stores): as far as the compiler knows a store to C may
-        // alias a later load, so interleaved loads and stores would run as 32
-        // dependent round trips (about 12 us per 128 x 256 tile on GB300,
-        // against 3.4 us for the TMA-store path).
-        float x[32];
-#pragma unroll
-        for (int r = 0; r < 32; ++r) x[r] = stg_f[r * 32 + (lane ^ r)];
         const int col = col0 + c * 32 + lane;
         const int nrows = min(32, e.M - row0);  // rows of the piece inside C
-        if (col < e.N && nrows > 0) {
-            constexpr int OB = OUT == OUT_F32 ? 4 : 2;
-            char *p0 = static_cast<char *>(e.C) +
-                       (static_cast<int64_t>(b) * e.strideC + static_cast<int64_t>(row0) * e.ldc + col) * OB;
-            const int64_t rstep = e.ldc * OB;
+        const bool live = col < e.N && nrows > 0;
+        constexpr int OB = OUT == OUT_F32 ? 4 : 2;
+        char *p0 = live ? static_cast<char *>(e.C) + (static_cast<int64_t>(b) * e.strideC +
+                                                      static_cast<int64_t>(row0) * e.ldc + col) * OB
+                        : nullptr;
+        const int64_t rstep = e.ldc * OB;
+        float cs = 1.f, bias = 0.f;
+        if constexpr (EPI) {
+            if (live && e.ep.col_scale) cs = __ldg(e.ep.col_scale + col);
+            if (live && e.ep.bias) bias = __ldg(e.ep.bias + col);
+        }
+        constexpr int GR = EPI ? 8 : 16;  // rows per group (registers)
+#pragma unroll
+        for (int g = 0; g < 32; g += GR) {
+            float x[GR];
+#pragma unroll
+            for (int r = 0; r < GR; ++r)
+                x[r] = __uint_as_float(ld_shared_b32(stg + 4u * ((g + r) * 32 + (lane ^ (g + r)))));
+            if (!live) continue;
             if constexpr (EPI) {
                 const EpiParams &ep = e.ep;
-                const float cs = ep.col_scale ? __ldg(ep.col_scale + col) : 1.f;
-                const float bias = ep.bias ? __ldg(ep.bias + col) : 0.f;
+                float rs[GR], prev[GR];
 #pragma unroll
-                for (int g = 0; g < 32; g += 16) {
-                    float rs[16], prev[16];
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        const bool in = g + r < nrows;
-                        rs[r] = (ep.row_scale && in) ? __ldg(ep.row_scale + row0 + g + r) : 1.f;
-                        prev[r] = (ep.beta != 0.f && in) ? load_one<OUT>(p0 + (g + r) * rstep, 0) : 0.f;
-                    }
-#pragma unroll
-                    for (int r = 0; r < 16; ++r)
-                        if (g + r < nrows)
-                            store_one<OUT>(p0 + (g + r) * rstep, 0,
-                                           epi_value(ep, x[g + r], rs[r], cs, bias, prev[r]));
+                for (int r = 0; r < GR; ++r) {
+                    const bool in = g + r < nrows;
+                    rs[r] = (ep.row_scale && in) ? __ldg(ep.row_scale + row0 + g + r) : 1.f;
+                    prev[r] = (ep.beta != 0.f && in) ? load_one<OUT>(p0 + (g + r) * rstep, 0) : 0.f;
                 }
+#pragma unroll
+                for (int r = 0; r < GR; ++r)
+                    if (g + r < nrows)
+                        store_one<OUT>(p0 + (g + r) * rstep, 0, epi_value(ep, x[r], rs[r], cs, bias, prev[r]));
             } else {
 #pragma unroll
-                for (int r = 0; r < 32; ++r)
-                    if (r < nrows) store_one<OUT>(p0 + r * rstep, 0, x[r]);
+                for (int r = 0; r < GR; ++r)
+                    if (g + r < nrows) store_one<OUT>(p0 + (g + r) * rstep, 0, x[r]);
             }
         }
     }
@@ -361,7 +379,7 @@ __device__ __forceinline__ void store_chunk(uint32_t (&v)[32], int c, uint32_t s
 // spill_accumulator writes; it is added to the accumulator (own + addend)
 // before the conversion.
 template <int OUT, bool TMA_STORE, int NCOLS, bool ADD = false, bool EPI = false, typename Release>
-__device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, float *stg_f,
+__device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg,
                                                   int &sbuf, int row0, int col0, int b,
                                                   const EpiArgs &e, Release release,
                                                   const float *addend = nullptr, int c_lo = 0,
@@ -412,7 +430,7 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, 
                 v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + a.w);
             }
         }
-        store_chunk<OUT, TMA_STORE, EPI>(v, c, stg, stg_f, sbuf, row0, col0, b, e);
+        store_chunk<OUT, TMA_STORE, EPI>(v, c, stg, sbuf, row0, col0, b, e);
     }
 }
 
@@ -425,7 +443,7 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tbase, uint32_t stg, 
 // of loads in flight).  nseg <= MAXSEG.
 template <int OUT, bool TMA_STORE, int NCOLS, int MAXSEG, bool EPI = false>
 __device__ __forceinline__ void drain_partials(const float *parts, int64_t seg_stride, int nseg,
-                                               uint32_t stg, float *stg_f, int &sbuf, int row0,
+                                               uint32_t stg, int &sbuf, int row0,
                                                int col0, int b, const EpiArgs &e) {
     const int lane = threadIdx.x & 31;
 #pragma unroll 1
@@ -462,7 +480,7 @@ __device__ __forceinline__ void drain_partials(const float *parts, int64_t seg_s
                 v[q + 3] = __float_as_uint(a.w);
             }
         }
-        store_chunk<OUT, TMA_STORE, EPI>(v, c, stg, stg_f, sbuf, row0, col0, b, e);
+        store_chunk<OUT, TMA_STORE, EPI>(v, c, stg, sbuf, row0, col0, b, e);
     }
 }
 
