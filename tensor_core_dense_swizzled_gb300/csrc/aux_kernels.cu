@@ -2,8 +2,9 @@
 //
 //   repack16   copies a 16-bit operand whose base, leading dimension or batch
 //              stride is not 16-byte aligned into an aligned workspace copy
-//              (leading dimension rounded up to 8 elements), so that TMA can
-//              read it.  TMA needs 16-byte-aligned global addresses and
+//              (leading dimension rounded up to whole 128-byte blocks for the
+//              tiled kernels, to 8 elements for the skinny kernels; padding
+//              written as zeros), so that TMA can read it.  TMA needs 16-byte-aligned global addresses and
 //              strides; the pages state the same 16-byte requirement for
 //              cp.async / ldmatrix rows ("tensor-cores-cutlass-and-cute",
 //              section 四.3 notes, and the 16-byte stride checks quoted from
