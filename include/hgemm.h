@@ -110,6 +110,11 @@ typedef struct {
                                  stored N x K row-major (element (k, j) at B + j*ldb + k, ldb >= K),
                                  i.e. C = A . B_stored^T -- a linear layer's weight, or attention's
                                  S = Q K^T with K stored [seq][dim] */
+    int tiled_epi_warps;      /* single-CTA tiled path, warps that drain the accumulators: 0
+                                 automatic (4; 8 for runs with the fused epilogue when the
+                                 inputs are 16-bit, the tile 128 or 256 wide and K <= 1024), 4,
+                                 or 8 (16-bit inputs and tile widths 128 / 256 only, else
+                                 HGEMM_ERR_UNSUPPORTED) */
 } hgemm_options_t;
 
 /* Read-only description of what a plan will launch. */
@@ -134,6 +139,9 @@ typedef struct {
     int stream_k;         /* K steps dealt in equal contiguous ranges: CTA pairs 1 (tail_mode 3)
                              or 2 (tail_mode 4), the skinny path 1 (skinny_stream_k; split_k is
                              then the most pieces a column tile is cut into) */
+    int epi_warps;        /* tiled path: warps draining the accumulators in plain runs (4 or 8;
+                             CTA pairs 4), else 0 */
+    int epi_warps_epilogue; /* the same for runs with the fused epilogue (hgemm_run_ex) */
 } hgemm_plan_info_t;
 
 /* Creates a plan for C_b = A_b . B_b, b < batch.

@@ -140,6 +140,8 @@ struct hgemm_plan_s {
     int path;
     // tiled path
     int bn;
+    int epi_warps = 4;     // single-CTA tiled kernel: epilogue warps of plain runs (4 or 8)
+    int epi_warps_ep = 4;  // the same for runs with the fused epilogue
     bool pair;  // 256 x 256 tiles on CTA pairs (cta_group::2)
     // pair path: tiles [0, full_tiles) whole, the tail split in tail_split K halves
     int64_t ptiles = 0, full_tiles = 0, units = 0;
@@ -420,6 +422,8 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         return fail(HGEMM_ERR_INVALID_ARG, "skinny_stream_k must be 0, 1 or 2");
     if (opt.group_m < 0 || opt.group_m > 4096)
         return fail(HGEMM_ERR_INVALID_ARG, "group_m must be in [0, 4096]");
+    if (opt.tiled_epi_warps != 0 && opt.tiled_epi_warps != 4 && opt.tiled_epi_warps != 8)
+        return fail(HGEMM_ERR_INVALID_ARG, "tiled_epi_warps must be 0, 4 or 8");
     if (opt.skinny_prefetch < -1 || opt.skinny_prefetch > 64)
         return fail(HGEMM_ERR_INVALID_ARG, "skinny_prefetch must be in [-1, 64]");
     if (opt.cta_pair == 1 && opt.tile_n != 0 && opt.tile_n != 256 && opt.tile_n != 224)
@@ -557,6 +561,23 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
                 }
                 p->grid = static_cast<int>(2 * (p->units < max_pairs ? p->units : max_pairs));
             }
+        }
+        if (!p->pair) {
+            // Eight epilogue warps for the fused epilogue on products with
+            // few K blocks per tile, where the epilogue's arithmetic and its
+            // reads of C bound a tile (batched S = Q K^T, 64 x 1024 x 1024 x
+            // 128, on GB300: + bias + GELU 100.7 -> 73.3 us, + beta C + bias
+            // + ReLU 204.7 -> 138.0 us).  Plain products keep four: there the
+            // stores are DRAM-bound and eight warps ran slower (53.2 ->
+            // 56.4 us).
+            const bool can8 = !is_f8(din) && (p->bn == 128 || p->bn == 256);
+            if (opt.tiled_epi_warps == 8 && !can8) {
+                delete p;
+                return fail(HGEMM_ERR_UNSUPPORTED,
+                            "eight epilogue warps need 16-bit inputs and tile width 128 or 256");
+            }
+            p->epi_warps = opt.tiled_epi_warps ? opt.tiled_epi_warps : 4;
+            p->epi_warps_ep = opt.tiled_epi_warps ? opt.tiled_epi_warps : (can8 && num_kb <= 16 ? 8 : 4);
         }
     } else if (p->path == HGEMM_PATH_SKINNY) {
         p->nu = M <= 16 ? 16 : 32;
@@ -774,6 +795,7 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.b_kmajor = p->opt.trans_b ? 1 : 0;
         tp.C = C;
         tp.ep = ep;
+        tp.epi_warps = ep.on ? p->epi_warps_ep : p->epi_warps;
         tp.ldc = p->ldc;
         tp.strideC = p->sC;
         tp.err = err;
@@ -981,7 +1003,9 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     if (plan->path == HGEMM_PATH_TILED) {
         r.tile_m = plan->pair ? 256 : 128;
         r.tile_n = plan->bn;
-        r.stages = plan->pair ? hg::pair_stages(plan->pair_ks) : hg::tiled_stages(plan->bn);
+        r.stages = plan->pair ? hg::pair_stages(plan->pair_ks) : hg::tiled_stages(plan->bn, plan->epi_warps);
+        r.epi_warps = plan->pair ? 4 : plan->epi_warps;
+        r.epi_warps_epilogue = plan->pair ? 4 : plan->epi_warps_ep;
         if (plan->pair) r.tile_k = kblock(plan->din) * plan->pair_ks;
         r.tma_store = plan->ldc_tma ? 1 : 0;
     } else if (plan->path == HGEMM_PATH_SKINNY) {

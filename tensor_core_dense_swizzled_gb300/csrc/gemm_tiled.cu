@@ -16,14 +16,19 @@
 //                        accumulate into a TMEM buffer, then tcgen05.commit
 //                        frees the stage.  After a tile's last K block it
 //                        commits tfull[buf].
-//   warps 2-5            epilogue: wait tfull[buf], tcgen05.ld 32-column
+//   warps 2-5 (or 2-9)   epilogue: wait tfull[buf], tcgen05.ld 32-column
 //                        chunks (lane = output row), convert, stage each
 //                        32-row x 128-byte piece in 128-byte-swizzled shared
 //                        memory and TMA-store it (section 四.5's point that
 //                        the epilogue should write full sectors), or write C
 //                        with predicated coalesced stores when C is not
 //                        16-byte aligned.  They release TMEM (tempty[buf]) as
-//                        soon as the last chunk is in registers.
+//                        soon as the last chunk is in registers.  With
+//                        eight epilogue warps (EW = 8: products with few K
+//                        blocks, where draining the accumulator bounds the
+//                        tile, e.g. batched S = Q K^T with K = 128), two
+//                        warps share each TMEM lane quarter, one per half of
+//                        the tile's 32-column chunks.
 // Two TMEM accumulator buffers let the epilogue of tile i overlap the main
 // loop of tile i+1 -- the effect "ping-pong" consumers buy on Hopper
 // (section 五.3).  The CTA loops over tiles (persistent; grid <= SM count) in
@@ -53,20 +58,21 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int NUM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int EPI_WARPS = 4;
 constexpr int STG_BYTES = EPI_STG_BYTES;
 constexpr int STG_BUFS = EPI_STG_BUFS;
 
-template <int BN>
+// EW: epilogue warps (4 or 8); warp 0 TMA, warp 1 MMA, warps 2 .. EW + 1 epilogue.
+template <int BN, int EW = 4>
 struct TiledCfg {
     static_assert(BN == 128 || BN == 192 || BN == 224 || BN == 256, "tile N");
+    static_assert(EW == 4 || EW == 8, "epilogue warps");
+    static constexpr int THREADS = 32 * (2 + EW);
     static constexpr int B_BLOCKS = (BN + 63) / 64;  // 64-column blocks of B per stage
     static constexpr uint32_t A_BYTES = BM * BK * 2;
     static constexpr uint32_t B_BLOCK = BK * 128;  // 64 k-rows x 64 n (128 bytes)
     static constexpr uint32_t B_BYTES = B_BLOCKS * B_BLOCK;
     static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STG_TOTAL = EPI_WARPS * STG_BUFS * STG_BYTES;
+    static constexpr int STG_TOTAL = EW * STG_BUFS * STG_BYTES;
     // as many stages as fit next to the epilogue staging (227 KB per CTA)
     static constexpr int STAGES = (232448 - STG_TOTAL - 2048) / (A_BYTES + B_BYTES);
     static constexpr uint32_t TMEM_STRIDE = BN <= 128 ? 128 : 256;  // column offset of buffer 1
@@ -87,13 +93,13 @@ __device__ __forceinline__ void tile_coords(const TiledParams &p, int t, int &b,
 
 // F8: 8-bit inputs (kind::f8f6f4), K blocks of 128 elements, both operands
 // K-major.
-template <int BN, int OUT, bool TMA_STORE, bool EPI, bool F8 = false>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int BN, int OUT, bool TMA_STORE, bool EPI, bool F8 = false, int EW = 4>
+__global__ void __launch_bounds__(32 * (2 + EW), 1)
     hgemm_tiled_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const TiledParams p) {
     constexpr int BKE = F8 ? 128 : 64;  // elements per K block (128 bytes either way)
-    using Cfg = TiledCfg<BN>;
+    using Cfg = TiledCfg<BN, EW>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -120,7 +126,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull(b), 1);
-            mbar_init(tempty(b), EPI_WARPS);
+            mbar_init(tempty(b), EW);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -247,6 +253,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;   // TMEM lane quarter this warp may read
         const int ew = warp - 2;  // staging slot
         const uint32_t stg = sC + ew * STG_BUFS * STG_BYTES;
+        // chunks [c_lo, c_hi) of the tile's 32-column chunks are this warp's
+        constexpr int NCH = BN / 32;
+        const int half = EW == 8 ? ew >> 2 : 0;
+        const int c_lo = EW == 8 && half ? (NCH + 1) / 2 : 0;
+        const int c_hi = EW == 8 && !half ? (NCH + 1) / 2 : NCH;
         const EpiArgs epi{&tmC, p.C, p.ldc, p.strideC, p.M, p.N, p.ep};
         int sbuf = 0;
         int local = 0;
@@ -257,15 +268,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t tph = (local >> 1) & 1;
             const int row0 = mt * BM + q * 32;
             const int col0 = nt * BN;
-            if constexpr (EPI) prefetch_c_prev<OUT>(epi, row0 + lane, col0, BN, b);
+            if constexpr (EPI) prefetch_c_prev<OUT>(epi, row0 + lane, col0 + 32 * c_lo, 32 * (c_hi - c_lo), b);
             if (!wait_bounded_warp(tfull(buf), tph, wc, timeout_code(ROLE_EPILOGUE, buf))) break;
             tc_fence_after();
             const uint32_t tbase =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * Cfg::TMEM_STRIDE;
-            drain_accumulator<OUT, TMA_STORE, BN, false, EPI>(tbase, stg, sbuf, row0, col0, b, epi,
-                                                  [&] {
-                                                      if (lane == 0) mbar_arrive(tempty(buf));
-                                                  });
+            drain_accumulator<OUT, TMA_STORE, BN, false, EPI>(
+                tbase, stg, sbuf, row0, col0, b, epi,
+                [&] {
+                    if (lane == 0) mbar_arrive(tempty(buf));
+                },
+                nullptr, c_lo, c_hi);
         }
         if (TMA_STORE && lane == 0) bulk_wait<0>();
     }
@@ -279,15 +292,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int BN, int OUT, bool TS, bool EPI, bool F8 = false>
+template <int BN, int OUT, bool TS, bool EPI, bool F8 = false, int EW = 4>
 cudaError_t launch_impl(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const TiledParams &p, int grid, cudaStream_t stream) {
-    auto kern = hgemm_tiled_kernel<BN, OUT, TS, EPI, F8>;
+    using Cfg = TiledCfg<BN, EW>;
+    auto kern = hgemm_tiled_kernel<BN, OUT, TS, EPI, F8, EW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TiledCfg<BN>::SMEM_TOTAL);
+                                         Cfg::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    return launch_dependent(kern, grid, NUM_THREADS, TiledCfg<BN>::SMEM_TOTAL, stream, tmA, tmB,
-                            tmC, p);
+    return launch_dependent(kern, grid, Cfg::THREADS, Cfg::SMEM_TOTAL, stream, tmA, tmB, tmC, p);
 }
 
 template <int BN, int OUT>
@@ -297,6 +310,7 @@ cudaError_t launch_ts(bool ts, const CUtensorMap &tmA, const CUtensorMap &tmB,
     // fused-epilogue variant
     if constexpr (BN == 128 || BN == 256) {
         if (p.f8) {
+            if (p.epi_warps != 4) return cudaErrorInvalidValue;
             if (p.ep.on)
                 return ts ? launch_impl<BN, OUT, true, true, true>(tmA, tmB, tmC, p, grid, s)
                           : launch_impl<BN, OUT, false, true, true>(tmA, tmB, tmC, p, grid, s);
@@ -306,6 +320,17 @@ cudaError_t launch_ts(bool ts, const CUtensorMap &tmA, const CUtensorMap &tmB,
     } else {
         if (p.f8) return cudaErrorInvalidValue;
     }
+    if constexpr (BN == 128 || BN == 256) {
+        // eight epilogue warps: 16-bit inputs, tile widths 128 and 256
+        if (p.epi_warps == 8) {
+            if (p.ep.on)
+                return ts ? launch_impl<BN, OUT, true, true, false, 8>(tmA, tmB, tmC, p, grid, s)
+                          : launch_impl<BN, OUT, false, true, false, 8>(tmA, tmB, tmC, p, grid, s);
+            return ts ? launch_impl<BN, OUT, true, false, false, 8>(tmA, tmB, tmC, p, grid, s)
+                      : launch_impl<BN, OUT, false, false, false, 8>(tmA, tmB, tmC, p, grid, s);
+        }
+    }
+    if (p.epi_warps != 4) return cudaErrorInvalidValue;
     if (p.ep.on)
         return ts ? launch_impl<BN, OUT, true, true>(tmA, tmB, tmC, p, grid, s)
                   : launch_impl<BN, OUT, false, true>(tmA, tmB, tmC, p, grid, s);
@@ -326,7 +351,14 @@ cudaError_t launch_out(int out, bool ts, const CUtensorMap &tmA, const CUtensorM
 
 }  // namespace
 
-int tiled_smem_bytes(int bn) {
+int tiled_smem_bytes(int bn, int epi_warps) {
+    if (epi_warps == 8) {
+        switch (bn) {
+            case 128: return TiledCfg<128, 8>::SMEM_TOTAL;
+            case 256: return TiledCfg<256, 8>::SMEM_TOTAL;
+            default: return 0;
+        }
+    }
     switch (bn) {
         case 128: return TiledCfg<128>::SMEM_TOTAL;
         case 192: return TiledCfg<192>::SMEM_TOTAL;
@@ -336,7 +368,14 @@ int tiled_smem_bytes(int bn) {
     }
 }
 
-int tiled_stages(int bn) {
+int tiled_stages(int bn, int epi_warps) {
+    if (epi_warps == 8) {
+        switch (bn) {
+            case 128: return TiledCfg<128, 8>::STAGES;
+            case 256: return TiledCfg<256, 8>::STAGES;
+            default: return 0;
+        }
+    }
     switch (bn) {
         case 128: return TiledCfg<128>::STAGES;
         case 192: return TiledCfg<192>::STAGES;

@@ -82,6 +82,10 @@ struct TiledParams {
     // 1: 8-bit inputs (E4M3 / E5M2, both operands K-major); a K block is 128
     // elements (num_kb counts those).
     int32_t f8;
+    // Single-CTA tiled kernel only: epilogue warps, 4 or 8 (8: two warps per
+    // TMEM lane quarter, each draining half of the tile's columns; 16-bit
+    // inputs and tile widths 128 / 256).
+    int32_t epi_warps;
 };
 
 // Skinny kernel: C^T = B^T . A^T, NB x 64 output columns of C per work
@@ -118,8 +122,8 @@ struct SkinnyParams {
 };
 
 // Shared memory the tiled kernel needs for a given BN (bytes, incl. alignment slack).
-int tiled_smem_bytes(int bn);
-int tiled_stages(int bn);
+int tiled_smem_bytes(int bn, int epi_warps);
+int tiled_stages(int bn, int epi_warps);
 int skinny_stages(int nu, int nb);
 
 // Launchers return cudaSuccess or the launch error.  `out` is an OutType.

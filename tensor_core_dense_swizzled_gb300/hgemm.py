@@ -65,6 +65,7 @@ class Options(ctypes.Structure):
         ("skinny_prefetch", ctypes.c_int),
         ("group_m", ctypes.c_int),
         ("trans_b", ctypes.c_int),
+        ("tiled_epi_warps", ctypes.c_int),
     ]
 
 
@@ -102,6 +103,8 @@ class PlanInfo(ctypes.Structure):
         ("wide_boxes", ctypes.c_int),
         ("trans_b", ctypes.c_int),
         ("stream_k", ctypes.c_int),
+        ("epi_warps", ctypes.c_int),
+        ("epi_warps_epilogue", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

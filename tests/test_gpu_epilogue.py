@@ -84,6 +84,11 @@ PATHS = {
     "pair_stream_k": (2560, 2048, 256, 1, H.Options(cta_pair=1, tail_mode=3), lambda i: i["stream_k"] == 1),
     "pair_dealt": (1536, 2560, 512, 1, H.Options(cta_pair=1, tail_mode=4), lambda i: i["stream_k"] == 2),
     "single_tma": (640, 512, 320, 1, H.Options(cta_pair=2), lambda i: i["tile_m"] == 128 and i["tma_store"]),
+    "single_tma_4warps": (640, 512, 320, 1, H.Options(cta_pair=2, tiled_epi_warps=4),
+                          lambda i: i["epi_warps"] == 4),
+    "single_generic_8warps": (333, 444, 222, 1, H.Options(cta_pair=2, tile_n=256, force_generic_store=1,
+                                                          tiled_epi_warps=8),
+                              lambda i: not i["tma_store"] and i["epi_warps"] == 8),
     "single_generic": (333, 444, 222, 1, H.Options(cta_pair=2, force_generic_store=1),
                        lambda i: not i["tma_store"]),
     "batched": (300, 256, 96, 3, H.Options(cta_pair=2), lambda i: i["tile_m"] == 128),

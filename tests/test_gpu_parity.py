@@ -381,6 +381,46 @@ def test_tile_variants(dev, tile_n, dout):
     check(got, Cref, Den, dout)
 
 
+@pytest.mark.parametrize("ew", [4, 8])
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("dout,generic", [("f32", False), ("bf16", False), ("f16", True), ("f32", True)])
+def test_tiled_epilogue_warps(dev, ew, tile_n, dout, generic):
+    """Four or eight epilogue warps on the single-CTA kernel (eight: two warps
+    per TMEM lane quarter, each storing half of a tile's 32-column chunks).
+    More tiles than SMs, so both accumulators and the stage ring wrap; ragged
+    M and N edges; TMA or predicated stores."""
+    M, N, K = 2900, 1904, 200  # rows of 16-bit C end on 16 bytes (TMA stores apply)
+    got, Cref, Den, info = run_case(dev, M, N, K, "bf16", dout, seed=ew + tile_n,
+                                    options=H.Options(cta_pair=2, tile_n=tile_n, tiled_epi_warps=ew,
+                                                      force_generic_store=int(generic)), runs=2)
+    assert info["epi_warps"] == ew and info["tile_n"] == tile_n and info["tma_store"] == int(not generic)
+    assert info["grid"] < ((M + 127) // 128) * ((N + tile_n - 1) // tile_n)
+    check(got, Cref, Den, dout)
+
+
+def test_tiled_epilogue_warps_choice_and_refusals(dev):
+    # automatic: four for plain runs; with the fused epilogue eight for few
+    # K blocks, four for long K (main loop bound)
+    for K, want in [(128, 8), (1024, 8), (1088, 4)]:
+        plan = H.hgemm_plan_create_ex(1024, 1024, K, K, 1024, 1024, 1, 0, 0, 0, DT["bf16"], DT["bf16"],
+                                      H.Options(cta_pair=2, tile_n=256))
+        try:
+            info = H.hgemm_plan_get_info(plan)
+            assert info["epi_warps"] == 4 and info["epi_warps_epilogue"] == want, K
+        finally:
+            H.hgemm_plan_destroy(plan)
+    for opt, status in [(H.Options(cta_pair=2, tile_n=192, tiled_epi_warps=8), 2),
+                        (H.Options(cta_pair=2, tiled_epi_warps=5), 1)]:
+        with pytest.raises(H.HgemmError) as ei:
+            H.hgemm_plan_create_ex(512, 512, 256, 256, 512, 512, 1, 0, 0, 0, DT["bf16"], DT["bf16"], opt)
+        assert ei.value.status == status
+    # 8-bit inputs keep four epilogue warps
+    with pytest.raises(H.HgemmError) as ei:
+        H.hgemm_plan_create_ex(512, 512, 256, 256, 256, 512, 1, 0, 0, 0, H.HGEMM_E4M3, DT["bf16"],
+                               H.Options(cta_pair=2, tile_n=256, trans_b=1, tiled_epi_warps=8))
+    assert ei.value.status == 2
+
+
 def test_many_tiles_per_cta(dev):
     """More tiles than SMs: every CTA loops, both TMEM buffers and the stage
     ring wrap many times."""
