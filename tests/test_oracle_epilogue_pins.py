@@ -5,8 +5,9 @@ The epilogue is D = act(alpha * rs[i] * cs[j] * (A.B)[i][j] + beta * C_prev[i][j
 "tensor-cores-cutlass-and-cute" lists among cuBLASLt's features (its
 comparison with cuBLAS), with the order of the terms read as scale, add,
 activate.  The pins below fix it against things other than its own formula:
-tabulated values of the normal CDF, identities of GELU and ReLU, the page-1
-worked example (D = 16 i j), and planted mistakes that must fail a pin.
+tabulated values of the normal CDF, PyTorch's own tanh-form GELU (a library
+routine, for the tanh form's constants), identities of GELU and ReLU, the
+page-1 worked example (D = 16 i j), and planted mistakes that must fail a pin.
 """
 import math
 
@@ -60,6 +61,51 @@ def test_gelu_tanh_form(oracle_mod):
     assert abs(oracle_mod.activation(np.array([20.0]), 3)[0] - 20.0) < 1e-12
     d = np.diff(g) / np.diff(x)
     assert d.max() <= oracle_mod.GELU_MAX_SLOPE + 2e-3
+
+
+def _torch_gelu_tanh(x):
+    """PyTorch's own tanh-form GELU (``approximate="tanh"``) in fp64: a
+    library routine written independently of the oracle, used here as the
+    fixed point the oracle's constants (sqrt(2/pi) and 0.044715) must meet."""
+    torch = pytest.importorskip("torch")
+    return torch.nn.functional.gelu(torch.from_numpy(np.asarray(x, dtype=np.float64)),
+                                    approximate="tanh").numpy()
+
+
+def test_gelu_tanh_matches_library(oracle_mod):
+    """Over [-10, 10] the oracle's tanh form agrees with PyTorch's to rounding
+    (both in fp64).  A wrong constant does not: 0.0447 for 0.044715 moves the
+    value by up to 8.7e-6, sqrt(2/pi) cut to 4 digits by more, seven orders of
+    magnitude above this pin's tolerance."""
+    x = np.linspace(-10.0, 10.0, 20001)
+    g = oracle_mod.activation(x, oracle_mod.ACT_GELU_TANH)
+    ref = _torch_gelu_tanh(x)
+    assert np.max(np.abs(g - ref)) <= 1e-13 * np.maximum(1.0, np.abs(x)).max()
+
+
+@pytest.mark.parametrize("mistake", ["cubic_constant_truncated", "sqrt_2_over_pi_truncated",
+                                     "cubic_term_squared", "half_dropped"])
+def test_planted_gelu_tanh_mistakes_are_caught(oracle_mod, mistake):
+    """Each slip in the tanh form fails the library pin above by orders of
+    magnitude more than its tolerance (the planted versions are computed here,
+    on the CPU, from the same formula with the slip in it)."""
+    x = np.linspace(-10.0, 10.0, 20001)
+    c, a, h = math.sqrt(2.0 / math.pi), 0.044715, 0.5
+    p = 3
+    if mistake == "cubic_constant_truncated":
+        a = 0.0447
+    elif mistake == "sqrt_2_over_pi_truncated":
+        c = 0.7979
+    elif mistake == "cubic_term_squared":
+        p = 2
+    else:
+        h = 1.0
+    bad = h * x * (1.0 + np.tanh(c * (x + a * x ** p)))
+    ref = _torch_gelu_tanh(x)
+    assert np.max(np.abs(bad - ref)) > 1e-6
+    # the oracle is not the planted version
+    g = oracle_mod.activation(x, oracle_mod.ACT_GELU_TANH)
+    assert np.max(np.abs(g - bad)) > 1e-6
 
 
 def test_relu(oracle_mod):
