@@ -25,6 +25,18 @@ the FLOPs of all ranks divided by the slowest rank's time.
 
 ``--impl reference`` times the CPU oracle (the only other implementation of
 the method) on the host cores on a bounded sample of the same workload.
+
+The default run (square4096) also measures every other GEMM configuration
+the method is judged on -- int512, square8192, batched_qk, ragged4095,
+ragged4095_h and skinny -- one after the other, outside the headline's timed
+region, and adds them to the same JSON line as ``per_config``: each with its
+own timed region (about half a second of back-to-back launches, L2 defeated
+the same way), roofline fraction, percentage of the stated peaks, the
+stated target when there is one, and clocks.  Each entry's ``cpu_baseline``
+times the oracle on sampled entries of that configuration's C and reports,
+from the same sample, the GPU result's normalised error
+(``max |C - Cref| / sum_k |A_ik||B_kj|``; int512 is compared in full, bit for
+bit).  ``--no-per-config`` skips them.
 """
 from __future__ import annotations
 
@@ -62,6 +74,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="square4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other configurations (default run only)")
+    ap.add_argument("--per-config-seconds", type=float, default=0.5,
+                    help="length of each configuration's timed region")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--epilogue", choices=["none", "bias_gelu", "bias_gelu_tanh", "beta_bias_relu"],
                     default="none",
@@ -337,6 +353,44 @@ def run_reference(args, w, rank, world):
     return 0
 
 
+# The targets stated for the configurations: a fraction of the stated dense
+# fp16/bf16 tensor peak (2.25 PFLOP/s) or of the stated HBM bandwidth (8 TB/s).
+STATED_TARGETS = {"square4096": ("tensor", 0.70), "square8192": ("tensor", 0.70),
+                  "skinny": ("hbm", 0.70)}
+PER_CONFIG = ("int512", "square8192", "batched_qk", "ragged4095", "ragged4095_h", "skinny")
+# acceptance bound on max |C - Cref| / Den per output type (bf16: the provable
+# 5e-3; the stated 4e-3 for 16-bit output is reported beside it)
+PARITY_TOL = {"f32": 1e-3, "f16": 4e-3, "bf16": 5e-3}
+STATED_16BIT_TOL = 4e-3
+
+
+def kernel_label(info) -> str:
+    """Which kernel a plan runs: pair (256 x 256 tiles on CTA pairs), single
+    (one CTA per 128 x tile_n tile) or skinny; "+copy" when an operand is
+    first copied to an aligned buffer."""
+    if info["path"] == 3:
+        k = "skinny"
+    elif info["path"] == 2:
+        k = "pair" if info["tile_m"] == 256 else "single"
+    else:
+        return {0: "empty", 1: "zero_fill"}.get(info["path"], "?")
+    return k + ("+copy" if info["repack_a"] or info["repack_b"] else "")
+
+
+def stated_target(w, tflops: float, gbs: float):
+    t = STATED_TARGETS.get(w.name)
+    if t is None:
+        return None
+    kind, frac = t
+    if kind == "tensor":
+        got = tflops / (NOMINAL_TC_TFLOPS * tensor_ratio(w))
+        return {"target": f">= {frac:.0%} of the stated {NOMINAL_TC_TFLOPS:g} TFLOP/s dense tensor peak",
+                "fraction": got, "met": got >= frac}
+    got = gbs / NOMINAL_HBM_GBS
+    return {"target": f">= {frac:.0%} of the stated {NOMINAL_HBM_GBS:g} GB/s HBM bandwidth",
+            "fraction": got, "met": got >= frac}
+
+
 def config_of(w, world, extra=None):
     c = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "dtype_in": w.dtype_in,
          "dtype_out": w.dtype_out, "seed": w.seed, "parallelism": "replicas" if world > 1 else "single",
@@ -344,6 +398,151 @@ def config_of(w, world, extra=None):
     if extra:
         c.update(extra)
     return c
+
+
+# ---------------------------------------------------------------- per-configuration runs
+
+def config_cpu_check(w, A, B, C_dev, sample_entries: int = 1024, seed: int = 99):
+    """The cpu_baseline leg of one configuration: times the oracle, as it
+    stands, on a sample of C's entries (every entry for int512, whose product
+    the oracle computes in a fraction of a second), and compares the GPU's C
+    with it there.  Returns (cpu_baseline, parity)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    ab = A.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    bb = B.contiguous().view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    din = ORACLE_IN[w.dtype_in]
+    C = C_dev.reshape(w.batch, w.M, w.N)
+    threads = os.cpu_count() or 1
+    if w.name == "int512":
+        t0 = time.perf_counter()
+        Cref, Den = oracle.gemm(ab, bb, din, w.M, w.N, w.K, w.lda, w.ldb, w.batch, w.strideA,
+                                w.strideB, threads=threads)
+        dt = time.perf_counter() - t0
+        got = C.double().cpu().numpy()
+        exact = bool(np.array_equal(got, Cref))
+        cpu = {"value": flops_of(w) / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"the whole {w.M}x{w.N}x{w.K} product, {dt:.2f} s"}
+        return cpu, {"entries": w.M * w.N, "bit_exact": exact,
+                     "max_normalised_error": oracle.normalized_error(got, Cref, Den), "pass": exact}
+    rng = np.random.default_rng(seed)
+    eb = rng.integers(0, w.batch, sample_entries)
+    ei = rng.integers(0, w.M, sample_entries)
+    ej = rng.integers(0, w.N, sample_entries)
+    # the corners and the last row and column (ragged edges)
+    eb = np.concatenate([eb, [0, 0, w.batch - 1, w.batch - 1], np.full(32, w.batch - 1),
+                         np.full(32, w.batch - 1)])
+    ei = np.concatenate([ei, [0, w.M - 1, 0, w.M - 1], np.full(32, w.M - 1), rng.integers(0, w.M, 32)])
+    ej = np.concatenate([ej, [0, w.N - 1, w.N - 1, 0], rng.integers(0, w.N, 32), np.full(32, w.N - 1)])
+    vals = C[torch.as_tensor(eb, device=C.device), torch.as_tensor(ei, device=C.device),
+             torch.as_tensor(ej, device=C.device)].cpu()
+    if w.dtype_out == "f32":
+        got = vals.double().numpy()
+    else:
+        got = oracle.decode(vals.view(torch.int16).numpy().view(np.uint16), ORACLE_IN[w.dtype_out])
+    t0 = time.perf_counter()
+    cref, den = oracle.gemm_entries(ab, bb, din, w.K, w.lda, w.ldb, eb, ei, ej, w.strideA, w.strideB)
+    dt = time.perf_counter() - t0
+    err = oracle.normalized_error(got, cref, den)
+    cpu = {"value": 2 * eb.size * w.K / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+           "sample": f"{eb.size} entries of C (random, corners, last row and column), "
+                     f"one fp64 dot product of length {w.K} each, {dt * 1e3:.0f} ms"}
+    par = {"entries": int(eb.size), "max_normalised_error": err, "tolerance": PARITY_TOL[w.dtype_out],
+           "pass": err <= PARITY_TOL[w.dtype_out]}
+    if w.dtype_out != "f32":
+        par["stated_tolerance"] = STATED_16BIT_TOL
+        par["pass_stated"] = err <= STATED_16BIT_TOL
+    return cpu, par
+
+
+def measure_config(name, H, dev, stream, sampler, peaks, seconds: float, with_cpu: bool):
+    """One configuration in the launch configuration of the headline: rotating
+    input/output sets larger than 2 x L2, warm-up, then back-to-back launches
+    for about `seconds` between two CUDA events on the launching stream."""
+    import torch
+
+    from tensor_core_dense_swizzled_gb300 import inputs
+    DT = {"f16": H.HGEMM_F16, "bf16": H.HGEMM_BF16, "f32": H.HGEMM_F32}
+    TD = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    w = inputs.WORKLOADS[name]
+    A, B = inputs.make_inputs(w)
+    fl = flops_of(w)
+    min_bytes, ob = min_bytes_of(w)
+    set_bytes = (A.numel() + B.numel()) * in_bytes_of(w) + w.batch * w.M * w.N * ob
+    nsets = max(1, math.ceil(2 * L2_BYTES / set_bytes))
+    shape_c = (w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N)
+    sets, plans = [], []
+    try:
+        for _ in range(nsets):
+            sets.append((A.to(dev), B.to(dev), torch.empty(shape_c, dtype=TD[w.dtype_out], device=dev)))
+            plans.append(H.hgemm_plan_create_ex(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, w.batch, w.strideA,
+                                                w.strideB, w.strideC, DT[w.dtype_in], DT[w.dtype_out],
+                                                H.Options(trans_b=int(w.trans_b))))
+        info = H.hgemm_plan_get_info(plans[0])
+
+        def run(n, i0=0):
+            for i in range(i0, i0 + n):
+                a, b, c = sets[i % nsets]
+                H.hgemm_run(plans[i % nsets], a, b, c, stream)
+
+        run(max(5, nsets))
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run(20)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        est_ms = e0.elapsed_time(e1) / 20
+        steps = int(min(20000, max(100, round(seconds * 1e3 / max(est_ms, 1e-3)))))
+        torch.cuda.synchronize(dev)
+        t_wall0 = time.time()
+        e0.record(stream)
+        run(steps)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall1 = time.time()
+        region_ms = e0.elapsed_time(e1)
+        for p in plans:
+            st = H.hgemm_check(p, stream)
+            if st != 0:
+                raise RuntimeError(f"{name}: {H.STATUS.get(st)} {H.hgemm_last_error_detail()}")
+        clocks = sampler.summary(t_wall0, t_wall1)
+        ms = region_ms / steps
+        tflops = fl / (ms * 1e-3) / 1e12
+        gbs = min_bytes / (ms * 1e-3) / 1e9
+        bound = roofline_bound(w)
+        sustained = region_ms > 1000.0
+        if bound == "tensor":
+            peak = (peaks["bf16_sustained"] if sustained else peaks["bf16"]) * tensor_ratio(w)
+            roof = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                    "frac": tflops / peak,
+                    "peak_kind": ("sustained" if sustained else "burst") + f" bf16, {peaks['source']}"}
+        else:
+            roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm"], "peak_kind": f"copy bandwidth, {peaks['source']}"}
+        roof["traffic"] = committed_traffic(w.name)
+        roof["kernels_per_launch"] = info["kernels_per_run"]
+        entry = {
+            "workload": name, "M": w.M, "N": w.N, "K": w.K, "batch": w.batch, "dtype_in": w.dtype_in,
+            "dtype_out": w.dtype_out, "seed": w.seed, "kernel": kernel_label(info),
+            "tile": [info["tile_m"], info["tile_n"], info["tile_k"]], "grid": info["grid"],
+            "steps": steps, "ms_per_step": ms, "value": tflops, "unit": "TFLOP/s", "gbs": gbs,
+            "pct_nominal_tensor_peak": 100.0 * tflops / (NOMINAL_TC_TFLOPS * tensor_ratio(w)),
+            "pct_nominal_hbm": 100.0 * gbs / NOMINAL_HBM_GBS, "roofline": roof,
+            "stated_target": stated_target(w, tflops, gbs), "clocks": clocks,
+            "l2": f"{nsets} rotating sets ({nsets * set_bytes / 2**20:.0f} MiB)",
+        }
+        if with_cpu:
+            entry["cpu_baseline"], entry["parity"] = config_cpu_check(w, A, B, sets[0][2])
+        return entry, steps * info["kernels_per_run"]
+    finally:
+        for p in plans:
+            H.hgemm_plan_destroy(p)
+        del sets
+        torch.cuda.empty_cache()
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -482,13 +681,35 @@ def run_ours(args, w, world, rank, local, pg):
         e2e = {"value": flops * args.e2e_steps * world / dt / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": A.numel() * ib + B.numel() * ib,
                "d2h_bytes_per_step": w.batch * w.M * w.N * ob, "steps": args.e2e_steps}
+        e2e.update(host_link_rates(Ah, Bh, Ch, sets[0], stream, dev))
+        e2e["ms_per_step"] = dt / args.e2e_steps * 1e3
+
+    for p in plans:
+        H.hgemm_plan_destroy(p)
+    del sets
+    torch.cuda.empty_cache()
+
+    # the other configurations, each with its own timed region (after the
+    # headline's, so they do not change it)
+    per_config = None
+    if (world == 1 and w.name == "square4096" and args.epilogue == "none"
+            and not args.no_per_config):
+        per_config = []
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.3)
+        try:
+            for name in PER_CONFIG:
+                entry, _ = measure_config(name, H, dev, stream, sampler, load_peaks(),
+                                          args.per_config_seconds, not args.no_cpu_baseline)
+                per_config.append(entry)
+        finally:
+            sampler.stop()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
 
-    for p in plans:
-        H.hgemm_plan_destroy(p)
     if rank != 0:
         return 0
     line = {
@@ -498,18 +719,52 @@ def run_ours(args, w, world, rank, local, pg):
         "config": config_of(w, world, {
             "l2": f"{nsets} rotating input/output sets ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)",
             "path": {2: "tiled", 3: "skinny", 1: "zero_fill", 0: "empty"}[info["path"]],
+            "kernel": kernel_label(info),
             "tile": [info["tile_m"], info["tile_n"], info["tile_k"]], "stages": info["stages"],
             "split_k": info["split_k"], "grid": info["grid"], "epilogue": args.epilogue}),
         "pct_nominal_tensor_peak": 100.0 * value / world / (NOMINAL_TC_TFLOPS * tensor_ratio(w)),
         "pct_nominal_hbm": 100.0 * (min_bytes * args.steps / (region_ms * 1e-3) / 1e9) / NOMINAL_HBM_GBS,
+        "stated_target": stated_target(w, value / world,
+                                       min_bytes * args.steps / (region_ms * 1e-3) / 1e9),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * info["kernels_per_run"],
         "clocks": clocks,
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
     return 0
+
+
+def host_link_rates(Ah, Bh, Ch, dev_set, stream, dev, reps: int = 5):
+    """Achieved host <-> device copy rates of the step's own buffers (pinned
+    host memory), each direction alone: best of `reps`, CUDA events on the
+    stream.  They bound the end-to-end step, whose copies and kernel run one
+    after the other on one stream."""
+    import torch
+    dA, dB, dC = dev_set
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    h2d, d2h = [], []
+    nb_in = Ah.numel() * Ah.element_size() + Bh.numel() * Bh.element_size()
+    nb_out = Ch.numel() * Ch.element_size()
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            e0.record(stream)
+            dA.copy_(Ah, non_blocking=True)
+            dB.copy_(Bh, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            h2d.append(e0.elapsed_time(e1))
+            e0.record(stream)
+            Ch.copy_(dC, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            d2h.append(e0.elapsed_time(e1))
+    return {"h2d_gbs": nb_in / (min(h2d) * 1e-3) / 1e9, "d2h_gbs": nb_out / (min(d2h) * 1e-3) / 1e9,
+            "copies": "serialised with the kernel on one stream"}
 
 
 # ---------------------------------------------------------------- attention

@@ -12,8 +12,10 @@
  * output (fp32 -> fp16/bf16 rounds to nearest even).  Element (i,k) of A_b is at
  * A + b*strideA + i*lda + k, element (k,j) of B_b at B + b*strideB + k*ldb + j,
  * and element (i,j) of C_b at C + b*strideC + i*ldc + j.  All leading
- * dimensions and strides count elements, not bytes.  C is overwritten (no
- * alpha/beta).  The argument checks follow the host wrapper of the
+ * dimensions and strides count elements, not bytes.  hgemm_run overwrites C;
+ * hgemm_run_ex adds a fused epilogue (alpha, beta times C's previous value,
+ * scales, bias, activation; declared below).  The argument checks follow the
+ * host wrapper of the
  * "tensor-cores-cutlass-and-cute" Ampere kernel (section 四.4): a bad dtype or
  * shape is refused, never reinterpreted.
  *
@@ -228,7 +230,10 @@ hgemm_status_t hgemm_run_ex(hgemm_plan_t plan, const void *A, const void *B, voi
  * copies A and B to plan-owned device buffers on `stream`, runs the product,
  * copies the M x N block(s) of C back into the host buffer (elements outside
  * the block are left untouched), and synchronises `stream` before returning.
- * The device buffers are allocated on the first call and kept by the plan. */
+ * It then reads the plan's device error word as hgemm_check does: after a
+ * watchdog timeout it returns HGEMM_ERR_TIMEOUT (C_host is then incomplete)
+ * and clears the word.  The device buffers are allocated on the first call
+ * and kept by the plan. */
 hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void *B_host,
                               void *C_host, void *stream);
 
@@ -279,8 +284,9 @@ hgemm_status_t hgemm_watchdog_selftest(uint64_t timeout_ns, void *stream, int32_
  *   `stream`, asynchronous.
  * Its split-K partial sums, counters and error word live in one 8 MiB
  * __device__ array inside the library, held by every GPU that loads it until
- * the process exits.  The first call on each device looks up that array's
- * device address; make the first call before any stream capture.  Every call
+ * the process exits.  The first call on each device (and the first after
+ * the device gets a new CUDA context) looks up that array's device address;
+ * make the first call before any stream capture.  Every call
  * shares the array: calls that overlap on the GPU race and must be ordered.
  * The split count is lowered to fit the array; a request that does not fit
  * even unsplit returns HGEMM_ERR_UNSUPPORTED, as do misaligned operands and

@@ -850,6 +850,23 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "skinny kernel launch");
 }
 
+// Reads the plan's device error word (the plan's stream must be idle):
+// HGEMM_ERR_TIMEOUT with the role and barrier when a watchdog fired, after
+// clearing the word and any split-K counters the aborted run left behind.
+hgemm_status_t read_error_word(hgemm_plan_s *p) {
+    if (!p->ws) return HGEMM_OK;
+    int32_t word = 0;
+    cudaError_t e = cudaMemcpy(&word, p->ws, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word == 0) return HGEMM_OK;
+    cudaMemset(p->ws, 0, p->off_partials);
+    const unsigned role = (static_cast<uint32_t>(word) >> 16) & 0xFFu;
+    const unsigned idx = static_cast<uint32_t>(word) & 0xFFFFu;
+    static const char *names[] = {"?", "TMA producer", "MMA issuer", "epilogue", "drain", "self-test"};
+    return fail(HGEMM_ERR_TIMEOUT, "device wait timed out: role %s, barrier %u (code 0x%08x)",
+                role < 6 ? names[role] : "?", idx, static_cast<uint32_t>(word));
+}
+
 // ---------------------------------------------------------------- one-shot cache
 
 using CacheKey = std::tuple<int, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t,
@@ -961,7 +978,8 @@ hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void 
     }
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    return HGEMM_OK;
+    // the product ran: a watchdog timeout left C incomplete
+    return read_error_word(p);
 }
 
 hgemm_status_t hgemm_check(hgemm_plan_t plan, void *stream) {
@@ -969,19 +987,7 @@ hgemm_status_t hgemm_check(hgemm_plan_t plan, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "stream reports an error");
-    int32_t word = 0;
-    e = cudaMemcpy(&word, plan->ws, sizeof(word), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-    if (word != 0) {
-        // clear the word and any split-K counters an aborted run left behind
-        cudaMemset(plan->ws, 0, plan->off_partials);
-        const unsigned role = (static_cast<uint32_t>(word) >> 16) & 0xFFu;
-        const unsigned idx = static_cast<uint32_t>(word) & 0xFFFFu;
-        static const char *names[] = {"?", "TMA producer", "MMA issuer", "epilogue", "drain", "self-test"};
-        return fail(HGEMM_ERR_TIMEOUT, "device wait timed out: role %s, barrier %u (code 0x%08x)",
-                    role < 6 ? names[role] : "?", idx, static_cast<uint32_t>(word));
-    }
-    return HGEMM_OK;
+    return read_error_word(plan);
 }
 
 hgemm_status_t hgemm_plan_destroy(hgemm_plan_t plan) {

@@ -16,12 +16,16 @@
 // it until the process exits.  In host code the name `g_scratch` is only a
 // host-side stand-in for the symbol, never a device address: the first call
 // on each device looks up the real address with cudaGetSymbolAddress (with
-// that device current) and caches it, so make that first call before any
-// stream capture.  All calls on a device share the one array and it keeps
-// the last call's contents: each call clears the error word and the counters
-// (cudaMemsetAsync on the caller's stream) before its kernel runs, and the
-// partial sums need no clearing because every one is written before it is
-// read.  Calls that overlap on the GPU (two streams, or two host threads
+// that device current) and caches it, keyed by the device's current CUDA
+// context, so make that first call before any stream capture.  A new context
+// on the device (after cudaDeviceReset, say) reloads the module and may move
+// the array: the next call sees the new context's id and looks the address
+// up again (when the driver cannot report a context id, every call looks it
+// up, which is a cheap host call).  All calls on a device share the one
+// array and it keeps the last call's contents: each call clears the error
+// word and the counters (cudaMemsetAsync on the caller's stream) before its
+// kernel runs, and the partial sums need no clearing because every one is
+// written before it is read.  Calls that overlap on the GPU (two streams, or two host threads
 // without ordering) race on the array and give wrong results: order them.
 //
 // Limits.  M <= 32, batch 1, and A and B must be directly readable by TMA
@@ -31,7 +35,9 @@
 // fit in the array, and a request that does not fit even unsplit is refused
 // with HGEMM_ERR_UNSUPPORTED.  A device watchdog timeout is recorded in the
 // array's error word (cleared by the next call) but not reported here.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdio>
 #include <mutex>
@@ -49,26 +55,66 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
+// The address of g_scratch found on a device, and the id of the context it
+// was found in.
+struct ScratchAddr {
+    bool valid;
+    unsigned long long ctx_id;
+    void *ptr;
+};
 std::mutex g_mu;
-void *g_scratch_dev[kMaxDevices] = {};
+ScratchAddr g_scratch_dev[kMaxDevices] = {};
 
-// Device address of g_scratch on `dev` (which must be current).
+// Unique id of the calling thread's current CUDA context (cuCtxGetId, reached
+// through the runtime's driver entry points); false when there is no current
+// context or the driver cannot say.
+bool current_context_id(unsigned long long *id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_scratch on `dev` (which must be current), looked up
+// once per context of that device.
 hgemm_status_t scratch_address(int dev, unsigned char **out) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (dev < 0 || dev >= kMaxDevices)
         return hg::set_error_detail(HGEMM_ERR_UNSUPPORTED, "device ordinal too large");
-    if (!g_scratch_dev[dev]) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            char msg[256];
-            snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(scratch) failed: %s",
-                     cudaGetErrorString(e));
-            return hg::set_error_detail(HGEMM_ERR_CUDA, msg);
-        }
-        g_scratch_dev[dev] = p;
+    ScratchAddr &slot = g_scratch_dev[dev];
+    unsigned long long id = 0;
+    if (slot.valid && current_context_id(&id) && id == slot.ctx_id) {
+        *out = static_cast<unsigned char *>(slot.ptr);
+        return HGEMM_OK;
     }
-    *out = static_cast<unsigned char *>(g_scratch_dev[dev]);
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);  // also makes the context current
+    if (e != cudaSuccess || p == nullptr) {
+        char msg[256];
+        snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(scratch) failed: %s", cudaGetErrorString(e));
+        return hg::set_error_detail(HGEMM_ERR_CUDA, msg);
+    }
+    // keyed by the context it belongs to; not kept when no id is available
+    slot.valid = current_context_id(&id);
+    slot.ctx_id = id;
+    slot.ptr = p;
+    *out = static_cast<unsigned char *>(p);
     return HGEMM_OK;
 }
 

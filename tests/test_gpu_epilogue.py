@@ -148,3 +148,19 @@ def test_epilogue_rejects_bad_arguments(dev):
                 H.hgemm_run_ex(plan, A, A, C, e)
     finally:
         H.hgemm_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("generic", [0, 1])
+@pytest.mark.parametrize("act", [H.HGEMM_ACT_GELU, H.HGEMM_ACT_GELU_TANH])
+@pytest.mark.parametrize("dout", ["bf16", "f32"])
+def test_eight_epilogue_warps_ragged_last_tile(dev, generic, act, dout):
+    """Eight epilogue warps split each 128 x 256 tile's eight 32-column chunks
+    in two halves.  With N = 1904 (= 7 x 256 + 112) the last column tile holds
+    3.5 chunks of C: the first half ends inside C and the second half lies
+    wholly past column N-1, so its C-prefetch and stores must do nothing.
+    beta != 0 (C read back), bias and GELU, TMA and predicated stores."""
+    epi = dict(alpha=0.75, beta=0.5, bias=True, rs=False, cs=True, act=act)
+    opt = H.Options(cta_pair=2, tile_n=256, tiled_epi_warps=8, force_generic_store=generic)
+    info = run_epi(dev, 300, 1904, 256, "bf16", dout, epi, options=opt, seed=11, runs=2)
+    assert info["epi_warps_epilogue"] == 8 and info["tile_n"] == 256
+    assert bool(info["tma_store"]) == (not generic)

@@ -28,6 +28,11 @@ pytestmark = pytest.mark.gpu
 DT = {"f16": H.HGEMM_F16, "bf16": H.HGEMM_BF16, "f32": H.HGEMM_F32}
 ORACLE_DT = {"f16": 0, "bf16": 1}
 TOL = {"f32": 1e-3, "f16": 4e-3, "bf16": 5e-3}
+# The target states 4e-3 for every 16-bit output.  For bf16 the arithmetic
+# guarantees only 5e-3 at any K (its unit roundoff is 2^-8), so TOL keeps the
+# provable bound; on the full-size workloads with 16-bit output the stated
+# 4e-3 is asserted as well.
+STATED_16BIT = 4e-3
 TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 
 
@@ -678,9 +683,40 @@ def test_workload_full_size_sampled(dev, name):
     else:
         got = oracle.decode(bits(vals), ORACLE_DT[w.dtype_out])
     err = oracle.normalized_error(got, cref, den)
+    print(f"{name}: max normalised error on {eb.size} sampled entries {err:.3e}")
     assert err <= TOL[w.dtype_out], f"{name}: normalised error {err:.3e}"
+    if w.dtype_out != "f32":
+        assert err <= STATED_16BIT, f"{name}: normalised error {err:.3e} > {STATED_16BIT}"
     # properties that hold everywhere: finite output
     assert torch.isfinite(Cc.float()).all()
+
+
+@pytest.mark.parametrize("name", ["square4096", "ragged4095", "ragged4095_h", "skinny"])
+def test_workload_full_compare(dev, name):
+    """Every element of the full-size product, run by the plan the bench times
+    (same shape, leading dimensions and options), against the oracle's full
+    product: the oracle needs a few seconds per 4096^3 product on the host
+    cores.  (square8192 stays sampled: its oracle product takes minutes.)"""
+    w = inputs.WORKLOADS[name]
+    A, B = inputs.make_inputs(w)
+    dA, dB = A.to(dev), B.to(dev)
+    C = torch.full((w.M, w.N), SENTINEL[w.dtype_out], dtype=TORCH[w.dtype_out], device=dev)
+    plan = H.hgemm_plan_create_ex(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, w.batch, w.strideA,
+                                  w.strideB, w.strideC, DT[w.dtype_in], DT[w.dtype_out],
+                                  H.Options(trans_b=0))
+    try:
+        H.hgemm_run(plan, dA, dB, C)
+        st = H.hgemm_check(plan)
+        assert st == 0, H.hgemm_last_error_detail()
+    finally:
+        H.hgemm_plan_destroy(plan)
+    Cref, Den = oracle.gemm(bits(A), bits(B), ORACLE_DT[w.dtype_in], w.M, w.N, w.K, w.lda, w.ldb)
+    got = read_c(C.reshape(-1), w.dtype_out, w.M, w.N, w.ldc, 1, 0, 0)
+    err = oracle.normalized_error(got, Cref, Den)
+    print(f"{name}: max normalised error over all {w.M * w.N} entries {err:.3e}")
+    assert err <= TOL[w.dtype_out], f"{name}: normalised error {err:.3e}"
+    if w.dtype_out != "f32":
+        assert err <= STATED_16BIT, f"{name}: normalised error {err:.3e} > {STATED_16BIT}"
 
 
 def test_batched_qk_full_compare(dev):

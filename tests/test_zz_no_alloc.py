@@ -98,6 +98,45 @@ def test_no_alloc_small_shapes_and_outputs(dev):
             assert oracle.normalized_error(got, Cref, Den) <= tol
 
 
+def test_no_alloc_lowers_the_split_to_fit(dev):
+    """M = 32, N = 16384, K = 8192: the planned path splits K seven ways
+    (64 column tiles of 256 fill too few of the SMs), and its fp32 partials,
+    7 x 128 sub-tiles x 32 x 128 x 4 bytes = 14 MiB, would not fit the 8 MiB
+    array.  The allocation-free call runs with the split lowered to three
+    (6 MiB) and must still match the oracle and the planned path, twice."""
+    M, N, K = 32, 16384, 8192
+    A = inputs.make_random((M, K), "bf16", 31)
+    B = inputs.make_random((K, N), "bf16", 32, "normal", 0.02)
+    dA, dB = A.to(dev), B.to(dev)
+    lib = H.load()
+    C_plan = torch.empty(M, N, dtype=torch.float32, device=dev)
+    plan = H.hgemm_plan_create(M, N, K, K, N, N, 1, 0, 0, 0, H.HGEMM_BF16, H.HGEMM_F32)
+    try:
+        info = H.hgemm_plan_get_info(plan)
+        # the premise: the planned split would overflow the fixed array
+        num_n = (N + info["tile_n"] - 1) // info["tile_n"] * (info["tile_n"] // 128)
+        assert info["split_k"] * num_n * 32 * 128 * 4 > (8 << 20)
+        H.hgemm_run(plan, dA, dB, C_plan)
+        assert H.hgemm_check(plan) == 0
+    finally:
+        H.hgemm_plan_destroy(plan)
+    Cref, Den = oracle.gemm(bits(A), bits(B), 1, M, N, K, K, N)
+    planned = C_plan.cpu().double().numpy()[None]
+    assert oracle.normalized_error(planned, Cref, Den) <= 1e-3
+    outs = []
+    for _ in range(2):
+        C = torch.full((M, N), 7.0, dtype=torch.float32, device=dev)
+        st = noalloc(lib, dA, dB, C, M, N, K, K, N, N, H.HGEMM_BF16, H.HGEMM_F32)
+        assert st == 0, H.hgemm_last_error_detail()
+        torch.cuda.synchronize()
+        got = C.cpu().double().numpy()[None]
+        assert oracle.normalized_error(got, Cref, Den) <= 1e-3
+        nz = Den > 0
+        assert np.max(np.abs(got - planned)[nz] / Den[nz]) <= 1e-3
+        outs.append(C.cpu())
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_no_alloc_refuses_what_it_cannot_do(dev):
     lib = H.load()
     A = torch.zeros(64 * 72, dtype=torch.float16, device=dev)
