@@ -117,6 +117,13 @@ typedef struct {
                                  inputs are 16-bit, the tile 128 or 256 wide and K <= 1024), 4,
                                  or 8 (16-bit inputs and tile widths 128 / 256 only, else
                                  HGEMM_ERR_UNSUPPORTED) */
+    int debug_withhold_kb;    /* testing the abort path only: 0 off; k >= 1 makes CTA 0 of the
+                                 single-CTA tiled kernel leave the pipeline stage of K block k of
+                                 its first tile unarmed and unloaded, so the MMA issuer's wait on it
+                                 runs out after timeout_ns; the run then leaves C incomplete and
+                                 hgemm_check returns HGEMM_ERR_TIMEOUT.  k <= ceil(K / 64); plans
+                                 that take another kernel (CTA pairs, skinny, 8-bit inputs) get
+                                 HGEMM_ERR_UNSUPPORTED */
 } hgemm_options_t;
 
 /* Read-only description of what a plan will launch. */

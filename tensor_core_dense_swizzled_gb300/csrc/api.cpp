@@ -426,6 +426,8 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         return fail(HGEMM_ERR_INVALID_ARG, "tiled_epi_warps must be 0, 4 or 8");
     if (opt.skinny_prefetch < -1 || opt.skinny_prefetch > 64)
         return fail(HGEMM_ERR_INVALID_ARG, "skinny_prefetch must be in [-1, 64]");
+    if (opt.debug_withhold_kb < 0)
+        return fail(HGEMM_ERR_INVALID_ARG, "debug_withhold_kb must be >= 0");
     if (opt.cta_pair == 1 && opt.tile_n != 0 && opt.tile_n != 256 && opt.tile_n != 224)
         return fail(HGEMM_ERR_INVALID_ARG, "CTA-pair tiles are 256 x 256 or 256 x 224 (tile_n 0, 256 or 224)");
     if (is_f8(din) && M > 0 && N > 0 && K > 0) {
@@ -608,6 +610,13 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
             const int64_t units = work * p->split;
             p->grid = static_cast<int>(units < sms ? units : sms);
         }
+    }
+    if (opt.debug_withhold_kb > 0 &&
+        (p->path != HGEMM_PATH_TILED || p->pair || is_f8(din) || opt.debug_withhold_kb > num_kb)) {
+        delete p;
+        return fail(HGEMM_ERR_UNSUPPORTED,
+                    "debug_withhold_kb applies to the single-CTA tiled kernel, 16-bit inputs, "
+                    "k <= ceil(K / 64)");
     }
     st = alloc_workspace(p);
     if (st != HGEMM_OK) {
@@ -808,6 +817,7 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.max_seg = p->max_seg;
         tp.partials = reinterpret_cast<float *>(p->ws + p->off_partials);
         tp.tail_sync = reinterpret_cast<int32_t *>(p->ws + p->off_counters);
+        tp.withhold_kb = p->pair ? 0 : p->opt.debug_withhold_kb;
         if (p->pair)
             e = hg::launch_pair(p->bn, p->pair_ks, out_type(p->dout), ts, p->tmA, p->tmB, p->tmC, tp,
                                 p->grid, s);

@@ -21,10 +21,11 @@
 //   full[s]    leader only: armed by the leader's producer with the bytes of
 //              BOTH CTAs' stage s (64 KB); each CTA's TMA load counts its
 //              bytes on the leader's barrier (.cta_group::2 loads).
-//   empty[s]   both CTAs: the leader's MMA thread commits with a multicast to
-//              both once the stage's MMAs are done; each producer waits on
-//              its own before overwriting its half of the stage.
-//   tfull[b]   both CTAs: multicast commit after a tile's last K block.
+//   empty[s]   both CTAs: the leader's MMA thread commits to each CTA's
+//              barrier (two point-to-point commits) once the stage's MMAs
+//              are done; each producer waits on its own before overwriting
+//              its half of the stage.
+//   tfull[b]   both CTAs: the same two commits after a tile's last K block.
 //   tempty[b]  leader only, 8 arrivals: the 4 epilogue warps of each CTA
 //              (the odd CTA's arrive remotely, cluster-scope release).
 //   drain      leader only: MMA completion before TMEM is freed.
@@ -407,6 +408,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
+            // Completion signals go to each CTA's barrier by its cluster
+            // address: the barriers sit at the same offsets in both CTAs, so
+            // one mapa per CTA of the barrier block gives them all.
+            const uint32_t own_bars = mapa_shared(bar0, 0);
+            const uint32_t peer_bars = mapa_shared(bar0, 1);
+            auto commit_both = [&](uint32_t bar) {
+                umma_commit_pair_to(own_bars + (bar - bar0));
+                umma_commit_pair_to(peer_bars + (bar - bar0));
+            };
             PairSched sched(p, num_ks, pair, npairs);
             Piece w;
             for (; ok && sched.next(p, num_ks, npairs, w); ++local) {
@@ -456,16 +466,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 umma_f16_pair(d_tmem, ad, bd, p.idesc, (s > 0 || k > 0) ? 1u : acc0);
                         }
                     }
-                    umma_commit_pair(empty(stage), 0x3);
+                    commit_both(empty(stage));
                     if (++stage == Cfg::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(tfull(buf), 0x3);
+                commit_both(tfull(buf));
             }
-            umma_commit_pair(drain, 0x1);
+            umma_commit_pair_to(own_bars + (drain - bar0));
             wait_bounded(drain, 0, wc, 0, /*honor_abort=*/false);
         }
     } else {

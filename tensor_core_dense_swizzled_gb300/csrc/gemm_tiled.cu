@@ -167,6 +167,18 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
                         ok = false;
                         break;
                     }
+                    if (p.withhold_kb && blockIdx.x == 0 && t == 0 && kb == p.withhold_kb - 1) {
+                        // Abort-path testing: this stage is never armed or
+                        // loaded, so the MMA issuer's wait on full[stage]
+                        // expires; it is still counted as issued, and the
+                        // teardown's wait on it is bounded as well.
+                        ++issued;
+                        if (++stage == Cfg::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     mbar_arrive_expect_tx(full(stage), Cfg::TX_BYTES);
                     tma_load_3d(sA + stage * Cfg::A_BYTES, &tmA, full(stage), kb * BKE, mt * BM, b);
                     // 64 x 64 blocks of B: (n, k) MN-major, or (k, n) K-major

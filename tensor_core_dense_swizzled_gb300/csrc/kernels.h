@@ -86,6 +86,10 @@ struct TiledParams {
     // TMEM lane quarter, each draining half of the tile's columns; 16-bit
     // inputs and tile widths 128 / 256).
     int32_t epi_warps;
+    // Single-CTA tiled kernel, abort-path testing only: 0 off; k >= 1 leaves
+    // the stage of K block k - 1 of CTA 0's first tile unarmed (no
+    // expect_tx, no copies), so the MMA issuer's bounded wait on it expires.
+    int32_t withhold_kb;
 };
 
 // Skinny kernel: C^T = B^T . A^T, NB x 64 output columns of C per work

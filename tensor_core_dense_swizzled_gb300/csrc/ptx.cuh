@@ -408,14 +408,15 @@ __device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t adesc, ui
         : "memory");
 }
 
-// Arrives once on the mbarrier at the same shared-memory offset in every CTA
-// of `cta_mask` when all pair MMAs issued so far by this thread are complete.
-__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
+// Arrives once on the mbarrier at `cluster_bar` (a shared::cluster address
+// from mapa_shared: this CTA's or its peer's) when all pair MMAs issued so far
+// by this thread are complete.  A stage or accumulator that both CTAs of the
+// pair wait on gets two of these, one per CTA: plain point-to-point
+// completion signals, no multicast form.
+__device__ __forceinline__ void umma_commit_pair_to(uint32_t cluster_bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     cluster_bar)
+                 : "memory");
 }
 
 // ---------------------------------------------------------------- TMEM stores, exp2

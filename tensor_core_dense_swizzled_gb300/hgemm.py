@@ -66,6 +66,7 @@ class Options(ctypes.Structure):
         ("group_m", ctypes.c_int),
         ("trans_b", ctypes.c_int),
         ("tiled_epi_warps", ctypes.c_int),
+        ("debug_withhold_kb", ctypes.c_int),
     ]
 
 

@@ -876,6 +876,48 @@ def test_watchdog_selftest(dev):
     check(got, Cref, Den, "f32")
 
 
+@pytest.mark.parametrize("kb", [1, 2])
+def test_tiled_kernel_abort_path(dev, kb):
+    """A real GEMM pipeline whose wait cannot complete: the single-CTA tiled
+    kernel's producer leaves the stage of K block `kb` unarmed
+    (debug_withhold_kb), so the MMA issuer's wait on it runs out after 1 ms.
+    Every role then takes its teardown (the producer waits, bounded, for its
+    copies in flight; the MMA issuer for its MMAs; TMEM is freed), the run
+    reports HGEMM_ERR_TIMEOUT, the error word is cleared on read, and a normal
+    product on the same context right after is correct."""
+    M = N = K = 128
+    A = inputs.make_random((M * K,), "f16", 71, "normal")
+    B = inputs.make_random((K * N,), "f16", 72, "normal")
+    dA, dB = A.to(dev), B.to(dev)
+    dC = torch.zeros(M * N, dtype=torch.float32, device=dev)
+    opt = H.Options(cta_pair=2, timeout_ns=1_000_000, debug_withhold_kb=kb)
+    plan = H.hgemm_plan_create_ex(M, N, K, K, N, N, 1, 0, 0, 0, H.HGEMM_F16, H.HGEMM_F32, opt)
+    try:
+        info = H.hgemm_plan_get_info(plan)
+        assert info["path"] == H.HGEMM_PATH_TILED and info["tile_m"] == 128
+        for _ in range(2):  # the same plan times out again after the word was cleared
+            H.hgemm_run(plan, dA.data_ptr(), dB.data_ptr(), dC.data_ptr())
+            st = H.hgemm_check(plan)
+            assert st == 6, f"expected HGEMM_ERR_TIMEOUT, got {H.STATUS.get(st)}"
+            detail = H.hgemm_last_error_detail()
+            assert "timed out" in detail and ("MMA issuer" in detail or "epilogue" in detail), detail
+            assert H.hgemm_check(plan) == 0, "error word not cleared on read"
+    finally:
+        H.hgemm_plan_destroy(plan)
+    got, Cref, Den, _ = run_case(dev, M, N, K, "f16", "f32", seed=71,
+                                 options=H.Options(cta_pair=2))
+    check(got, Cref, Den, "f32")
+
+
+def test_withhold_option_refused_off_the_single_cta_kernel(dev):
+    for opt, shape in ((H.Options(cta_pair=1, debug_withhold_kb=1), (512, 512, 512)),
+                       (H.Options(force_path=H.HGEMM_PATH_SKINNY, debug_withhold_kb=1), (8, 256, 256)),
+                       (H.Options(cta_pair=2, debug_withhold_kb=3), (128, 128, 128))):
+        M, N, K = shape
+        with pytest.raises(H.HgemmError):
+            H.hgemm_plan_create_ex(M, N, K, K, N, N, 1, 0, 0, 0, H.HGEMM_F16, H.HGEMM_F32, opt)
+
+
 def test_plan_rejects_wrong_device_pointer_use(dev):
     plan = H.hgemm_plan_create(64, 64, 64, 64, 64, 64, 1, 0, 0, 0, H.HGEMM_F16, H.HGEMM_F32)
     try:
