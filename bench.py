@@ -85,7 +85,26 @@ def parse():
                          "form), or beta = 1 (reads C) + bias + ReLU")
     ap.add_argument("--probe-seconds", type=float, default=1.0,
                     help="untimed load after the timed region so the clock sampler sees the GPU busy")
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K: the workload's inputs (types, distributions, seed) at another "
+                         "size, for profiling captures; implies --no-per-config")
+    ap.add_argument("--plan-options", default="",
+                    help="comma-separated hgemm_options_t fields for the timed plans, e.g. "
+                         "cta_pair=2,force_generic_store=1 (recorded in config)")
     return ap.parse_args()
+
+
+def plan_options(args, w):
+    """hgemm_options_t of the timed plans: the workload's B layout plus
+    --plan-options."""
+    from tensor_core_dense_swizzled_gb300 import hgemm as H
+    kw = {"trans_b": int(w.trans_b)}
+    for item in filter(None, (x.strip() for x in args.plan_options.split(","))):
+        k, _, v = item.partition("=")
+        if k not in dict(H.Options._fields_):
+            raise SystemExit(f"--plan-options: unknown field {k}")
+        kw[k] = int(v)
+    return H.Options(**kw)
 
 
 def load_peaks():
@@ -572,7 +591,7 @@ def run_ours(args, w, world, rank, local, pg):
         sets.append((A.to(dev), B.to(dev), torch.empty(shape_c, dtype=TD[w.dtype_out], device=dev)))
         plans.append(H.hgemm_plan_create_ex(w.M, w.N, w.K, w.lda, w.ldb, w.ldc, w.batch, w.strideA,
                                             w.strideB, w.strideC, DT[w.dtype_in], DT[w.dtype_out],
-                                            H.Options(trans_b=int(w.trans_b))))
+                                            plan_options(args, w)))
     info = H.hgemm_plan_get_info(plans[0])
     stream = torch.cuda.current_stream(dev)
 
@@ -721,7 +740,8 @@ def run_ours(args, w, world, rank, local, pg):
             "path": {2: "tiled", 3: "skinny", 1: "zero_fill", 0: "empty"}[info["path"]],
             "kernel": kernel_label(info),
             "tile": [info["tile_m"], info["tile_n"], info["tile_k"]], "stages": info["stages"],
-            "split_k": info["split_k"], "grid": info["grid"], "epilogue": args.epilogue}),
+            "split_k": info["split_k"], "grid": info["grid"], "epilogue": args.epilogue,
+            **({"plan_options": args.plan_options} if args.plan_options else {})}),
         "pct_nominal_tensor_peak": 100.0 * value / world / (NOMINAL_TC_TFLOPS * tensor_ratio(w)),
         "pct_nominal_hbm": 100.0 * (min_bytes * args.steps / (region_ms * 1e-3) / 1e9) / NOMINAL_HBM_GBS,
         "stated_target": stated_target(w, value / world,
@@ -988,6 +1008,11 @@ def main():
         raise SystemExit(f"unknown workload {args.workload}; choose from "
                          f"{sorted(inputs.WORKLOADS) + sorted(inputs.ATTENTION_WORKLOADS)}")
     w = inputs.WORKLOADS[args.workload]
+    if args.shape:
+        import dataclasses
+        M, N, K = (int(x) for x in args.shape.split(","))
+        w = dataclasses.replace(w, name=f"{w.name}@{M}x{N}x{K}", M=M, N=N, K=K)
+        args.no_per_config = True
     world, rank, local, pg = dist_setup(args)
     try:
         if args.impl == "reference":

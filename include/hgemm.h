@@ -107,7 +107,8 @@ typedef struct {
     int skinny_prefetch;      /* skinny path: stages of B each CTA asks L2 for before it waits on
                                  the previous kernel of the stream; 0 or -1 none */
     int group_m;              /* tiled path: m-tiles per raster group (tiles run m-fastest within a
-                                 group of group_m tile rows); 0 automatic (16) */
+                                 group of group_m tile rows); 0 automatic (16; 8 for CTA-pair
+                                 tiles when M spans at least 32 of them) */
     int trans_b;              /* 0: B is K x N row-major (element (k, j) at B + k*ldb + j); 1: B is
                                  stored N x K row-major (element (k, j) at B + j*ldb + k, ldb >= K),
                                  i.e. C = A . B_stored^T -- a linear layer's weight, or attention's

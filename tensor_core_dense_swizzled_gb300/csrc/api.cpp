@@ -28,6 +28,7 @@ namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr int64_t kMaxDim = (1ll << 31) - 1;
+constexpr int kMaxHostChunks = 4;  // row chunks of the hgemm_run_host pipeline
 
 thread_local std::string g_detail;
 
@@ -166,6 +167,15 @@ struct hgemm_plan_s {
     // host-buffer (end-to-end) staging
     char *dA = nullptr, *dB = nullptr, *dC = nullptr;
     size_t dA_bytes = 0, dB_bytes = 0, dC_bytes = 0;
+    // hgemm_run_host pipeline (see host_pipeline): row chunks of A and C run
+    // as plans of their own on the caller's stream while the next chunk's
+    // rows of A arrive on s_in and finished rows of C leave on s_out
+    hgemm_plan_s *sub[2] = {nullptr, nullptr};  // full chunks, shorter last chunk
+    int64_t chunk_rows = 0;
+    int nchunks = 0;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_a[kMaxHostChunks] = {}, ev_c[kMaxHostChunks] = {};
     // tensor-map cache
     const void *mA = nullptr, *mB = nullptr;
     void *mC = nullptr;
@@ -795,7 +805,12 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.num_n = static_cast<int32_t>(ceil_div(p->N, p->bn));
         tp.num_kb = static_cast<int32_t>(ceil_div(p->K, kblock(p->din)));
         tp.tiles = tp.batch * tp.num_m * tp.num_n;
-        tp.group_m = p->opt.group_m ? p->opt.group_m : 16;
+        // Raster groups: 16 m-tiles, or 8 for pair tiles when there are at
+        // least 32 m-tiles.  On GB300 at 8192^3 (32 m-tiles) groups of 8 read
+        // 0.94 GB from DRAM per launch against 1.15 GB with 16 (2.09 GB with
+        // 32), in the same time; at 4096^3 (16 m-tiles) 8 read 86 MB against
+        // 71 MB, also in the same time.
+        tp.group_m = p->opt.group_m ? p->opt.group_m : (p->pair && tp.num_m >= 32 ? 8 : 16);
         // B MN-major (stored K x N, N contiguous) or K-major (trans_b: N x K)
         tp.idesc = f8 ? hg::idesc_f8(f8fmt, f8fmt, 0, 0, p->pair ? 256 : 128, static_cast<uint32_t>(p->bn))
                       : hg::idesc_f16(bf, 0, p->opt.trans_b ? 0 : 1, p->pair ? 256 : 128,
@@ -930,6 +945,153 @@ hgemm_status_t hgemm_run_ex(hgemm_plan_t plan, const void *A, const void *B, voi
     return plan_run(plan, A, B, C, static_cast<cudaStream_t>(stream), ep);
 }
 
+}  // extern "C"
+
+namespace {
+
+// hgemm_run_host in row chunks: worth it for one large product (batch 1, M
+// >= 1024, A and C together >= 16 MB), where the host link, not the kernel,
+// sets the time.  M is cut into at most kMaxHostChunks chunks of a multiple
+// of 256 rows (so every chunk starts 16-byte aligned whenever the rows are).
+bool host_chunking(const hgemm_plan_s *p, int64_t &rows, int &n) {
+    if (p->path != HGEMM_PATH_TILED || p->batch != 1 || p->M < 1024 || p->opt.debug_withhold_kb)
+        return false;
+    const double bytes = static_cast<double>(p->M) * p->K * in_bytes(p->din) +
+                         static_cast<double>(p->M) * p->N * out_bytes(p->dout);
+    if (bytes < 16e6) return false;
+    rows = round_up(ceil_div(p->M, kMaxHostChunks), 256);
+    n = static_cast<int>(ceil_div(p->M, rows));
+    return n >= 2;
+}
+
+// Copies rows [r0, r0 + rows) of C (batch 1) from the device staging buffer
+// to the host on stream s; only the N columns of each row.
+cudaError_t copy_c_rows(hgemm_plan_s *p, void *C_host, int64_t r0, int64_t rows, cudaStream_t s) {
+    const int ob = out_bytes(p->dout);
+    const size_t off = static_cast<size_t>(r0 * p->ldc) * ob;
+    if (p->ldc == p->N)
+        return cudaMemcpyAsync(static_cast<char *>(C_host) + off, p->dC + off,
+                               static_cast<size_t>(rows * p->N) * ob, cudaMemcpyDeviceToHost, s);
+    return cudaMemcpy2DAsync(static_cast<char *>(C_host) + off, static_cast<size_t>(p->ldc) * ob,
+                             p->dC + off, static_cast<size_t>(p->ldc) * ob,
+                             static_cast<size_t>(p->N) * ob, static_cast<size_t>(rows),
+                             cudaMemcpyDeviceToHost, s);
+}
+
+// The chunked hgemm_run_host.  Three streams: s_in copies B, then the rows of
+// A chunk by chunk; the caller's stream runs chunk i's product (a plan of its
+// own over rows [r0, r0 + rows) of the staging buffers) once its rows of A
+// have arrived; s_out copies chunk i's rows of C back once its product is
+// done.  So the copies in, the products and the copies out of different
+// chunks overlap (host-to-device and device-to-host use the link's two
+// directions).  Everything is ordered after the caller's earlier work on
+// `s` (ev_start) and before its later work (ev_done).
+hgemm_status_t host_pipeline(hgemm_plan_s *p, const void *A_host, const void *B_host, void *C_host,
+                             cudaStream_t s, size_t b_bytes) {
+    const int ib = in_bytes(p->din);
+    cudaError_t e = cudaSuccess;
+    if (!p->s_in) {
+        if ((e = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&p->ev_start, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&p->ev_done, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "host pipeline streams");
+        for (int i = 0; i < kMaxHostChunks; ++i)
+            if ((e = cudaEventCreateWithFlags(&p->ev_a[i], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&p->ev_c[i], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e, "host pipeline events");
+    }
+    for (int k = 0; k < 2; ++k) {  // the chunks' plans, made on first use
+        const int64_t rows = k == 0 ? p->chunk_rows : p->M - (p->nchunks - 1) * p->chunk_rows;
+        if (p->sub[k] || (k == 1 && rows == p->chunk_rows)) continue;
+        hgemm_status_t st = plan_create(&p->sub[k], rows, p->N, p->K, p->lda, p->ldb, p->ldc, 1, 0, 0,
+                                        0, p->din, p->dout, &p->opt);
+        if (st != HGEMM_OK) return st;
+    }
+    auto drain = [&] {  // on a failure after work was enqueued: let it finish
+        cudaStreamSynchronize(p->s_in);
+        cudaStreamSynchronize(p->s_out);
+        cudaStreamSynchronize(s);
+    };
+    if ((e = cudaEventRecord(p->ev_start, s)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(p->s_in, p->ev_start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(p->s_out, p->ev_start, 0)) != cudaSuccess)
+        return cuda_fail(e, "host pipeline ordering");
+    if ((e = cudaMemcpyAsync(p->dB, B_host, b_bytes, cudaMemcpyHostToDevice, p->s_in)) != cudaSuccess) {
+        drain();
+        return cuda_fail(e, "copy B to device");
+    }
+    for (int i = 0; i < p->nchunks; ++i) {
+        const int64_t r0 = i * p->chunk_rows;
+        const int64_t rows = p->M - r0 < p->chunk_rows ? p->M - r0 : p->chunk_rows;
+        const size_t off = static_cast<size_t>(r0 * p->lda) * ib;
+        const size_t len = static_cast<size_t>(span_elems(rows, p->K, p->lda, 1, 0)) * ib;
+        if ((e = cudaMemcpyAsync(p->dA + off, static_cast<const char *>(A_host) + off, len,
+                                 cudaMemcpyHostToDevice, p->s_in)) != cudaSuccess ||
+            (e = cudaEventRecord(p->ev_a[i], p->s_in)) != cudaSuccess) {
+            drain();
+            return cuda_fail(e, "copy A to device");
+        }
+    }
+    const int ob = out_bytes(p->dout);
+    for (int i = 0; i < p->nchunks; ++i) {
+        const int64_t r0 = i * p->chunk_rows;
+        const int64_t rows = p->M - r0 < p->chunk_rows ? p->M - r0 : p->chunk_rows;
+        hgemm_plan_s *sub = rows == p->chunk_rows ? p->sub[0] : p->sub[1];
+        if ((e = cudaStreamWaitEvent(s, p->ev_a[i], 0)) != cudaSuccess) {
+            drain();
+            return cuda_fail(e, "host pipeline ordering");
+        }
+        hgemm_status_t st = plan_run(sub, p->dA + static_cast<size_t>(r0 * p->lda) * ib, p->dB,
+                                     p->dC + static_cast<size_t>(r0 * p->ldc) * ob, s);
+        if (st != HGEMM_OK) {
+            drain();
+            return st;
+        }
+        if ((e = cudaEventRecord(p->ev_c[i], s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(p->s_out, p->ev_c[i], 0)) != cudaSuccess ||
+            (e = copy_c_rows(p, C_host, r0, rows, p->s_out)) != cudaSuccess) {
+            drain();
+            return cuda_fail(e, "copy C to host");
+        }
+    }
+    if ((e = cudaEventRecord(p->ev_done, p->s_out)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, p->ev_done, 0)) != cudaSuccess) {
+        drain();
+        return cuda_fail(e, "host pipeline ordering");
+    }
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    // the products ran: a watchdog timeout left C incomplete
+    for (hgemm_plan_s *sub : p->sub) {
+        if (!sub) continue;
+        hgemm_status_t st = read_error_word(sub);
+        if (st != HGEMM_OK) return st;
+    }
+    return HGEMM_OK;
+}
+
+void free_plan(hgemm_plan_s *plan) {
+    if (plan->ws) cudaFree(plan->ws);
+    if (plan->dA) cudaFree(plan->dA);
+    if (plan->dB) cudaFree(plan->dB);
+    if (plan->dC) cudaFree(plan->dC);
+    for (hgemm_plan_s *sub : plan->sub)
+        if (sub) free_plan(sub);
+    if (plan->s_in) cudaStreamDestroy(plan->s_in);
+    if (plan->s_out) cudaStreamDestroy(plan->s_out);
+    if (plan->ev_start) cudaEventDestroy(plan->ev_start);
+    if (plan->ev_done) cudaEventDestroy(plan->ev_done);
+    for (int i = 0; i < kMaxHostChunks; ++i) {
+        if (plan->ev_a[i]) cudaEventDestroy(plan->ev_a[i]);
+        if (plan->ev_c[i]) cudaEventDestroy(plan->ev_c[i]);
+    }
+    delete plan;
+}
+
+}  // namespace
+
+extern "C" {
+
 hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void *B_host, void *C_host,
                               void *stream) {
     if (!plan) return fail(HGEMM_ERR_INVALID_ARG, "plan is NULL");
@@ -958,6 +1120,8 @@ hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void 
     if ((e = grow(&p->dA, &p->dA_bytes, a_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(A staging)");
     if ((e = grow(&p->dB, &p->dB_bytes, b_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(B staging)");
     if ((e = grow(&p->dC, &p->dC_bytes, c_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(C staging)");
+    if (host_chunking(p, p->chunk_rows, p->nchunks))
+        return host_pipeline(p, A_host, B_host, C_host, s, b_bytes);
     if (p->path != HGEMM_PATH_ZERO_FILL) {
         if ((e = cudaMemcpyAsync(p->dA, A_host, a_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
             return cuda_fail(e, "copy A to device");
@@ -1002,11 +1166,7 @@ hgemm_status_t hgemm_check(hgemm_plan_t plan, void *stream) {
 
 hgemm_status_t hgemm_plan_destroy(hgemm_plan_t plan) {
     if (!plan) return HGEMM_OK;
-    if (plan->ws) cudaFree(plan->ws);
-    if (plan->dA) cudaFree(plan->dA);
-    if (plan->dB) cudaFree(plan->dB);
-    if (plan->dC) cudaFree(plan->dC);
-    delete plan;
+    free_plan(plan);
     return HGEMM_OK;
 }
 

@@ -492,6 +492,67 @@ def test_operand_copy_every_misalignment(dev, off):
         check(got, Cref, Den, "f32")
 
 
+PAIR_COPY_CASES = [
+    # M, N, K, kwargs: copies of A only, B only, both, B stored N x K, batches
+    # with misaligned strides, K of one, several and a partial 1024-element
+    # copy segment
+    (300, 520, 600, dict(lda=600, ldb=521, ldc=520)),
+    (513, 700, 2500, dict(lda=2500, ldb=700, ldc=701)),
+    (1000, 1100, 4095, dict(lda=4095, ldb=1100, ldc=1100)),
+    (600, 640, 1500, dict(off_a=1)),
+    (600, 640, 1500, dict(off_b=5)),
+    (260, 300, 2100, dict(lda=2101, ldb=2101, trans_b=True)),
+    (270, 260, 1100, dict(batch=2, sA=270 * 1100 + 3, sB=1100 * 260 + 1, sC=270 * 260)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PAIR_COPY_CASES)))
+@pytest.mark.parametrize("dout", ["f32", "f16"])
+def test_cta_pair_on_copied_operands(dev, case, dout):
+    """CTA pairs reading operands from their aligned copies (misaligned leading
+    dimension, base pointer or batch stride): the result matches the oracle
+    and three runs in a row agree bit for bit."""
+    M, N, K, kw = PAIR_COPY_CASES[case]
+    kw = dict(kw)
+    tb = kw.pop("trans_b", False)
+    opt = H.Options(cta_pair=1, trans_b=1 if tb else 0)
+    if tb:
+        got, Cref, Den, info = run_case_bt(dev, M, N, K, dout, opt, seed=300 + case, **kw)
+    else:
+        got, Cref, Den, info = run_case(dev, M, N, K, "f16", dout, seed=300 + case, options=opt,
+                                        runs=3, **kw)
+    assert info["tile_m"] == 256
+    assert info["repack_a"] or info["repack_b"] or "off_a" in kw or "off_b" in kw
+    check(got, Cref, Den, dout)
+
+
+def run_case_bt(dev, M, N, K, dout, opt, *, lda, ldb, seed):
+    """C = A . B_stored^T with B stored N x K (ldb >= K), through run_case's
+    machinery: the oracle gets B transposed into K x N."""
+    A = inputs.make_random((M * lda,), "f16", seed, "normal")
+    Bs = inputs.make_random((N * ldb,), "f16", seed + 1, "normal")
+    dA, dB = A.to(dev), Bs.to(dev)
+    dC = torch.full((M * N + 64,), SENTINEL[dout], dtype=TORCH[dout], device=dev)
+    plan = H.hgemm_plan_create_ex(M, N, K, lda, ldb, N, 1, 0, 0, 0, H.HGEMM_F16, DT[dout], opt)
+    try:
+        info = H.hgemm_plan_get_info(plan)
+        res = []
+        for _ in range(3):
+            H.hgemm_run(plan, dA.data_ptr(), dB.data_ptr(), dC.data_ptr())
+            assert H.hgemm_check(plan) == 0, H.hgemm_last_error_detail()
+            res.append(dC.clone())
+    finally:
+        H.hgemm_plan_destroy(plan)
+    for r in res[1:]:
+        assert torch.equal(r, res[0]), "repeated runs differ"
+    assert torch.all(dC[M * N:].cpu() == SENTINEL[dout])
+    Bkn = torch.as_strided(Bs, (N, K), (ldb, 1)).t().contiguous().reshape(-1)
+    Cref, Den = oracle.gemm(bits(torch.as_strided(A, (M, K), (lda, 1)).contiguous().reshape(-1)),
+                            bits(Bkn), 0, M, N, K, K, N, 1, 0, 0)
+    got = read_c(dC[:M * N], dout, M, N, N, 1, 0, 0)
+    return got, Cref, Den, info
+
+
 @pytest.mark.parametrize("opt", [H.Options(force_repack=1), H.Options(force_generic_store=1),
                                  H.Options(force_repack=1, force_generic_store=1)])
 def test_forced_fallbacks_match(dev, opt):
@@ -841,6 +902,37 @@ def test_run_host_end_to_end(dev):
     assert torch.all(C[:, N:] == -7.0)
     Cref, Den = oracle.gemm(bits(A), bits(B), 0, M, N, K, K, N)
     check(C[:, :N].double().numpy()[None], Cref, Den, "f32")
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldc,din,dout", [
+    (2348, 1100, 4096, 4096, 1100, "bf16", "bf16"),  # chunks of 768 rows, the last of 44
+    (1500, 1000, 4000, 4000, 1008, "f16", "f32"),    # chunks of 512, the last of 476; padded C rows
+    (2000, 1300, 4095, 4095, 1301, "f16", "f16"),    # misaligned rows of A and C
+])
+def test_run_host_row_chunks(dev, M, N, K, lda, ldc, din, dout):
+    """Large products through hgemm_run_host run in row chunks whose copies in,
+    products and copies out overlap on three streams; every element of C is
+    right, host elements outside the M x N block stay intact, and the plan
+    gives the same C on a second call."""
+    A = inputs.make_random((M * lda,), din, 62).pin_memory()
+    B = inputs.make_random((K * N,), din, 63).pin_memory()
+    C = torch.full((M * ldc,), -7.0, dtype=TORCH[dout]).pin_memory()
+    plan = H.hgemm_plan_create(M, N, K, lda, N, ldc, 1, 0, 0, 0, DT[din], DT[dout])
+    try:
+        H.hgemm_run_host(plan, A, B, C)
+        first = C.clone()
+        H.hgemm_run_host(plan, A, B, C)
+    finally:
+        H.hgemm_plan_destroy(plan)
+    assert torch.equal(C, first), "repeated calls differ"
+    view = torch.as_strided(C, (M, N), (ldc, 1))
+    mask = torch.ones(M * ldc, dtype=torch.bool)
+    torch.as_strided(mask, (M, N), (ldc, 1)).fill_(False)
+    assert torch.all(C[mask] == -7.0), "host elements outside C changed"
+    Cref, Den = oracle.gemm(bits(A), bits(B), ORACLE_DT[din], M, N, K, lda, N)
+    got = view.double().numpy()[None] if dout == "f32" else \
+        oracle.decode(bits(view), ORACLE_DT[dout]).reshape(1, M, N)
+    check(got, Cref, Den, dout)
 
 
 @pytest.mark.parametrize("ldc,gap", [(96, 0), (104, 0), (96, 500)])
