@@ -152,6 +152,8 @@ typedef struct {
     int epi_warps;        /* tiled path: warps draining the accumulators in plain runs (4 or 8;
                              CTA pairs 4), else 0 */
     int epi_warps_epilogue; /* the same for runs with the fused epilogue (hgemm_run_ex) */
+    int host_chunks;      /* hgemm_run_host: row chunks whose copies in, products and copies out
+                             overlap (batch 1, M >= 1024, A and C >= 16 MB together), or 1 */
 } hgemm_plan_info_t;
 
 /* Creates a plan for C_b = A_b . B_b, b < batch.
@@ -238,6 +240,13 @@ hgemm_status_t hgemm_run_ex(hgemm_plan_t plan, const void *A, const void *B, voi
  * copies A and B to plan-owned device buffers on `stream`, runs the product,
  * copies the M x N block(s) of C back into the host buffer (elements outside
  * the block are left untouched), and synchronises `stream` before returning.
+ * A large product (plan info host_chunks > 1) runs in row chunks: B and then
+ * the rows of A chunk by chunk are copied in on a second stream, each chunk's
+ * product runs on `stream` as soon as its rows have arrived, and its rows of
+ * C are copied out on a third stream as soon as it is done, so copies in,
+ * products and copies out overlap.  The streams and the chunks' plans are
+ * made on the first such call and kept by the plan; all the work is ordered
+ * after what was queued on `stream` before the call.
  * It then reads the plan's device error word as hgemm_check does: after a
  * watchdog timeout it returns HGEMM_ERR_TIMEOUT (C_host is then incomplete)
  * and clears the word.  The device buffers are allocated on the first call

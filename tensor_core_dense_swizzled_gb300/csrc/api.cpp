@@ -1197,6 +1197,9 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     r.kernels_per_run = plan->path == HGEMM_PATH_EMPTY ? 0 : 1 + ((r.repack_a || r.repack_b) ? 1 : 0);
     if (plan->path == HGEMM_PATH_ZERO_FILL) r.kernels_per_run = 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
+    int64_t chunk_rows = 0;
+    int nchunks = 1;
+    r.host_chunks = host_chunking(plan, chunk_rows, nchunks) ? nchunks : 1;
     r.tail_split = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->tail_split : 1;
     r.trans_b = plan->opt.trans_b;
     r.stream_k = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->stream_k

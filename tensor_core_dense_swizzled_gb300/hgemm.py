@@ -106,6 +106,7 @@ class PlanInfo(ctypes.Structure):
         ("stream_k", ctypes.c_int),
         ("epi_warps", ctypes.c_int),
         ("epi_warps_epilogue", ctypes.c_int),
+        ("host_chunks", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
