@@ -966,7 +966,9 @@ def run_attention_ours(args, w, world, rank, local, pg):
         dt = max_over_ranks(pg, dt, dev)
         e2e = {"value": flops * args.e2e_steps * world / dt / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": (Q.numel() + K.numel() + V.numel()) * 2,
-               "d2h_bytes_per_step": Q.numel() * 2, "steps": args.e2e_steps}
+               "d2h_bytes_per_step": Q.numel() * 2, "steps": args.e2e_steps,
+               "ms_per_step": dt / args.e2e_steps * 1e3,
+               "copies": "serialised with the kernel on one stream"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = attn_cpu_baseline(w)

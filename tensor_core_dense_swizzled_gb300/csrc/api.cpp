@@ -170,8 +170,9 @@ struct hgemm_plan_s {
     // hgemm_run_host pipeline (see host_pipeline): row chunks of A and C run
     // as plans of their own on the caller's stream while the next chunk's
     // rows of A arrive on s_in and finished rows of C leave on s_out
-    hgemm_plan_s *sub[2] = {nullptr, nullptr};  // full chunks, shorter last chunk
-    int64_t chunk_rows = 0;
+    hgemm_plan_s *sub[kMaxHostChunks] = {};  // chunk i's plan (chunks of equal rows share one)
+    bool sub_own[kMaxHostChunks] = {};       // sub[i] is owned (first chunk of its size)
+    int64_t chunk_r0[kMaxHostChunks + 1] = {};  // chunk i: rows [chunk_r0[i], chunk_r0[i + 1])
     int nchunks = 0;
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t ev_start = nullptr, ev_done = nullptr;
@@ -951,16 +952,22 @@ namespace {
 
 // hgemm_run_host in row chunks: worth it for one large product (batch 1, M
 // >= 1024, A and C together >= 16 MB), where the host link, not the kernel,
-// sets the time.  M is cut into at most kMaxHostChunks chunks of a multiple
-// of 256 rows (so every chunk starts 16-byte aligned whenever the rows are).
-bool host_chunking(const hgemm_plan_s *p, int64_t &rows, int &n) {
+// sets the time.  M is cut into up to four chunks of a multiple of 256 rows
+// (so every chunk starts 16-byte aligned whenever the rows are).  r0[i] is the
+// first row of chunk i, r0[n] = M.  (Splitting the last 256 rows off as a
+// fifth chunk, to shorten what is left after the last rows of A arrive,
+// measured slower on GB300: 4096^3 0.486 against 0.471 ms per call -- a
+// 256-row product takes nearly as long as a whole wave.)
+bool host_chunking(const hgemm_plan_s *p, int64_t *r0, int &n) {
     if (p->path != HGEMM_PATH_TILED || p->batch != 1 || p->M < 1024 || p->opt.debug_withhold_kb)
         return false;
     const double bytes = static_cast<double>(p->M) * p->K * in_bytes(p->din) +
                          static_cast<double>(p->M) * p->N * out_bytes(p->dout);
     if (bytes < 16e6) return false;
-    rows = round_up(ceil_div(p->M, kMaxHostChunks), 256);
-    n = static_cast<int>(ceil_div(p->M, rows));
+    const int64_t rows = round_up(ceil_div(p->M, 4), 256);
+    n = 0;
+    for (int64_t r = 0; r < p->M; r += rows) r0[n++] = r;
+    r0[n] = p->M;
     return n >= 2;
 }
 
@@ -1001,12 +1008,16 @@ hgemm_status_t host_pipeline(hgemm_plan_s *p, const void *A_host, const void *B_
                 (e = cudaEventCreateWithFlags(&p->ev_c[i], cudaEventDisableTiming)) != cudaSuccess)
                 return cuda_fail(e, "host pipeline events");
     }
-    for (int k = 0; k < 2; ++k) {  // the chunks' plans, made on first use
-        const int64_t rows = k == 0 ? p->chunk_rows : p->M - (p->nchunks - 1) * p->chunk_rows;
-        if (p->sub[k] || (k == 1 && rows == p->chunk_rows)) continue;
-        hgemm_status_t st = plan_create(&p->sub[k], rows, p->N, p->K, p->lda, p->ldb, p->ldc, 1, 0, 0,
+    for (int i = 0; i < p->nchunks; ++i) {  // the chunks' plans, made on first use
+        if (p->sub[i]) continue;
+        const int64_t rows = p->chunk_r0[i + 1] - p->chunk_r0[i];
+        for (int j = 0; j < i; ++j)
+            if (p->chunk_r0[j + 1] - p->chunk_r0[j] == rows) p->sub[i] = p->sub[j];
+        if (p->sub[i]) continue;
+        hgemm_status_t st = plan_create(&p->sub[i], rows, p->N, p->K, p->lda, p->ldb, p->ldc, 1, 0, 0,
                                         0, p->din, p->dout, &p->opt);
         if (st != HGEMM_OK) return st;
+        p->sub_own[i] = true;
     }
     auto drain = [&] {  // on a failure after work was enqueued: let it finish
         cudaStreamSynchronize(p->s_in);
@@ -1022,8 +1033,8 @@ hgemm_status_t host_pipeline(hgemm_plan_s *p, const void *A_host, const void *B_
         return cuda_fail(e, "copy B to device");
     }
     for (int i = 0; i < p->nchunks; ++i) {
-        const int64_t r0 = i * p->chunk_rows;
-        const int64_t rows = p->M - r0 < p->chunk_rows ? p->M - r0 : p->chunk_rows;
+        const int64_t r0 = p->chunk_r0[i];
+        const int64_t rows = p->chunk_r0[i + 1] - r0;
         const size_t off = static_cast<size_t>(r0 * p->lda) * ib;
         const size_t len = static_cast<size_t>(span_elems(rows, p->K, p->lda, 1, 0)) * ib;
         if ((e = cudaMemcpyAsync(p->dA + off, static_cast<const char *>(A_host) + off, len,
@@ -1035,9 +1046,9 @@ hgemm_status_t host_pipeline(hgemm_plan_s *p, const void *A_host, const void *B_
     }
     const int ob = out_bytes(p->dout);
     for (int i = 0; i < p->nchunks; ++i) {
-        const int64_t r0 = i * p->chunk_rows;
-        const int64_t rows = p->M - r0 < p->chunk_rows ? p->M - r0 : p->chunk_rows;
-        hgemm_plan_s *sub = rows == p->chunk_rows ? p->sub[0] : p->sub[1];
+        const int64_t r0 = p->chunk_r0[i];
+        const int64_t rows = p->chunk_r0[i + 1] - r0;
+        hgemm_plan_s *sub = p->sub[i];
         if ((e = cudaStreamWaitEvent(s, p->ev_a[i], 0)) != cudaSuccess) {
             drain();
             return cuda_fail(e, "host pipeline ordering");
@@ -1062,9 +1073,9 @@ hgemm_status_t host_pipeline(hgemm_plan_s *p, const void *A_host, const void *B_
     }
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     // the products ran: a watchdog timeout left C incomplete
-    for (hgemm_plan_s *sub : p->sub) {
-        if (!sub) continue;
-        hgemm_status_t st = read_error_word(sub);
+    for (int i = 0; i < p->nchunks; ++i) {
+        if (!p->sub_own[i]) continue;
+        hgemm_status_t st = read_error_word(p->sub[i]);
         if (st != HGEMM_OK) return st;
     }
     return HGEMM_OK;
@@ -1075,8 +1086,8 @@ void free_plan(hgemm_plan_s *plan) {
     if (plan->dA) cudaFree(plan->dA);
     if (plan->dB) cudaFree(plan->dB);
     if (plan->dC) cudaFree(plan->dC);
-    for (hgemm_plan_s *sub : plan->sub)
-        if (sub) free_plan(sub);
+    for (int i = 0; i < kMaxHostChunks; ++i)
+        if (plan->sub_own[i]) free_plan(plan->sub[i]);
     if (plan->s_in) cudaStreamDestroy(plan->s_in);
     if (plan->s_out) cudaStreamDestroy(plan->s_out);
     if (plan->ev_start) cudaEventDestroy(plan->ev_start);
@@ -1120,7 +1131,7 @@ hgemm_status_t hgemm_run_host(hgemm_plan_t plan, const void *A_host, const void 
     if ((e = grow(&p->dA, &p->dA_bytes, a_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(A staging)");
     if ((e = grow(&p->dB, &p->dB_bytes, b_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(B staging)");
     if ((e = grow(&p->dC, &p->dC_bytes, c_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(C staging)");
-    if (host_chunking(p, p->chunk_rows, p->nchunks))
+    if (host_chunking(p, p->chunk_r0, p->nchunks))
         return host_pipeline(p, A_host, B_host, C_host, s, b_bytes);
     if (p->path != HGEMM_PATH_ZERO_FILL) {
         if ((e = cudaMemcpyAsync(p->dA, A_host, a_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
@@ -1197,9 +1208,9 @@ hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info) {
     r.kernels_per_run = plan->path == HGEMM_PATH_EMPTY ? 0 : 1 + ((r.repack_a || r.repack_b) ? 1 : 0);
     if (plan->path == HGEMM_PATH_ZERO_FILL) r.kernels_per_run = 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
-    int64_t chunk_rows = 0;
+    int64_t r0[kMaxHostChunks + 1];
     int nchunks = 1;
-    r.host_chunks = host_chunking(plan, chunk_rows, nchunks) ? nchunks : 1;
+    r.host_chunks = host_chunking(plan, r0, nchunks) ? nchunks : 1;
     r.tail_split = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->tail_split : 1;
     r.trans_b = plan->opt.trans_b;
     r.stream_k = plan->path == HGEMM_PATH_TILED && plan->pair ? plan->stream_k

@@ -186,6 +186,30 @@ def test_attention_host_buffers(dev):
     check(O, q, k, v, bh, sq, skv, 0.09, True, "f16")
 
 
+@pytest.mark.parametrize("bh,causal", [(24, False), (25, True)])
+def test_attention_host_buffers_many_heads(dev, bh, causal):
+    """hgemm_attention_run_host on 24 and 25 heads of 1024 x 1024: the last
+    query row of every head and random rows match the oracle, and a second
+    call gives the same O."""
+    sq = skv = 1024
+    q, k, v = draw((bh, sq, D), 21, "bf16"), draw((bh, skv, D), 22, "bf16"), draw((bh, skv, D), 23, "bf16")
+    O = torch.empty(bh * sq * D, dtype=torch.bfloat16).pin_memory()
+    plan = H.hgemm_attention_plan_create(bh, sq, skv, D, 0.0884, int(causal), DT["bf16"])
+    try:
+        qp, kp, vp = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        H.hgemm_attention_run_host(plan, qp, kp, vp, O)
+        first = O.clone()
+        H.hgemm_attention_run_host(plan, qp, kp, vp, O)
+        assert H.hgemm_attention_check(plan) == 0
+    finally:
+        H.hgemm_attention_plan_destroy(plan)
+    assert torch.equal(O, first), "repeated calls differ"
+    g = np.random.default_rng(9)
+    rb = np.concatenate([np.arange(bh), g.integers(0, bh, 64)])
+    ri = np.concatenate([np.full(bh, sq - 1), g.integers(0, sq, 64)])
+    check(O, q, k, v, bh, sq, skv, 0.0884, causal, "bf16", rows=(rb, ri))
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_attention_full_size_sampled(dev, causal):
     """The attention workload at full size (64 heads x 1024 x 1024, head 128,
