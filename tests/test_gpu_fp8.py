@@ -162,6 +162,25 @@ def test_fp8_host_buffers(dev):
     check(C.double().numpy().reshape(1, M, N), Cref, Den, "f32")
 
 
+def test_fp8_host_buffers_in_row_chunks(dev):
+    """A large 8-bit product through hgemm_run_host runs in row chunks (plan
+    info host_chunks > 1): chunk pointers stay 16-byte aligned, every element
+    of C is right."""
+    M, N, K = 2048, 1024, 8192
+    A = inputs.make_random((M * K,), "e4m3", 33)
+    Bs = inputs.make_random((N * K,), "e4m3", 34)
+    C = torch.empty(M * N, dtype=torch.bfloat16).pin_memory()
+    plan = H.hgemm_plan_create_ex(M, N, K, K, K, N, 1, 0, 0, 0, F8["e4m3"], DT["bf16"], H.Options(trans_b=1))
+    try:
+        assert H.hgemm_plan_get_info(plan)["host_chunks"] == 4
+        H.hgemm_run_host(plan, A.view(torch.uint8).pin_memory(), Bs.view(torch.uint8).pin_memory(), C)
+    finally:
+        H.hgemm_plan_destroy(plan)
+    Cref, Den = oracle.gemm_bt(bits8(A), bits8(Bs), oracle.E4M3, M, N, K, K, K)
+    got = read_c(C, "bf16", M, N, N, 1, 0, 0)
+    check(got, Cref, Den, "bf16")
+
+
 def test_fp8_misaligned_pointer_is_unsupported(dev):
     """No aligned copy is made for 8-bit operands: a base pointer off the
     16-byte grid is refused at run time, before any launch."""

@@ -908,6 +908,7 @@ def test_run_host_end_to_end(dev):
     (2348, 1100, 4096, 4096, 1100, "bf16", "bf16"),  # chunks of 768 rows, the last of 44
     (1500, 1000, 4000, 4000, 1008, "f16", "f32"),    # chunks of 512, the last of 476; padded C rows
     (2000, 1300, 4095, 4095, 1301, "f16", "f16"),    # misaligned rows of A and C
+    (1030, 4096, 4096, 4096, 4096, "bf16", "f32"),   # chunks of 512, 512 and 6 rows (skinny kernel)
 ])
 def test_run_host_row_chunks(dev, M, N, K, lda, ldc, din, dout):
     """Large products through hgemm_run_host run in row chunks whose copies in,
@@ -919,6 +920,7 @@ def test_run_host_row_chunks(dev, M, N, K, lda, ldc, din, dout):
     C = torch.full((M * ldc,), -7.0, dtype=TORCH[dout]).pin_memory()
     plan = H.hgemm_plan_create(M, N, K, lda, N, ldc, 1, 0, 0, 0, DT[din], DT[dout])
     try:
+        assert H.hgemm_plan_get_info(plan)["host_chunks"] > 1
         H.hgemm_run_host(plan, A, B, C)
         first = C.clone()
         H.hgemm_run_host(plan, A, B, C)
