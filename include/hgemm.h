@@ -105,7 +105,8 @@ typedef struct {
     int skinny_stream_k;      /* skinny path: 0 automatic (off), 1 off, 2 on: the (tile, K block)
                                  steps are dealt to the SMs in equal contiguous ranges */
     int skinny_prefetch;      /* skinny path: stages of B each CTA asks L2 for before it waits on
-                                 the previous kernel of the stream; 0 or -1 none */
+                                 the previous kernel of the stream; 0 automatic (4 for 8-bit
+                                 inputs, none for 16-bit), -1 none */
     int group_m;              /* tiled path: m-tiles per raster group (tiles run m-fastest within a
                                  group of group_m tile rows); 0 automatic (16; 8 for CTA-pair
                                  tiles when M spans at least 32 of them) */
