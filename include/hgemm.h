@@ -64,7 +64,9 @@ typedef enum {
     HGEMM_ERR_NO_DEVICE = 3,   /* no CUDA device, or not an sm_103 device */
     HGEMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (see detail) */
     HGEMM_ERR_OOM = 5,         /* device or host allocation failed */
-    HGEMM_ERR_TIMEOUT = 6      /* a device-side wait ran out of time (kernel aborted cleanly) */
+    HGEMM_ERR_TIMEOUT = 6,     /* a device-side wait ran out of time (kernel aborted cleanly) */
+    HGEMM_ERR_INTERNAL = 7     /* a device-side invariant check failed (debug_checks; the kernel
+                                  stopped before using the offending work item) */
 } hgemm_status_t;
 
 /* Execution paths a plan can take (hgemm_plan_info_t.path). */
@@ -126,6 +128,15 @@ typedef struct {
                                  hgemm_check returns HGEMM_ERR_TIMEOUT.  k <= ceil(K / 64); plans
                                  that take another kernel (CTA pairs, skinny, 8-bit inputs) get
                                  HGEMM_ERR_UNSUPPORTED */
+    int debug_checks;         /* 0: off unless the environment variable HGEMM_DEBUG is set to a
+                                 non-zero value; 1: the kernels check their own scheduling
+                                 invariants before every work item (tile coordinates inside the
+                                 output, K ranges inside K, piece indices inside their tile) and,
+                                 on a violation, record it in the device error word and stop
+                                 before touching memory with it: hgemm_check then returns
+                                 HGEMM_ERR_INTERNAL.  No trap, no assert.  2: testing the check
+                                 only -- the first work item of CTA 0 (or CTA pair 0) is given a
+                                 tile index past the last tile, which the check must catch */
 } hgemm_options_t;
 
 /* Read-only description of what a plan will launch. */

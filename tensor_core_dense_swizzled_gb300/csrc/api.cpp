@@ -14,6 +14,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -290,6 +291,36 @@ int choose_tile_n(int64_t batch, int64_t M, int64_t N, int sms, bool f8) {
     return best;
 }
 
+// Debugging overrides from the environment, read at every plan creation and
+// applied only where the caller's options leave the field at its default:
+//   HGEMM_DEBUG=1          debug_checks = 1 (kernel invariant checks)
+//   HGEMM_TIMEOUT_NS=<n>   the watchdog limit of every pipeline wait
+//   HGEMM_FORCE_CONFIG=    pair | single | single:<tile_n> | skinny: the kernel
+//                          (CTA pairs, single-CTA tiles, the skinny path)
+// An unrecognised value is ignored.
+void apply_env_overrides(hgemm_options_t &opt) {
+    if (const char *v = std::getenv("HGEMM_DEBUG"))
+        if (opt.debug_checks == 0 && std::atoi(v) != 0) opt.debug_checks = 1;
+    if (const char *v = std::getenv("HGEMM_TIMEOUT_NS")) {
+        const long long ns = std::atoll(v);
+        if (opt.timeout_ns == 0 && ns > 0) opt.timeout_ns = static_cast<uint64_t>(ns);
+    }
+    if (const char *v = std::getenv("HGEMM_FORCE_CONFIG")) {
+        if (opt.force_path == 0 && opt.cta_pair == 0) {
+            if (std::strcmp(v, "pair") == 0) {
+                opt.force_path = HGEMM_PATH_TILED;
+                opt.cta_pair = 1;
+            } else if (std::strncmp(v, "single", 6) == 0) {
+                opt.force_path = HGEMM_PATH_TILED;
+                opt.cta_pair = 2;
+                if (v[6] == ':' && opt.tile_n == 0) opt.tile_n = std::atoi(v + 7);
+            } else if (std::strcmp(v, "skinny") == 0) {
+                opt.force_path = HGEMM_PATH_SKINNY;
+            }
+        }
+    }
+}
+
 hgemm_status_t alloc_workspace(hgemm_plan_s *p) {
     size_t off = 256;  // error word (+ padding)
     p->off_counters = off;
@@ -414,6 +445,7 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
     if (st != HGEMM_OK) return st;
     hgemm_options_t opt{};
     if (options) opt = *options;
+    apply_env_overrides(opt);
     if (opt.force_path != 0 && opt.force_path != HGEMM_PATH_TILED && opt.force_path != HGEMM_PATH_SKINNY)
         return fail(HGEMM_ERR_INVALID_ARG, "force_path must be 0, HGEMM_PATH_TILED or HGEMM_PATH_SKINNY");
     if (opt.tile_n != 0 && opt.tile_n != 128 && opt.tile_n != 192 && opt.tile_n != 224 &&
@@ -437,6 +469,8 @@ hgemm_status_t plan_create(hgemm_plan_t *out, int64_t M, int64_t N, int64_t K, i
         return fail(HGEMM_ERR_INVALID_ARG, "tiled_epi_warps must be 0, 4 or 8");
     if (opt.skinny_prefetch < -1 || opt.skinny_prefetch > 64)
         return fail(HGEMM_ERR_INVALID_ARG, "skinny_prefetch must be in [-1, 64]");
+    if (opt.debug_checks < 0 || opt.debug_checks > 2)
+        return fail(HGEMM_ERR_INVALID_ARG, "debug_checks must be 0, 1 or 2");
     if (opt.debug_withhold_kb < 0)
         return fail(HGEMM_ERR_INVALID_ARG, "debug_withhold_kb must be >= 0");
     if (opt.cta_pair == 1 && opt.tile_n != 0 && opt.tile_n != 256 && opt.tile_n != 224)
@@ -834,6 +868,7 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         tp.partials = reinterpret_cast<float *>(p->ws + p->off_partials);
         tp.tail_sync = reinterpret_cast<int32_t *>(p->ws + p->off_counters);
         tp.withhold_kb = p->pair ? 0 : p->opt.debug_withhold_kb;
+        tp.debug = p->opt.debug_checks;
         if (p->pair)
             e = hg::launch_pair(p->bn, p->pair_ks, out_type(p->dout), ts, p->tmA, p->tmB, p->tmC, tp,
                                 p->grid, s);
@@ -870,6 +905,7 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
                   : hg::idesc_f16(bf, p->opt.trans_b ? 0 : 1, 0, 128, static_cast<uint32_t>(p->nu));
     sp.f8 = f8 ? 1 : 0;
     sp.b_kmajor = p->opt.trans_b ? 1 : 0;
+    sp.debug = p->opt.debug_checks;
     sp.C = C;
     sp.ep = ep;
     sp.ldc = p->ldc;
@@ -894,6 +930,14 @@ hgemm_status_t read_error_word(hgemm_plan_s *p) {
     cudaMemset(p->ws, 0, p->off_partials);
     const unsigned role = (static_cast<uint32_t>(word) >> 16) & 0xFFu;
     const unsigned idx = static_cast<uint32_t>(word) & 0xFFFFu;
+    if ((static_cast<uint32_t>(word) & 0xC0000000u) == 0x40000000u) {
+        static const char *kernels[] = {"?", "single-CTA tiled", "CTA-pair", "skinny"};
+        static const char *checks[] = {"?", "tile outside the output", "K range outside K",
+                                       "piece outside its tile"};
+        return fail(HGEMM_ERR_INTERNAL, "device invariant check failed: %s kernel, %s (code 0x%08x)",
+                    role < 4 ? kernels[role] : "?", idx < 4 ? checks[idx] : "?",
+                    static_cast<uint32_t>(word));
+    }
     static const char *names[] = {"?", "TMA producer", "MMA issuer", "epilogue", "drain", "self-test"};
     return fail(HGEMM_ERR_TIMEOUT, "device wait timed out: role %s, barrier %u (code 0x%08x)",
                 role < 6 ? names[role] : "?", idx, static_cast<uint32_t>(word));
@@ -1288,6 +1332,7 @@ const char *hgemm_status_string(hgemm_status_t s) {
         case HGEMM_ERR_CUDA: return "HGEMM_ERR_CUDA";
         case HGEMM_ERR_OOM: return "HGEMM_ERR_OOM";
         case HGEMM_ERR_TIMEOUT: return "HGEMM_ERR_TIMEOUT";
+        case HGEMM_ERR_INTERNAL: return "HGEMM_ERR_INTERNAL";
         default: return "HGEMM_ERR_UNKNOWN";
     }
 }

@@ -214,6 +214,29 @@ struct PairSched {
         u += npairs;
         return true;
     }
+    // next() with the debug checks (p.debug): the piece's tile, its
+    // coordinates, its K range and its segment must lie inside the problem,
+    // else the failure is recorded and the sequence ends here -- for every
+    // role of the pair alike, since all walk the same sequence.
+    bool first = true;
+    __device__ __forceinline__ bool checked(const TiledParams &p, int num_ks, int npairs, Piece &w,
+                                            int pair) {
+        if (!next(p, num_ks, npairs, w)) return false;
+        if (!p.debug) return true;
+        if (p.debug == 2 && first && pair == 0) w.t += p.tiles;  // planted: past the last tile
+        first = false;
+        if (w.t < 0 || w.t >= p.tiles)
+            return invariant_failed(p.err, invariant_code(KERNEL_PAIR, CHECK_TILE));
+        int b, mt, nt;
+        grouped_tile(w.t, p.num_m, p.num_n, p.group_m, b, mt, nt);
+        if (b < 0 || b >= p.batch || mt < 0 || mt >= p.num_m || nt < 0 || nt >= p.num_n)
+            return invariant_failed(p.err, invariant_code(KERNEL_PAIR, CHECK_TILE));
+        if (w.ks0 < 0 || w.ks0 >= w.ks1 || w.ks1 > num_ks)
+            return invariant_failed(p.err, invariant_code(KERNEL_PAIR, CHECK_KRANGE));
+        if (w.role == PIECE_PART && (w.seg < 0 || w.seg >= w.nseg || w.nseg > p.max_seg))
+            return invariant_failed(p.err, invariant_code(KERNEL_PAIR, CHECK_PIECE));
+        return true;
+    }
 };
 
 // Bounded spin on a global flag set (with release) by another CTA.  Polls
@@ -325,7 +348,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             PairSched sched(p, num_ks, pair, npairs);
             Piece w;
-            while (ok && sched.next(p, num_ks, npairs, w)) {
+            while (ok && sched.checked(p, num_ks, npairs, w, pair)) {
                 int b, mt, nt;
                 grouped_tile(w.t, p.num_m, p.num_n, p.group_m, b, mt, nt);
                 const int m0 = mt * (2 * BM) + static_cast<int>(rank) * BM;
@@ -419,7 +442,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             };
             PairSched sched(p, num_ks, pair, npairs);
             Piece w;
-            for (; ok && sched.next(p, num_ks, npairs, w); ++local) {
+            for (; ok && sched.checked(p, num_ks, npairs, w, pair); ++local) {
                 const int ks0 = w.ks0, ks1 = w.ks1;
                 const int buf = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
@@ -489,7 +512,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr int NCH = PN / 32;  // 32-column chunks of a warp's accumulator rows
         PairSched sched(p, num_ks, pair, npairs);
         Piece w;
-        while (sched.next(p, num_ks, npairs, w)) {
+        while (sched.checked(p, num_ks, npairs, w, pair)) {
             const int t = w.t;
             int b, mt, nt;
             grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);

@@ -151,6 +151,23 @@ struct SkinnySched {
         u += gridDim.x;
         return true;
     }
+    // next() with the debug checks (p.debug): the piece's batch entry, column
+    // tile, K range and segment must lie inside the problem, else the failure
+    // is recorded and the sequence ends here for every role of the CTA alike.
+    bool first = true;
+    __device__ __forceinline__ bool checked(const SkinnyParams &p, SkPiece &w) {
+        if (!next(p, w)) return false;
+        if (!p.debug) return true;
+        if (p.debug == 2 && first && blockIdx.x == 0) w.nt += p.num_tiles;  // planted
+        first = false;
+        if (w.b < 0 || w.b >= p.batch || w.nt < 0 || w.nt >= p.num_tiles)
+            return invariant_failed(p.err, invariant_code(KERNEL_SKINNY, CHECK_TILE));
+        if (w.kb0 < 0 || w.kb0 >= w.kb1 || w.kb1 > p.num_kb)
+            return invariant_failed(p.err, invariant_code(KERNEL_SKINNY, CHECK_KRANGE));
+        if (w.seg < 0 || w.seg >= w.nseg || w.nseg > p.split)
+            return invariant_failed(p.err, invariant_code(KERNEL_SKINNY, CHECK_PIECE));
+        return true;
+    }
 };
 
 // F8: 8-bit inputs (kind::f8f6f4), K blocks of 128 elements, both operands
@@ -241,7 +258,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             SkinnySched sched(p);
             SkPiece w;
-            while (ok && sched.next(p, w)) {
+            while (ok && sched.checked(p, w)) {
                 const int b = w.b, nt = w.nt;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(empty(stage), phase ^ 1u, wc,
@@ -325,7 +342,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int local = 0;
             SkinnySched sched(p);
             SkPiece w;
-            for (; ok && sched.next(p, w); ++local) {
+            for (; ok && sched.checked(p, w); ++local) {
                 const int kb0 = w.kb0, kb1 = w.kb1;
                 const int buf = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
@@ -381,7 +398,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int num_sub = p.num_tiles * NT;  // 128-column sub-tiles: NT per unit
         SkinnySched sched(p);
         SkPiece w;
-        for (; sched.next(p, w); ++local) {
+        for (; sched.checked(p, w); ++local) {
             const int b = w.b, nt = w.nt;
             const int buf = local & 1;
             const uint32_t tph = (local >> 1) & 1;

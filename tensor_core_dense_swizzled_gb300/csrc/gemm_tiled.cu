@@ -91,6 +91,23 @@ __device__ __forceinline__ void tile_coords(const TiledParams &p, int t, int &b,
     grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);
 }
 
+// Debug checks (p.debug): tile t, which this CTA is about to process, and its
+// coordinates must lie inside the problem; `first`: the CTA's first tile
+// (planted past the last tile for CTA 0 when p.debug == 2).  On a failure
+// the role records it and leaves its tile loop -- every role alike, since all
+// walk the same tiles.  Returns the tile to use.
+__device__ __forceinline__ bool tiled_item_ok(const TiledParams &p, int &t, bool first) {
+    if (!p.debug) return true;
+    if (p.debug == 2 && first && blockIdx.x == 0) t += p.tiles;
+    if (t < 0 || t >= p.tiles) return invariant_failed(p.err, invariant_code(KERNEL_TILED, CHECK_TILE));
+    int b, mt, nt;
+    tile_coords(p, t, b, mt, nt);
+    if (b < 0 || b >= p.batch || mt < 0 || mt >= p.num_m || nt < 0 || nt >= p.num_n)
+        return invariant_failed(p.err, invariant_code(KERNEL_TILED, CHECK_TILE));
+    if (p.num_kb < 1) return invariant_failed(p.err, invariant_code(KERNEL_TILED, CHECK_KRANGE));
+    return true;
+}
+
 // F8: 8-bit inputs (kind::f8f6f4), K blocks of 128 elements, both operands
 // K-major.
 template <int BN, int OUT, bool TMA_STORE, bool EPI, bool F8 = false, int EW = 4>
@@ -158,7 +175,9 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+            for (int t0 = blockIdx.x; ok && t0 < p.tiles; t0 += gridDim.x) {
+                int t = t0;
+                if (!tiled_item_ok(p, t, t0 == static_cast<int>(blockIdx.x))) break;
                 int b, mt, nt;
                 tile_coords(p, t, b, mt, nt);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -219,7 +238,9 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++local) {
+            for (int t0 = blockIdx.x; ok && t0 < p.tiles; t0 += gridDim.x, ++local) {
+                int t = t0;
+                if (!tiled_item_ok(p, t, t0 == static_cast<int>(blockIdx.x))) break;
                 const int buf = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
                 if (!wait_bounded(tempty(buf), tph ^ 1u, wc, timeout_code(ROLE_MMA, 0x100 + buf))) {
@@ -273,7 +294,9 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
         const EpiArgs epi{&tmC, p.C, p.ldc, p.strideC, p.M, p.N, p.ep};
         int sbuf = 0;
         int local = 0;
-        for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++local) {
+        for (int t0 = blockIdx.x; t0 < p.tiles; t0 += gridDim.x, ++local) {
+            int t = t0;
+            if (!tiled_item_ok(p, t, t0 == static_cast<int>(blockIdx.x))) break;
             int b, mt, nt;
             tile_coords(p, t, b, mt, nt);
             const int buf = local & 1;

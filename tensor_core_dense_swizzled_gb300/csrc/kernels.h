@@ -90,6 +90,9 @@ struct TiledParams {
     // the stage of K block k - 1 of CTA 0's first tile unarmed (no
     // expect_tx, no copies), so the MMA issuer's bounded wait on it expires.
     int32_t withhold_kb;
+    // Invariant checks (debug_checks): 0 off, 1 on, 2 on with an out-of-range
+    // tile planted in the first work item of CTA 0 / pair 0.
+    int32_t debug;
 };
 
 // Skinny kernel: C^T = B^T . A^T, NB x 64 output columns of C per work
@@ -123,6 +126,8 @@ struct SkinnyParams {
     int32_t b_kmajor;
     // 1: 8-bit inputs (K-major only); K blocks of 128 elements.
     int32_t f8;
+    // Invariant checks, as TiledParams::debug.
+    int32_t debug;
 };
 
 // Shared memory the tiled kernel needs for a given BN (bytes, incl. alignment slack).

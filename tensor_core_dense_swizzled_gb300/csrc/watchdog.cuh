@@ -30,6 +30,25 @@ __host__ __device__ constexpr int32_t timeout_code(uint32_t role, uint32_t index
     return static_cast<int32_t>(0x80000000u | (role << 16) | (index & 0xFFFFu));
 }
 
+// Invariant violations (debug checks): bit 30 set; bits 16-23 the kernel
+// (KERNEL_*), bits 0-15 which check failed.
+enum : uint32_t { KERNEL_TILED = 1, KERNEL_PAIR = 2, KERNEL_SKINNY = 3 };
+enum : uint32_t {
+    CHECK_TILE = 1,   // tile index or its (batch, m, n) outside the output
+    CHECK_KRANGE = 2, // K range empty or outside K
+    CHECK_PIECE = 3,  // piece / segment index outside its tile's pieces
+};
+__host__ __device__ constexpr int32_t invariant_code(uint32_t kernel, uint32_t check) {
+    return static_cast<int32_t>(0x40000000u | (kernel << 16) | (check & 0xFFFFu));
+}
+
+// Records a failed invariant (first error wins) and reports it to the caller,
+// who stops before using the work item.
+__device__ __forceinline__ bool invariant_failed(int32_t *err, int32_t code) {
+    atomicCAS(err, 0, code);
+    return false;
+}
+
 // Hard cap on polling iterations, independent of the clock.
 constexpr uint32_t kMaxWaitIterations = 1u << 30;
 // mbarrier polls between two reads of the clock and the abort flag.

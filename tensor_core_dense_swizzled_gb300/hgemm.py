@@ -30,6 +30,7 @@ HGEMM_PATH_EMPTY, HGEMM_PATH_ZERO_FILL, HGEMM_PATH_TILED, HGEMM_PATH_SKINNY = 0,
 STATUS = {
     0: "HGEMM_OK", 1: "HGEMM_ERR_INVALID_ARG", 2: "HGEMM_ERR_UNSUPPORTED",
     3: "HGEMM_ERR_NO_DEVICE", 4: "HGEMM_ERR_CUDA", 5: "HGEMM_ERR_OOM", 6: "HGEMM_ERR_TIMEOUT",
+    7: "HGEMM_ERR_INTERNAL",
 }
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -67,6 +68,7 @@ class Options(ctypes.Structure):
         ("trans_b", ctypes.c_int),
         ("tiled_epi_warps", ctypes.c_int),
         ("debug_withhold_kb", ctypes.c_int),
+        ("debug_checks", ctypes.c_int),
     ]
 
 

@@ -107,7 +107,7 @@ def test_null_handles(lib):
 def test_bad_options_are_refused(lib):
     h = ctypes.c_void_p()
     for opt in (H.Options(force_path=7), H.Options(tile_n=160), H.Options(split_k=-2),
-                H.Options(debug_withhold_kb=-1)):
+                H.Options(debug_withhold_kb=-1), H.Options(debug_checks=3)):
         st = lib.hgemm_plan_create_ex(ctypes.byref(h), *GOOD, ctypes.byref(opt))
         assert st == 1
     # the skinny path is for M <= 32
