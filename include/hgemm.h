@@ -129,12 +129,14 @@ typedef struct {
                                  that take another kernel (CTA pairs, skinny, 8-bit inputs) get
                                  HGEMM_ERR_UNSUPPORTED */
     int debug_checks;         /* 0: off unless the environment variable HGEMM_DEBUG is set to a
-                                 non-zero value; 1: the kernels check their own scheduling
-                                 invariants before every work item (tile coordinates inside the
-                                 output, K ranges inside K, piece indices inside their tile) and,
-                                 on a violation, record it in the device error word and stop
-                                 before touching memory with it: hgemm_check then returns
-                                 HGEMM_ERR_INTERNAL.  No trap, no assert.  2: testing the check
+                                 non-zero value; 1: before its roles start, every CTA walks its
+                                 whole sequence of work items with the scheduler's own code and
+                                 checks their invariants (tile and coordinates inside the output,
+                                 K range inside K, piece inside its tile); on a violation it
+                                 records it in the device error word and does no work at all:
+                                 hgemm_check then returns HGEMM_ERR_INTERNAL.  No trap, no assert.
+                                 (A CTA pair whose K-half or stream-K partner stopped this way
+                                 waits for it until the watchdog limit.)  2: testing the check
                                  only -- the first work item of CTA 0 (or CTA pair 0) is given a
                                  tile index past the last tile, which the check must catch */
 } hgemm_options_t;

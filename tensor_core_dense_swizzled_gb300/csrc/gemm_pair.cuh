@@ -214,16 +214,21 @@ struct PairSched {
         u += npairs;
         return true;
     }
-    // next() with the debug checks (p.debug): the piece's tile, its
-    // coordinates, its K range and its segment must lie inside the problem,
-    // else the failure is recorded and the sequence ends here -- for every
-    // role of the pair alike, since all walk the same sequence.
+};
+
+// Debug checks (p.debug): walks this CTA's whole piece sequence with the
+// schedule's own code, before any role starts, and checks that every piece's
+// tile, coordinates, K range and segment lie inside the problem (with
+// p.debug == 2, pair 0's first piece is given a tile past the last, which the
+// check must catch).  On a failure it records it in the error word and the
+// CTA does no work at all.  Checking up front keeps the roles' loops as they
+// are: a check inside them cost the kernel 1-3 % on GB300.
+__device__ __noinline__ bool pair_sequence_ok(const TiledParams &p, int num_ks, int pair, int npairs) {
+    PairSched sched(p, num_ks, pair, npairs);
+    Piece w;
     bool first = true;
-    __device__ __forceinline__ bool checked(const TiledParams &p, int num_ks, int npairs, Piece &w,
-                                            int pair) {
-        if (!next(p, num_ks, npairs, w)) return false;
-        if (!p.debug) return true;
-        if (p.debug == 2 && first && pair == 0) w.t += p.tiles;  // planted: past the last tile
+    while (sched.next(p, num_ks, npairs, w)) {
+        if (p.debug == 2 && first && pair == 0) w.t += p.tiles;
         first = false;
         if (w.t < 0 || w.t >= p.tiles)
             return invariant_failed(p.err, invariant_code(KERNEL_PAIR, CHECK_TILE));
@@ -235,9 +240,9 @@ struct PairSched {
             return invariant_failed(p.err, invariant_code(KERNEL_PAIR, CHECK_KRANGE));
         if (w.role == PIECE_PART && (w.seg < 0 || w.seg >= w.nseg || w.nseg > p.max_seg))
             return invariant_failed(p.err, invariant_code(KERNEL_PAIR, CHECK_PIECE));
-        return true;
     }
-};
+    return true;
+}
 
 // Bounded spin on a global flag set (with release) by another CTA.  Polls
 // with relaxed loads; the fence after the load that sees the flag makes the
@@ -299,6 +304,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t drain = bar0 + 8u * (2 * Cfg::STAGES + 4);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Cfg::SMEM_MISC);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + Cfg::SMEM_MISC + 4);
+    volatile int32_t *skip_all = reinterpret_cast<volatile int32_t *>(smem + Cfg::SMEM_MISC + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -318,6 +324,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
+        *skip_all = p.debug && !pair_sequence_ok(p, num_ks, pair, npairs) ? 1 : 0;
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -332,6 +339,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
+    const bool run = *skip_all == 0;  // both CTAs of a pair walk the same pieces: same answer
     // The next kernel of the stream may be scheduled now; it waits for this
     // one to complete before it reads memory (griddep_wait below).
     if (threadIdx.x == 0) griddep_launch_dependents();
@@ -345,10 +353,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
-            bool ok = true;
+            bool ok = run;
             PairSched sched(p, num_ks, pair, npairs);
             Piece w;
-            while (ok && sched.checked(p, num_ks, npairs, w, pair)) {
+            while (ok && sched.next(p, num_ks, npairs, w)) {
                 int b, mt, nt;
                 grouped_tile(w.t, p.num_m, p.num_n, p.group_m, b, mt, nt);
                 const int m0 = mt * (2 * BM) + static_cast<int>(rank) * BM;
@@ -429,7 +437,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (rank == 0 && lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            bool ok = true;
+            bool ok = run;
             int local = 0;
             // Completion signals go to each CTA's barrier by its cluster
             // address: the barriers sit at the same offsets in both CTAs, so
@@ -442,7 +450,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             };
             PairSched sched(p, num_ks, pair, npairs);
             Piece w;
-            for (; ok && sched.checked(p, num_ks, npairs, w, pair); ++local) {
+            for (; ok && sched.next(p, num_ks, npairs, w); ++local) {
                 const int ks0 = w.ks0, ks1 = w.ks1;
                 const int buf = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
@@ -512,7 +520,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr int NCH = PN / 32;  // 32-column chunks of a warp's accumulator rows
         PairSched sched(p, num_ks, pair, npairs);
         Piece w;
-        while (sched.checked(p, num_ks, npairs, w, pair)) {
+        while (run && sched.next(p, num_ks, npairs, w)) {
             const int t = w.t;
             int b, mt, nt;
             grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);

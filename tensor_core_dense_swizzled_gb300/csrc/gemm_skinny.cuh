@@ -151,14 +151,19 @@ struct SkinnySched {
         u += gridDim.x;
         return true;
     }
-    // next() with the debug checks (p.debug): the piece's batch entry, column
-    // tile, K range and segment must lie inside the problem, else the failure
-    // is recorded and the sequence ends here for every role of the CTA alike.
+};
+
+// Debug checks (p.debug): walks this CTA's whole piece sequence before any
+// role starts and checks that every piece's batch entry, column tile, K range
+// and segment lie inside the problem (with p.debug == 2, CTA 0's first piece
+// is moved past the last column tile, which the check must catch).  On a
+// failure it records it in the error word and the CTA does no work at all.
+__device__ __noinline__ bool skinny_sequence_ok(const SkinnyParams &p) {
+    SkinnySched sched(p);
+    SkPiece w;
     bool first = true;
-    __device__ __forceinline__ bool checked(const SkinnyParams &p, SkPiece &w) {
-        if (!next(p, w)) return false;
-        if (!p.debug) return true;
-        if (p.debug == 2 && first && blockIdx.x == 0) w.nt += p.num_tiles;  // planted
+    while (sched.next(p, w)) {
+        if (p.debug == 2 && first && blockIdx.x == 0) w.nt += p.num_tiles;
         first = false;
         if (w.b < 0 || w.b >= p.batch || w.nt < 0 || w.nt >= p.num_tiles)
             return invariant_failed(p.err, invariant_code(KERNEL_SKINNY, CHECK_TILE));
@@ -166,9 +171,9 @@ struct SkinnySched {
             return invariant_failed(p.err, invariant_code(KERNEL_SKINNY, CHECK_KRANGE));
         if (w.seg < 0 || w.seg >= w.nseg || w.nseg > p.split)
             return invariant_failed(p.err, invariant_code(KERNEL_SKINNY, CHECK_PIECE));
-        return true;
     }
-};
+    return true;
+}
 
 // F8: 8-bit inputs (kind::f8f6f4), K blocks of 128 elements, both operands
 // K-major.
@@ -194,6 +199,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t drain = bar0 + 8u * (2 * Cfg::STAGES + 4);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Cfg::SMEM_MISC);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + Cfg::SMEM_MISC + 4);
+    volatile int32_t *skip_all = reinterpret_cast<volatile int32_t *>(smem + Cfg::SMEM_MISC + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -209,6 +215,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
+        *skip_all = p.debug && !skinny_sequence_ok(p) ? 1 : 0;
         fence_mbar_init();
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
@@ -222,6 +229,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
+    const bool run = *skip_all == 0;
     // The next kernel of the stream may be scheduled now; it waits for this
     // one to complete before it reads memory (griddep_wait below).
     if (threadIdx.x == 0) griddep_launch_dependents();
@@ -255,10 +263,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
-            bool ok = true;
+            bool ok = run;
             SkinnySched sched(p);
             SkPiece w;
-            while (ok && sched.checked(p, w)) {
+            while (ok && sched.next(p, w)) {
                 const int b = w.b, nt = w.nt;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(empty(stage), phase ^ 1u, wc,
@@ -338,11 +346,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            bool ok = true;
+            bool ok = run;
             int local = 0;
             SkinnySched sched(p);
             SkPiece w;
-            for (; ok && sched.checked(p, w); ++local) {
+            for (; ok && sched.next(p, w); ++local) {
                 const int kb0 = w.kb0, kb1 = w.kb1;
                 const int buf = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
@@ -398,7 +406,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int num_sub = p.num_tiles * NT;  // 128-column sub-tiles: NT per unit
         SkinnySched sched(p);
         SkPiece w;
-        for (; sched.checked(p, w); ++local) {
+        for (; run && sched.next(p, w); ++local) {
             const int b = w.b, nt = w.nt;
             const int buf = local & 1;
             const uint32_t tph = (local >> 1) & 1;

@@ -91,20 +91,22 @@ __device__ __forceinline__ void tile_coords(const TiledParams &p, int t, int &b,
     grouped_tile(t, p.num_m, p.num_n, p.group_m, b, mt, nt);
 }
 
-// Debug checks (p.debug): tile t, which this CTA is about to process, and its
-// coordinates must lie inside the problem; `first`: the CTA's first tile
-// (planted past the last tile for CTA 0 when p.debug == 2).  On a failure
-// the role records it and leaves its tile loop -- every role alike, since all
-// walk the same tiles.  Returns the tile to use.
-__device__ __forceinline__ bool tiled_item_ok(const TiledParams &p, int &t, bool first) {
-    if (!p.debug) return true;
-    if (p.debug == 2 && first && blockIdx.x == 0) t += p.tiles;
-    if (t < 0 || t >= p.tiles) return invariant_failed(p.err, invariant_code(KERNEL_TILED, CHECK_TILE));
-    int b, mt, nt;
-    tile_coords(p, t, b, mt, nt);
-    if (b < 0 || b >= p.batch || mt < 0 || mt >= p.num_m || nt < 0 || nt >= p.num_n)
-        return invariant_failed(p.err, invariant_code(KERNEL_TILED, CHECK_TILE));
+// Debug checks (p.debug): walks this CTA's tiles before any role starts and
+// checks that each tile and its coordinates lie inside the problem (with
+// p.debug == 2, CTA 0's first tile is moved past the last, which the check
+// must catch).  On a failure it records it in the error word and the CTA
+// does no work at all.
+__device__ __noinline__ bool tiled_sequence_ok(const TiledParams &p) {
     if (p.num_kb < 1) return invariant_failed(p.err, invariant_code(KERNEL_TILED, CHECK_KRANGE));
+    for (int t0 = blockIdx.x; t0 < p.tiles; t0 += gridDim.x) {
+        const int t = (p.debug == 2 && blockIdx.x == 0 && t0 == 0) ? t0 + p.tiles : t0;
+        if (t < 0 || t >= p.tiles)
+            return invariant_failed(p.err, invariant_code(KERNEL_TILED, CHECK_TILE));
+        int b, mt, nt;
+        tile_coords(p, t, b, mt, nt);
+        if (b < 0 || b >= p.batch || mt < 0 || mt >= p.num_m || nt < 0 || nt >= p.num_n)
+            return invariant_failed(p.err, invariant_code(KERNEL_TILED, CHECK_TILE));
+    }
     return true;
 }
 
@@ -132,6 +134,7 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
     const uint32_t drain = bar0 + 8u * (2 * Cfg::STAGES + 4);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + Cfg::SMEM_MISC);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem + Cfg::SMEM_MISC + 4);
+    volatile int32_t *skip_all = reinterpret_cast<volatile int32_t *>(smem + Cfg::SMEM_MISC + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -147,6 +150,7 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
+        *skip_all = p.debug && !tiled_sequence_ok(p) ? 1 : 0;
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -161,6 +165,8 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
+    // first tile of this CTA; past the last when the debug checks failed
+    const int t_first = *skip_all ? p.tiles : static_cast<int>(blockIdx.x);
     // The next kernel of the stream may be scheduled now; it waits for this
     // one to complete before it reads memory (griddep_wait below).
     if (threadIdx.x == 0) griddep_launch_dependents();
@@ -175,9 +181,7 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int t0 = blockIdx.x; ok && t0 < p.tiles; t0 += gridDim.x) {
-                int t = t0;
-                if (!tiled_item_ok(p, t, t0 == static_cast<int>(blockIdx.x))) break;
+            for (int t = t_first; ok && t < p.tiles; t += gridDim.x) {
                 int b, mt, nt;
                 tile_coords(p, t, b, mt, nt);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -238,9 +242,7 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
-            for (int t0 = blockIdx.x; ok && t0 < p.tiles; t0 += gridDim.x, ++local) {
-                int t = t0;
-                if (!tiled_item_ok(p, t, t0 == static_cast<int>(blockIdx.x))) break;
+            for (int t = t_first; ok && t < p.tiles; t += gridDim.x, ++local) {
                 const int buf = local & 1;
                 const uint32_t tph = (local >> 1) & 1;
                 if (!wait_bounded(tempty(buf), tph ^ 1u, wc, timeout_code(ROLE_MMA, 0x100 + buf))) {
@@ -294,9 +296,7 @@ __global__ void __launch_bounds__(32 * (2 + EW), 1)
         const EpiArgs epi{&tmC, p.C, p.ldc, p.strideC, p.M, p.N, p.ep};
         int sbuf = 0;
         int local = 0;
-        for (int t0 = blockIdx.x; t0 < p.tiles; t0 += gridDim.x, ++local) {
-            int t = t0;
-            if (!tiled_item_ok(p, t, t0 == static_cast<int>(blockIdx.x))) break;
+        for (int t = t_first; t < p.tiles; t += gridDim.x, ++local) {
             int b, mt, nt;
             tile_coords(p, t, b, mt, nt);
             const int buf = local & 1;

@@ -1,12 +1,13 @@
 """Debug invariant checks of the kernels and the debugging environment
 overrides (HGEMM_DEBUG, HGEMM_TIMEOUT_NS, HGEMM_FORCE_CONFIG).
 
-With debug_checks the kernels check each work item before using it (tile
-and its coordinates inside the output, K range inside K, piece inside its
-tile) and report a violation through the device error word, never by
-trapping.  Checks that never fire must not change any result; a planted
-out-of-range tile (debug_checks = 2, testing only) must be caught, reported
-by hgemm_check as HGEMM_ERR_INTERNAL, and leave the context usable.
+With debug_checks every CTA walks its whole sequence of work items before
+its roles start (tile and its coordinates inside the output, K range inside
+K, piece inside its tile) and reports a violation through the device error
+word, never by trapping; a CTA with a bad item does no work.  Checks that
+never fire must not change any result; a planted out-of-range tile
+(debug_checks = 2, testing only) must be caught, reported by hgemm_check as
+HGEMM_ERR_INTERNAL, and leave the context usable.
 """
 import os
 
@@ -46,8 +47,8 @@ def test_checks_on_change_nothing(dev, case):
                                 dict(force_path=H.HGEMM_PATH_SKINNY),
                                 dict(force_path=H.HGEMM_PATH_SKINNY, split_k=2)])
 def test_planted_tile_is_caught(dev, kw):
-    """CTA 0 (pair 0) is handed a tile past the last one; the check stops it
-    before any load or store with that tile, the run reports
+    """CTA 0 (pair 0) is handed a tile past the last one; the check stops the
+    CTA before any load or store, the run reports
     HGEMM_ERR_INTERNAL, the error word is cleared on read, and a normal run
     right after is correct."""
     skinny = kw.get("force_path") == H.HGEMM_PATH_SKINNY
