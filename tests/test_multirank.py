@@ -76,3 +76,29 @@ def test_reference_arm_prints_one_json_line():
     assert d["higher_is_better"] is True and d["config"]["workload"] == "int512"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_bench_shape_and_plan_options_parse():
+    """--shape takes the workload's inputs at another size (and drops the other
+    configurations); --plan-options sets hgemm_options_t fields by name and
+    refuses unknown ones."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from tensor_core_dense_swizzled_gb300 import inputs
+    w = inputs.WORKLOADS["square4096"]
+    old = sys.argv
+    try:
+        sys.argv = ["bench.py", "--shape", "512,256,128", "--plan-options", "cta_pair=2,group_m=8"]
+        args = bench.parse()
+        opt = bench.plan_options(args, w)
+        assert (opt.cta_pair, opt.group_m, opt.trans_b) == (2, 8, 0)
+        assert args.shape == "512,256,128"
+        sys.argv = ["bench.py", "--plan-options", "no_such_field=1"]
+        args = bench.parse()
+        try:
+            bench.plan_options(args, w)
+            raise AssertionError("an unknown field was accepted")
+        except SystemExit:
+            pass
+    finally:
+        sys.argv = old
