@@ -321,10 +321,21 @@ hgemm_status_t hgemm_watchdog_selftest(uint64_t timeout_ns, void *stream, int32_
  * shares the array: calls that overlap on the GPU race and must be ordered.
  * The split count is lowered to fit the array; a request that does not fit
  * even unsplit returns HGEMM_ERR_UNSUPPORTED, as do misaligned operands and
- * M > 32.  Watchdog timeouts are not reported by this entry point. */
+ * M > 32.  A device watchdog timeout is not returned here (the kernel runs
+ * after the call returns): hgemm_skinny_noalloc_check reports it. */
 hgemm_status_t hgemm_skinny_noalloc(const void *A, const void *B, void *C, int64_t M, int64_t N,
                                     int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                                     hgemm_dtype_t dtype_in, hgemm_dtype_t dtype_out, void *stream);
+
+/* Status of the last hgemm_skinny_noalloc product on the current device, the
+ * allocation-free counterpart of hgemm_check: synchronises `stream` (the
+ * stream that product used), reads the array's device error word and clears
+ * it.  HGEMM_OK, or HGEMM_ERR_TIMEOUT when a device wait of that product
+ * timed out (C is then incomplete; the detail names the role and barrier).
+ * Allocates nothing.  Call it after the product and before the next
+ * hgemm_skinny_noalloc on the device, which clears the word before its
+ * kernel runs. */
+hgemm_status_t hgemm_skinny_noalloc_check(void *stream);
 
 /* ---------------------------------------------------------------- attention
  *

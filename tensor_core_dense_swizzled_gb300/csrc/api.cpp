@@ -928,19 +928,7 @@ hgemm_status_t read_error_word(hgemm_plan_s *p) {
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
     if (word == 0) return HGEMM_OK;
     cudaMemset(p->ws, 0, p->off_partials);
-    const unsigned role = (static_cast<uint32_t>(word) >> 16) & 0xFFu;
-    const unsigned idx = static_cast<uint32_t>(word) & 0xFFFFu;
-    if ((static_cast<uint32_t>(word) & 0xC0000000u) == 0x40000000u) {
-        static const char *kernels[] = {"?", "single-CTA tiled", "CTA-pair", "skinny"};
-        static const char *checks[] = {"?", "tile outside the output", "K range outside K",
-                                       "piece outside its tile"};
-        return fail(HGEMM_ERR_INTERNAL, "device invariant check failed: %s kernel, %s (code 0x%08x)",
-                    role < 4 ? kernels[role] : "?", idx < 4 ? checks[idx] : "?",
-                    static_cast<uint32_t>(word));
-    }
-    static const char *names[] = {"?", "TMA producer", "MMA issuer", "epilogue", "drain", "self-test"};
-    return fail(HGEMM_ERR_TIMEOUT, "device wait timed out: role %s, barrier %u (code 0x%08x)",
-                role < 6 ? names[role] : "?", idx, static_cast<uint32_t>(word));
+    return hg::status_from_error_word(word);
 }
 
 // ---------------------------------------------------------------- one-shot cache
@@ -1382,5 +1370,22 @@ int pick_skinny_nb(int64_t N, int64_t batch, int num_sms) {
 }
 
 hgemm_status_t set_error_detail(hgemm_status_t s, const char *msg) { return fail(s, "%s", msg); }
+
+hgemm_status_t status_from_error_word(int32_t word) {
+    if (word == 0) return HGEMM_OK;
+    const unsigned role = (static_cast<uint32_t>(word) >> 16) & 0xFFu;
+    const unsigned idx = static_cast<uint32_t>(word) & 0xFFFFu;
+    if ((static_cast<uint32_t>(word) & 0xC0000000u) == 0x40000000u) {
+        static const char *kernels[] = {"?", "single-CTA tiled", "CTA-pair", "skinny"};
+        static const char *checks[] = {"?", "tile outside the output", "K range outside K",
+                                       "piece outside its tile"};
+        return fail(HGEMM_ERR_INTERNAL, "device invariant check failed: %s kernel, %s (code 0x%08x)",
+                    role < 4 ? kernels[role] : "?", idx < 4 ? checks[idx] : "?",
+                    static_cast<uint32_t>(word));
+    }
+    static const char *names[] = {"?", "TMA producer", "MMA issuer", "epilogue", "drain", "self-test"};
+    return fail(HGEMM_ERR_TIMEOUT, "device wait timed out: role %s, barrier %u (code 0x%08x)",
+                role < 6 ? names[role] : "?", idx, static_cast<uint32_t>(word));
+}
 
 }  // namespace hg

@@ -30,4 +30,9 @@ int pick_skinny_nb(int64_t N, int64_t batch, int num_sms);
 // Records `msg` as the calling thread's hgemm_last_error_detail() and returns s.
 hgemm_status_t set_error_detail(hgemm_status_t s, const char *msg);
 
+// The status a nonzero device error word stands for (a watchdog timeout:
+// HGEMM_ERR_TIMEOUT; a failed debug invariant check: HGEMM_ERR_INTERNAL),
+// with the word decoded into hgemm_last_error_detail(); HGEMM_OK for 0.
+hgemm_status_t status_from_error_word(int32_t word);
+
 }  // namespace hg

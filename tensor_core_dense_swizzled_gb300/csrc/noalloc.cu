@@ -34,7 +34,8 @@
 // count is the planned path's; it is lowered when the partial sums would not
 // fit in the array, and a request that does not fit even unsplit is refused
 // with HGEMM_ERR_UNSUPPORTED.  A device watchdog timeout is recorded in the
-// array's error word (cleared by the next call) but not reported here.
+// array's error word; hgemm_skinny_noalloc_check reads and clears it (the
+// next product clears it too, before its kernel runs).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -229,4 +230,22 @@ extern "C" hgemm_status_t hgemm_skinny_noalloc(const void *A, const void *B, voi
     e = hg::launch_skinny(nu, nb, out, tmX, tmW, sp, grid, s);
     if (e != cudaSuccess) return set_error_detail(HGEMM_ERR_CUDA, cudaGetErrorString(e));
     return HGEMM_OK;
+}
+
+extern "C" hgemm_status_t hgemm_skinny_noalloc_check(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return hg::set_error_detail(HGEMM_ERR_CUDA, cudaGetErrorString(e));
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return hg::set_error_detail(HGEMM_ERR_NO_DEVICE, "no CUDA device");
+    unsigned char *scratch = nullptr;
+    hgemm_status_t st = scratch_address(dev, &scratch);
+    if (st != HGEMM_OK) return st;
+    int32_t word = 0;
+    e = cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return hg::set_error_detail(HGEMM_ERR_CUDA, cudaGetErrorString(e));
+    if (word == 0) return HGEMM_OK;
+    e = cudaMemset(scratch, 0, sizeof(word));
+    if (e != cudaSuccess) return hg::set_error_detail(HGEMM_ERR_CUDA, cudaGetErrorString(e));
+    return hg::status_from_error_word(word);
 }

@@ -17,7 +17,8 @@ __all__ = [
     "HGEMM_PATH_TILED", "HGEMM_PATH_SKINNY", "HgemmError", "Options", "PlanInfo", "lib_path",
     "load", "hgemm_plan_create", "hgemm_plan_create_ex", "hgemm_run", "hgemm_run_host",
     "hgemm_check", "hgemm_plan_destroy", "hgemm_plan_get_info", "hgemm", "hgemm_cache_clear",
-    "hgemm_watchdog_selftest", "hgemm_skinny_noalloc", "hgemm_status_string", "Epilogue",
+    "hgemm_watchdog_selftest", "hgemm_skinny_noalloc", "hgemm_skinny_noalloc_check",
+    "hgemm_status_string", "Epilogue",
     "hgemm_run_ex", "HGEMM_ACT_NONE", "HGEMM_ACT_RELU", "HGEMM_ACT_GELU", "HGEMM_ACT_GELU_TANH",
     "hgemm_last_error_detail", "hgemm_version", "hgemm_attention_plan_create",
     "hgemm_attention_run", "hgemm_attention_run_host", "hgemm_attention_check",
@@ -143,6 +144,7 @@ def load():
         lib.hgemm_watchdog_selftest.argtypes = [ctypes.c_uint64, p, ctypes.POINTER(ctypes.c_int32)]
         lib.hgemm_skinny_noalloc.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int,
                                              ctypes.c_int, p]
+        lib.hgemm_skinny_noalloc_check.argtypes = [p]
         lib.hgemm_attention_plan_create.argtypes = [plan_p, i64, i64, i64, i64, ctypes.c_float,
                                                     ctypes.c_int, ctypes.c_int]
         lib.hgemm_attention_run.argtypes = [p, p, p, p, p, p]
@@ -154,7 +156,8 @@ def load():
                      "hgemm_attention_run_host", "hgemm_attention_check",
                      "hgemm_attention_plan_destroy",
                      "hgemm_check", "hgemm_plan_destroy", "hgemm_plan_get_info", "hgemm",
-                     "hgemm_cache_clear", "hgemm_watchdog_selftest", "hgemm_skinny_noalloc"):
+                     "hgemm_cache_clear", "hgemm_watchdog_selftest", "hgemm_skinny_noalloc",
+                     "hgemm_skinny_noalloc_check"):
             getattr(lib, name).restype = st
         lib.hgemm_status_string.argtypes = [ctypes.c_int]
         lib.hgemm_status_string.restype = ctypes.c_char_p
@@ -276,6 +279,12 @@ def hgemm_skinny_noalloc(A, B, C, M, N, K, lda, ldb, ldc, dtype_in, dtype_out, s
     _check(load().hgemm_skinny_noalloc(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc,
                                        dtype_in, dtype_out, _stream(stream)),
            "hgemm_skinny_noalloc")
+
+
+def hgemm_skinny_noalloc_check(stream=None) -> int:
+    """Status of the last hgemm_skinny_noalloc product on the current device
+    (0, or HGEMM_ERR_TIMEOUT=6); returned instead of raised, like hgemm_check."""
+    return load().hgemm_skinny_noalloc_check(_stream(stream))
 
 
 def hgemm_status_string(status: int) -> str:

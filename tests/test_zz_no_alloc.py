@@ -69,6 +69,8 @@ def test_no_alloc_matches_planned_path_twice(dev):
         C = torch.full((w.M, w.N), 7.0, dtype=torch.bfloat16, device=dev)
         st = noalloc(lib, dA, dB, C, w.M, w.N, w.K, w.lda, w.ldb, w.ldc, H.HGEMM_BF16, H.HGEMM_BF16)
         assert st == 0, H.hgemm_last_error_detail()
+        # the allocation-free status check: no watchdog timeout, word cleared
+        assert H.hgemm_skinny_noalloc_check(torch.cuda.current_stream().cuda_stream) == 0
         torch.cuda.synchronize()
         got = oracle.decode(bits(C), 1).reshape(1, w.M, w.N)
         diff = np.abs(got - planned)
@@ -90,6 +92,7 @@ def test_no_alloc_small_shapes_and_outputs(dev):
             C = torch.empty(M, N, dtype=td, device=dev)
             st = noalloc(lib, A.to(dev), B.to(dev), C, M, N, K, K, N, N, H.HGEMM_F16, dout)
             assert st == 0, H.hgemm_last_error_detail()
+            assert H.hgemm_skinny_noalloc_check() == 0, H.hgemm_last_error_detail()
             torch.cuda.synchronize()
             Cref, Den = oracle.gemm(bits(A), bits(B), 0, M, N, K, K, N)
             got = C.cpu().double().numpy()[None] if dout == H.HGEMM_F32 else \
