@@ -231,21 +231,26 @@ def kernel_family(kernel_name: str) -> str:
     return "attention" if "attention" in kernel_name else "other"
 
 
-def kernel_hash(family: str) -> str:
+# Headers every kernel is compiled with (the host-only ones, hgemm.h and
+# internal.h, do not reach device code and are left out).
+DEVICE_HEADERS = ("kernels.h", "ptx.cuh", "tile_common.cuh", "watchdog.cuh")
+
+
+def kernel_hash(family: str, csrc: str | None = None) -> str:
     """Hash of the device sources a kernel family is built from: its own
-    files and the shared headers (the stored entry names the kernel variant
-    the capture saw)."""
+    files and the headers device code includes (the stored entry names the
+    kernel variant the capture saw)."""
     own = {
         "pair": ("gemm_pair",),
         "tiled": ("gemm_tiled",),
         "skinny": ("gemm_skinny",),
         "attention": ("attention.cu",),
     }.get(family, ())
+    csrc = csrc or os.path.join(ROOT, "tensor_core_dense_swizzled_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "tensor_core_dense_swizzled_gb300", "csrc", "*"))):
+    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
         base = os.path.basename(f)
-        shared = base.endswith((".h", ".cuh")) and not base.startswith(("gemm_", "attention"))
-        if not shared and not base.startswith(own):
+        if base not in DEVICE_HEADERS and not base.startswith(own):
             continue
         with open(f, "rb") as fh:
             h.update(fh.read())
