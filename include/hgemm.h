@@ -283,8 +283,10 @@ hgemm_status_t hgemm_plan_destroy(hgemm_plan_t plan);
 hgemm_status_t hgemm_plan_get_info(hgemm_plan_t plan, hgemm_plan_info_t *info);
 
 /* One-shot product: looks up (or creates and keeps) a plan for these
- * arguments in a process-wide cache, then runs it on `stream`.  Cached plans
- * live until hgemm_cache_clear() or process exit. */
+ * arguments and this stream in a process-wide cache, then runs it on
+ * `stream`.  Each stream gets a plan (and workspace) of its own, so one-shot
+ * calls may run on several streams and from several host threads at once.
+ * Cached plans live until hgemm_cache_clear() or process exit. */
 hgemm_status_t hgemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                      int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t strideA,
                      int64_t strideB, int64_t strideC, hgemm_dtype_t dtype_in,

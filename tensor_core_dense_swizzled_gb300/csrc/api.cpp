@@ -17,6 +17,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <tuple>
@@ -932,11 +933,21 @@ hgemm_status_t read_error_word(hgemm_plan_s *p) {
 }
 
 // ---------------------------------------------------------------- one-shot cache
+//
+// One plan per (device, arguments, stream): a plan must not run on two streams
+// at once (its workspace is shared), so callers on different streams get
+// plans of their own.  Each entry's lock keeps two host threads that use the
+// same stream from updating the plan's cached tensor maps at the same time;
+// their runs are ordered by the stream itself.
 
 using CacheKey = std::tuple<int, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t,
-                            int64_t, int64_t, int64_t, int, int>;
+                            int64_t, int64_t, int64_t, int, int, uintptr_t>;
+struct CacheEntry {
+    hgemm_plan_s *plan = nullptr;
+    std::mutex mu;
+};
 std::mutex g_cache_mu;
-std::map<CacheKey, hgemm_plan_s *> g_cache;
+std::map<CacheKey, std::unique_ptr<CacheEntry>> g_cache;
 
 }  // namespace
 
@@ -1270,26 +1281,31 @@ hgemm_status_t hgemm(const void *A, const void *B, void *C, int64_t M, int64_t N
     cudaGetDevice(&dev);
     CacheKey key{dev, M, N, K, lda, ldb, ldc, batch, batch > 1 ? strideA : 0,
                  batch > 1 ? strideB : 0, batch > 1 ? strideC : 0, static_cast<int>(dtype_in),
-                 static_cast<int>(dtype_out)};
-    hgemm_plan_s *p = nullptr;
+                 static_cast<int>(dtype_out), reinterpret_cast<uintptr_t>(stream)};
+    CacheEntry *entry = nullptr;
     {
         std::lock_guard<std::mutex> g(g_cache_mu);
         auto it = g_cache.find(key);
         if (it != g_cache.end()) {
-            p = it->second;
+            entry = it->second.get();
         } else {
+            hgemm_plan_s *p = nullptr;
             hgemm_status_t st = plan_create(&p, M, N, K, lda, ldb, ldc, batch, strideA, strideB,
                                             strideC, dtype_in, dtype_out, nullptr);
             if (st != HGEMM_OK) return st;
-            g_cache[key] = p;
+            auto e = std::make_unique<CacheEntry>();
+            e->plan = p;
+            entry = e.get();
+            g_cache[key] = std::move(e);
         }
     }
-    return plan_run(p, A, B, C, static_cast<cudaStream_t>(stream));
+    std::lock_guard<std::mutex> g(entry->mu);
+    return plan_run(entry->plan, A, B, C, static_cast<cudaStream_t>(stream));
 }
 
 hgemm_status_t hgemm_cache_clear(void) {
     std::lock_guard<std::mutex> g(g_cache_mu);
-    for (auto &kv : g_cache) hgemm_plan_destroy(kv.second);
+    for (auto &kv : g_cache) hgemm_plan_destroy(kv.second->plan);
     g_cache.clear();
     return HGEMM_OK;
 }

@@ -854,6 +854,43 @@ def test_one_shot_and_matmul(dev):
     H.hgemm_cache_clear()
 
 
+def test_one_shot_on_two_streams_from_two_threads(dev):
+    """hgemm() from two host threads, each on a stream of its own, many times
+    over, on a split-K shape (partial sums in the plan's workspace): the
+    cache gives each stream its own plan, so neither run disturbs the other."""
+    import threading
+    M, N, K = 16, 1024, 8192
+    B = inputs.make_random((K, N), "bf16", 70)
+    As = [inputs.make_random((M, K), "bf16", 71 + i) for i in range(2)]
+    dB = B.to(dev)
+    dA = [a.to(dev) for a in As]
+    Cs = [torch.zeros(M, N, dtype=torch.float32, device=dev) for _ in range(2)]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    H.hgemm_cache_clear()
+    errors = []
+
+    def work(i):
+        try:
+            with torch.cuda.stream(streams[i]):
+                for _ in range(30):
+                    H.hgemm(dA[i], dB, Cs[i], M, N, K, K, N, N, 1, 0, 0, 0, H.HGEMM_BF16, H.HGEMM_F32,
+                            streams[i].cuda_stream)
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for i in range(2):
+        Cref, Den = oracle.gemm(bits(As[i]), bits(B), 1, M, N, K, K, N)
+        check(Cs[i].cpu().double().numpy()[None], Cref, Den, "f32")
+    H.hgemm_cache_clear()
+
+
 def test_matmul_transposed_fp8_and_epilogue(dev):
     """The torch front end's planned paths: B given as W.t() (transposed-B
     kernels), 8-bit inputs, and the fused epilogue."""
