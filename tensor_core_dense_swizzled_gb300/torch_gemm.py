@@ -9,7 +9,10 @@ Plain products go through the one-shot ``hgemm`` entry point (its plan cache
 lives in the library).  Products with B given as the transpose of a row-major
 N x K tensor (``B = W.t()``), 8-bit inputs or a fused epilogue go through
 plans created with ``hgemm_plan_create_ex`` and kept in a cache here
-(:func:`matmul_cache_clear` frees them).
+(:func:`matmul_cache_clear` frees them).  Both caches hold one plan per
+stream (a plan's workspace must not serve two streams at once), and a plan's
+host-side run is serialised, so matmul may be called from several threads
+and streams at once.
 """
 from __future__ import annotations
 
@@ -27,24 +30,25 @@ _OUT = {torch.float16: _h.HGEMM_F16, torch.bfloat16: _h.HGEMM_BF16, torch.float3
 _ACT = {None: _h.HGEMM_ACT_NONE, "none": _h.HGEMM_ACT_NONE, "relu": _h.HGEMM_ACT_RELU,
         "gelu": _h.HGEMM_ACT_GELU, "gelu_tanh": _h.HGEMM_ACT_GELU_TANH}
 
-_plans: dict = {}
+_plans: dict = {}  # key (arguments, stream) -> (plan handle, lock held while it runs)
 _plans_lock = threading.Lock()
 
 
-def _plan(key, M, N, K, lda, ldb, ldc, batch, sA, sB, sC, din, dout, trans_b) -> int:
+def _plan(key, M, N, K, lda, ldb, ldc, batch, sA, sB, sC, din, dout, trans_b):
     with _plans_lock:
-        h = _plans.get(key)
-        if h is None:
+        entry = _plans.get(key)
+        if entry is None:
             h = _h.hgemm_plan_create_ex(M, N, K, lda, ldb, ldc, batch, sA, sB, sC, din, dout,
                                         _h.Options(trans_b=int(trans_b)))
-            _plans[key] = h
-        return h
+            entry = (h, threading.Lock())
+            _plans[key] = entry
+        return entry
 
 
 def matmul_cache_clear() -> None:
     """Destroys the plans :func:`matmul` created (none may still be running)."""
     with _plans_lock:
-        for h in _plans.values():
+        for h, _ in _plans.values():
             _h.hgemm_plan_destroy(h)
         _plans.clear()
 
@@ -126,13 +130,15 @@ def matmul(A: torch.Tensor, B: torch.Tensor, out_dtype: torch.dtype | None = Non
         if not trans_b and not epi:
             _h.hgemm(A, B, out, M, N, K, lda, ldb, ldc, batch, sA, sB, sC, din, dout, stream)
             return out
-        key = (A.device.index, M, N, K, lda, ldb, ldc, batch, sA, sB, sC, din, dout, trans_b)
-        plan = _plan(key, M, N, K, lda, ldb, ldc, batch, sA, sB, sC, din, dout, trans_b)
-        if epi:
-            ep = types.SimpleNamespace(alpha=float(alpha), beta=float(beta), bias=bias,
-                                       row_scale=row_scale, col_scale=col_scale,
-                                       activation=_ACT[activation])
-            _h.hgemm_run_ex(plan, A, B, out, ep, stream)
-        else:
-            _h.hgemm_run(plan, A, B, out, stream)
+        key = (A.device.index, M, N, K, lda, ldb, ldc, batch, sA, sB, sC, din, dout, trans_b,
+               stream.cuda_stream)
+        plan, lock = _plan(key, M, N, K, lda, ldb, ldc, batch, sA, sB, sC, din, dout, trans_b)
+        with lock:
+            if epi:
+                ep = types.SimpleNamespace(alpha=float(alpha), beta=float(beta), bias=bias,
+                                           row_scale=row_scale, col_scale=col_scale,
+                                           activation=_ACT[activation])
+                _h.hgemm_run_ex(plan, A, B, out, ep, stream)
+            else:
+                _h.hgemm_run(plan, A, B, out, stream)
     return out

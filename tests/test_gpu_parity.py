@@ -891,6 +891,43 @@ def test_one_shot_on_two_streams_from_two_threads(dev):
     H.hgemm_cache_clear()
 
 
+def test_matmul_planned_path_on_two_streams_from_two_threads(dev):
+    """The torch front end's own plan cache (B given as W.t(): planned,
+    transposed-B path) from two host threads on two streams, on a split-K
+    shape: each stream gets its own plan."""
+    import threading
+
+    from tensor_core_dense_swizzled_gb300 import matmul, matmul_cache_clear
+    M, N, K = 16, 1024, 8192
+    W = inputs.make_random((N, K), "bf16", 80)  # stored N x K
+    As = [inputs.make_random((M, K), "bf16", 81 + i) for i in range(2)]
+    dW = W.to(dev)
+    dA = [a.to(dev) for a in As]
+    Cs = [torch.zeros(M, N, dtype=torch.float32, device=dev) for _ in range(2)]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    matmul_cache_clear()
+    errors = []
+
+    def work(i):
+        try:
+            for _ in range(30):
+                matmul(dA[i], dW.t(), out_dtype=torch.float32, out=Cs[i], stream=streams[i])
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for i in range(2):
+        Cref, Den = oracle.gemm_bt(bits(As[i]), bits(W), 1, M, N, K, K, K)
+        check(Cs[i].cpu().double().numpy()[None], Cref, Den, "f32")
+    matmul_cache_clear()
+
+
 def test_matmul_transposed_fp8_and_epilogue(dev):
     """The torch front end's planned paths: B given as W.t() (transposed-B
     kernels), 8-bit inputs, and the fused epilogue."""
