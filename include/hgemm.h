@@ -23,7 +23,9 @@
  * workspace (error word, split-K partials, aligned copies of misaligned
  * operands) and its cached TMA descriptors; hgemm_plan_destroy frees them.
  * A plan is bound to the CUDA device that is current when it is created, and
- * one plan must not run on two streams at once (its workspace is shared).
+ * one plan must not run on two streams, or from two host threads, at once (its
+ * workspace and cached descriptors are shared); the one-shot hgemm() keeps a
+ * plan per stream for this reason.
  *
  * Errors.  Every entry point returns a status and never aborts, exits or
  * prints.  hgemm_last_error_detail() gives a message for the calling thread's
@@ -363,7 +365,9 @@ hgemm_status_t hgemm_skinny_noalloc_check(void *stream);
  * causal needs seq_q <= seq_kv, so that every row has a key (else
  * HGEMM_ERR_INVALID_ARG).  seq_q == 0 does nothing; seq_kv == 0 writes
  * zeros (the empty sum).  Plans own a small device workspace (the error
- * word) and the staging buffers of hgemm_attention_run_host. */
+ * word), cached TMA descriptors and the staging buffers of
+ * hgemm_attention_run_host; as with GEMM plans, one plan must not run on two
+ * streams or from two host threads at once: give each its own plan. */
 typedef struct hgemm_attn_plan_s *hgemm_attn_plan_t;
 
 hgemm_status_t hgemm_attention_plan_create(hgemm_attn_plan_t *plan, int64_t batch_heads,
