@@ -223,6 +223,22 @@ hgemm_status_t validate(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     if (batch > 1 && M > 0 && N > 0 && sC < (M - 1) * ldc + N)
         return fail(HGEMM_ERR_INVALID_ARG, "strideC (%lld) makes the batches of C overlap",
                     static_cast<long long>(sC));
+    {
+        // every byte count derived from a span (staging buffers, copies,
+        // tensor-map strides) must fit comfortably in 64 bits
+        auto span_bytes = [](int64_t rows, int64_t cols, int64_t ld, int64_t nb, int64_t stride, int eb) {
+            if (rows == 0 || cols == 0) return static_cast<__int128>(0);
+            return (static_cast<__int128>(nb - 1) * stride + static_cast<__int128>(rows - 1) * ld + cols) * eb;
+        };
+        const __int128 kMaxSpan = static_cast<__int128>(1) << 60;
+        const int ib = in_bytes(din), ob = out_bytes(dout);
+        const int64_t nb = batch > 1 ? batch : 1;
+        if (span_bytes(M, K, lda, nb, batch > 1 ? sA : 0, ib) > kMaxSpan ||
+            span_bytes(trans_b ? N : K, trans_b ? K : N, ldb, nb, batch > 1 ? sB : 0, ib) > kMaxSpan ||
+            span_bytes(M, N, ldc, nb, batch > 1 ? sC : 0, ob) > kMaxSpan)
+            return fail(HGEMM_ERR_UNSUPPORTED, "an operand spans more than 2^60 bytes (leading dimension or "
+                                               "batch stride too large)");
+    }
     const int64_t tiles = batch * ceil_div(M, 128) * ceil_div(N, 128);
     if (tiles > kMaxDim) return fail(HGEMM_ERR_UNSUPPORTED, "too many output tiles");
     if (is_f8(din) && M > 0 && N > 0 && K > 0) {

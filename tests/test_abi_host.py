@@ -96,6 +96,23 @@ def test_oversized_request_is_unsupported(lib):
     assert st == 2
 
 
+@pytest.mark.parametrize("args,why", [
+    ((1 << 20, 64, 64, 1 << 45, 64, 64, 1, 0, 0, 0, H.HGEMM_F16, H.HGEMM_F32), "huge lda"),
+    ((64, 64, 1 << 20, 1 << 20, 1 << 45, 64, 1, 0, 0, 0, H.HGEMM_F16, H.HGEMM_F32), "huge ldb"),
+    ((1 << 20, 64, 64, 64, 64, 1 << 45, 1, 0, 0, 0, H.HGEMM_F16, H.HGEMM_F32), "huge ldc"),
+    ((64, 64, 64, 64, 64, 64, 1 << 20, 1 << 45, 4096, 4096, H.HGEMM_F16, H.HGEMM_F32), "huge strideA"),
+    ((64, 64, 64, 64, (1 << 62) + 1, 64, 1 << 10, 4096, 1, 4096, H.HGEMM_F16, H.HGEMM_F32),
+     "span past 64 bits"),
+])
+def test_spans_beyond_2_60_bytes_are_unsupported(lib, args, why):
+    """A leading dimension or batch stride whose operand span passes 2^60
+    bytes is refused before any byte count could overflow."""
+    st, h = _create(*args)
+    assert st == 2, f"{why}: got {H.STATUS.get(st, st)}"
+    assert h is None
+    assert "2^60" in H.hgemm_last_error_detail()
+
+
 def test_null_handles(lib):
     assert lib.hgemm_run(None, None, None, None, None) == 1
     assert lib.hgemm_check(None, None) == 1
