@@ -133,6 +133,10 @@ hgemm_status_t hgemm_attention_plan_create(hgemm_attn_plan_t *plan, int64_t batc
     if (seq_q > kMax32 || seq_kv > kMax32 || batch_heads > kMax32 ||
         batch_heads * ((seq_q + 127) / 128) > kMax32)
         return afail(HGEMM_ERR_UNSUPPORTED, "sizes above 2^31-1 are not supported");
+    // the byte sizes of Q / O and of K / V (staging buffers, copies) must fit
+    // comfortably in 64 bits: batch_heads x seq x 128 x 2 bytes <= 2^60
+    if (batch_heads > ((1ll << 52) / (seq_q > seq_kv ? (seq_q > 0 ? seq_q : 1) : (seq_kv > 0 ? seq_kv : 1))))
+        return afail(HGEMM_ERR_UNSUPPORTED, "batch_heads x sequence length too large (over 2^60 bytes)");
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

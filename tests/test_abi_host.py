@@ -176,7 +176,8 @@ def test_attention_argument_checks_need_no_gpu(lib):
            ((2, 32, 16, 128, 1.0, 1, H.HGEMM_BF16), 1),     # causal, seq_q > seq_kv
            ((2, 16, 16, 128, 1.0, 2, H.HGEMM_BF16), 1),     # causal not 0 / 1
            ((2, 16, 16, 128, 1.0, 0, H.HGEMM_E4M3), 1),     # 8-bit inputs
-           ((2, 16, 16, 64, 1.0, 0, H.HGEMM_BF16), 2)]      # head_dim 64
+           ((2, 16, 16, 64, 1.0, 0, H.HGEMM_BF16), 2),      # head_dim 64
+           (((1 << 31) - 1, 16, (1 << 31) - 1, 128, 1.0, 0, H.HGEMM_BF16), 2)]  # K / V past 2^60 bytes
     for args, want in bad:
         assert lib.hgemm_attention_plan_create(ctypes.byref(h), *args) == want, args
     assert lib.hgemm_attention_plan_create(None, 2, 16, 16, 128, 1.0, 0, H.HGEMM_BF16) == 1
