@@ -30,7 +30,11 @@
  * Errors.  Every entry point returns a status and never aborts, exits or
  * prints.  hgemm_last_error_detail() gives a message for the calling thread's
  * last failure.  Kernel launches are asynchronous: a device-side watchdog
- * timeout surfaces at hgemm_check().
+ * timeout surfaces at hgemm_check().  Operand pointers of the device-memory
+ * entry points must point into device memory of the plan's GPU (or managed
+ * memory): each run asks cudaPointerGetAttributes about a pointer the first
+ * time it sees it and refuses host memory, another GPU's memory or an
+ * unknown address with HGEMM_ERR_INVALID_ARG, before anything is launched.
  *
  * Alignment.  Pointers must be element-aligned.  When a base pointer is
  * 16-byte aligned and its leading dimension and batch stride are multiples of

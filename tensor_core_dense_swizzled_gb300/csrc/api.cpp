@@ -180,6 +180,8 @@ struct hgemm_plan_s {
     cudaEvent_t ev_start = nullptr, ev_done = nullptr;
     cudaEvent_t ev_a[kMaxHostChunks] = {}, ev_c[kMaxHostChunks] = {};
     // tensor-map cache
+    const void *okA = nullptr, *okB = nullptr;  // the last A, B, C that passed
+    const void *okC = nullptr;                  //   check_device_pointer
     const void *mA = nullptr, *mB = nullptr;
     void *mC = nullptr;
     bool maps_ok = false;
@@ -800,6 +802,11 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
     cudaGetDevice(&cur);
     if (cur != p->device)
         return fail(HGEMM_ERR_INVALID_ARG, "plan was created on device %d but device %d is current", p->device, cur);
+    if (C != p->okC) {  // checked once per pointer
+        hgemm_status_t pst = hg::check_device_pointer(C, p->device, "C");
+        if (pst != HGEMM_OK) return pst;
+        p->okC = C;
+    }
     cudaError_t e;
     if (p->path == HGEMM_PATH_ZERO_FILL) {
         if (ep.on) {
@@ -811,6 +818,13 @@ hgemm_status_t plan_run(hgemm_plan_s *p, const void *A, const void *B, void *C, 
         return e == cudaSuccess ? HGEMM_OK : cuda_fail(e, "zero-fill launch");
     }
     if (!A || !B) return fail(HGEMM_ERR_INVALID_ARG, "A or B is NULL");
+    if (A != p->okA || B != p->okB) {  // checked once per pointer pair
+        hgemm_status_t pst = hg::check_device_pointer(A, p->device, "A");
+        if (pst == HGEMM_OK) pst = hg::check_device_pointer(B, p->device, "B");
+        if (pst != HGEMM_OK) return pst;
+        p->okA = A;
+        p->okB = B;
+    }
     if (in_bytes(p->din) == 2 &&
         ((reinterpret_cast<uintptr_t>(A) & 1) || (reinterpret_cast<uintptr_t>(B) & 1)))
         return fail(HGEMM_ERR_INVALID_ARG, "A or B is not element-aligned");
@@ -1402,6 +1416,23 @@ int pick_skinny_nb(int64_t N, int64_t batch, int num_sms) {
 }
 
 hgemm_status_t set_error_detail(hgemm_status_t s, const char *msg) { return fail(s, "%s", msg); }
+
+hgemm_status_t check_device_pointer(const void *ptr, int device, const char *what) {
+    cudaPointerAttributes a{};
+    cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // the query's error is not the caller's
+        return fail(HGEMM_ERR_INVALID_ARG, "%s (%p) is not a pointer CUDA knows: %s", what, ptr,
+                    cudaGetErrorString(e));
+    }
+    if (a.type == cudaMemoryTypeManaged) return HGEMM_OK;
+    if (a.type == cudaMemoryTypeDevice && a.device == device) return HGEMM_OK;
+    if (a.type == cudaMemoryTypeDevice)
+        return fail(HGEMM_ERR_INVALID_ARG, "%s (%p) is memory of device %d, not of the plan's device %d",
+                    what, ptr, a.device, device);
+    return fail(HGEMM_ERR_INVALID_ARG, "%s (%p) is host memory; device pointers are required "
+                "(hgemm_run_host takes host buffers)", what, ptr);
+}
 
 hgemm_status_t status_from_error_word(int32_t word) {
     if (word == 0) return HGEMM_OK;

@@ -47,6 +47,8 @@ struct hgemm_attn_plan_s {
     int32_t *err = nullptr;  // device error word (256 B)
     // host-buffer staging
     char *dQ = nullptr, *dK = nullptr, *dV = nullptr, *dO = nullptr;
+    // the last Q, K, V, O that passed check_device_pointer
+    const void *okQ = nullptr, *okK = nullptr, *okV = nullptr, *okO = nullptr;
     // tensor-map cache
     const void *mQ = nullptr, *mK = nullptr, *mV = nullptr;
     bool maps_ok = false;
@@ -67,12 +69,24 @@ hgemm_status_t attn_run(hgemm_attn_plan_s *p, const void *Q, const void *K, cons
     if (cur != p->device)
         return afail(HGEMM_ERR_INVALID_ARG, "plan was created on device %d but device %d is current",
                      p->device, cur);
+    if (O != p->okO) {  // checked once per pointer
+        hgemm_status_t st = hg::check_device_pointer(O, p->device, "O");
+        if (st != HGEMM_OK) return st;
+        p->okO = O;
+    }
     cudaError_t e;
     if (p->skv == 0) {  // the empty sum
         e = hg::launch_zero_fill(O, p->d, 0, p->bh * p->sq, p->d, 1, 2, p->num_sms, s);
         return e == cudaSuccess ? HGEMM_OK : acuda(e, "zero-fill launch");
     }
     if (!Q || !K || !V) return afail(HGEMM_ERR_INVALID_ARG, "Q, K or V is NULL");
+    if (!(Q == p->okQ && K == p->okK && V == p->okV)) {  // once per pointer set
+        hgemm_status_t st = hg::check_device_pointer(Q, p->device, "Q");
+        if (st == HGEMM_OK) st = hg::check_device_pointer(K, p->device, "K");
+        if (st == HGEMM_OK) st = hg::check_device_pointer(V, p->device, "V");
+        if (st != HGEMM_OK) return st;
+        p->okQ = Q; p->okK = K; p->okV = V;
+    }
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V))
         return afail(HGEMM_ERR_INVALID_ARG, "Q, K and V must be 16-byte aligned");
     const int bf = p->dt == HGEMM_BF16 ? 1 : 0;

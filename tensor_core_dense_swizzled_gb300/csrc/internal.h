@@ -35,4 +35,10 @@ hgemm_status_t set_error_detail(hgemm_status_t s, const char *msg);
 // with the word decoded into hgemm_last_error_detail(); HGEMM_OK for 0.
 hgemm_status_t status_from_error_word(int32_t word);
 
+// HGEMM_OK when `ptr` points into device (or managed) memory that `device`
+// can read with TMA; HGEMM_ERR_INVALID_ARG naming `what` otherwise (host
+// memory, another device's memory, or an address CUDA does not know), so
+// that a wrong pointer is refused on the host instead of faulting the GPU.
+hgemm_status_t check_device_pointer(const void *ptr, int device, const char *what);
+
 }  // namespace hg

@@ -158,12 +158,19 @@ extern "C" hgemm_status_t hgemm_skinny_noalloc(const void *A, const void *B, voi
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int out = dtype_out == HGEMM_F32 ? hg::OUT_F32 : (dtype_out == HGEMM_BF16 ? hg::OUT_BF16 : hg::OUT_F16);
 
+    hgemm_status_t cst = hg::check_device_pointer(C, dev, "C");
+    if (cst != HGEMM_OK) return cst;
     if (K == 0) {  // the empty sum
         e = hg::launch_zero_fill(C, ldc, 0, M, N, 1, ob, sms, s);
         if (e != cudaSuccess) return set_error_detail(HGEMM_ERR_CUDA, cudaGetErrorString(e));
         return HGEMM_OK;
     }
     if (!A || !B) return set_error_detail(HGEMM_ERR_INVALID_ARG, "A or B is NULL");
+    {
+        hgemm_status_t pst = hg::check_device_pointer(A, dev, "A");
+        if (pst == HGEMM_OK) pst = hg::check_device_pointer(B, dev, "B");
+        if (pst != HGEMM_OK) return pst;
+    }
     if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) ||
         (lda * 2) % 16 || (ldb * 2) % 16)
         return set_error_detail(HGEMM_ERR_UNSUPPORTED,
