@@ -181,7 +181,8 @@ struct hgemm_plan_s {
     cudaEvent_t ev_a[kMaxHostChunks] = {}, ev_c[kMaxHostChunks] = {};
     // tensor-map cache
     const void *okA = nullptr, *okB = nullptr;  // the last A, B, C that passed
-    const void *okC = nullptr;                  //   check_device_pointer
+    const void *okC = nullptr;                  //   check_device_pointer, and the
+    const float *okBias = nullptr, *okRow = nullptr, *okCol = nullptr;  // epilogue's vectors
     const void *mA = nullptr, *mB = nullptr;
     void *mC = nullptr;
     bool maps_ok = false;
@@ -1021,6 +1022,22 @@ hgemm_status_t hgemm_run_ex(hgemm_plan_t plan, const void *A, const void *B, voi
         ep.col_scale = epilogue->col_scale;
         ep.act = epilogue->activation;
         ep.on = 1;
+        // the epilogue's vectors are read by the kernels too: device memory
+        // of the plan's GPU, checked once per pointer set
+        if (ep.bias != plan->okBias || ep.row_scale != plan->okRow || ep.col_scale != plan->okCol) {
+            const struct {
+                const float *ptr;
+                const char *name;
+            } vecs[3] = {{ep.bias, "bias"}, {ep.row_scale, "row_scale"}, {ep.col_scale, "col_scale"}};
+            for (const auto &v : vecs) {
+                if (!v.ptr) continue;
+                hgemm_status_t st = hg::check_device_pointer(v.ptr, plan->device, v.name);
+                if (st != HGEMM_OK) return st;
+            }
+            plan->okBias = ep.bias;
+            plan->okRow = ep.row_scale;
+            plan->okCol = ep.col_scale;
+        }
     }
     return plan_run(plan, A, B, C, static_cast<cudaStream_t>(stream), ep);
 }

@@ -117,3 +117,31 @@ def test_no_alloc_refuses_host_operands(dev):
     assert H.hgemm_skinny_noalloc_check() == 0
     Cref, Den = oracle.gemm(bits(A), bits(B), 1, M, N, K, K, N)
     check(dC.cpu().double().numpy()[None], Cref, Den, "f32")
+
+
+def test_fused_epilogue_refuses_host_vectors(dev):
+    """The fused epilogue's bias, row_scale and col_scale are read by the
+    kernels as well: a host vector is refused like a host operand."""
+    import types
+    M, N, K = 128, 256, 128
+    A = inputs.make_random((M, K), "bf16", 99)
+    B = inputs.make_random((K, N), "bf16", 100)
+    dA, dB = A.to(dev), B.to(dev)
+    dC = torch.zeros(M, N, dtype=torch.float32, device=dev)
+    hvec = {"bias": torch.ones(N), "row_scale": torch.ones(M), "col_scale": torch.ones(N)}
+    dvec = {k: v.to(dev) for k, v in hvec.items()}
+    plan = H.hgemm_plan_create(M, N, K, K, N, N, 1, 0, 0, 0, H.HGEMM_BF16, H.HGEMM_F32)
+    try:
+        for name in hvec:
+            ep = types.SimpleNamespace(**{k: (hvec[k] if k == name else dvec[k]) for k in hvec})
+            with pytest.raises(H.HgemmError) as ei:
+                H.hgemm_run_ex(plan, dA, dB, dC, ep)
+            assert ei.value.status == INVALID_ARG and name in str(ei.value) and "host memory" in str(ei.value)
+        torch.cuda.synchronize()
+        H.hgemm_run_ex(plan, dA, dB, dC, types.SimpleNamespace(**dvec))
+        assert H.hgemm_check(plan) == 0
+    finally:
+        H.hgemm_plan_destroy(plan)
+    # all-ones scales and bias: C = A.B + 1
+    Cref, Den = oracle.gemm(bits(A), bits(B), 1, M, N, K, K, N)
+    check((dC.cpu().double().numpy() - 1.0)[None], Cref, Den, "f32")
